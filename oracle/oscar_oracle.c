@@ -18,7 +18,8 @@
  *
  * Conventions fixed by the workload definition where the pages are silent:
  *   - row vectors: x_rot = x · R, so q_rot·k_rot = q·k and o = (sum p v_rot) · R_V^T;
- *   - asymmetric INT2 per group of g channels: lo = c·min, hi = c·max,
+ *   - asymmetric INT2 per group of g channels: lo = c·min, hi = c·max
+ *     (min/max of the group's fp32 values, a signed zero read as +0),
  *     zero = bf16(lo), scale = bf16((hi - lo)/3),
  *     code = clamp(rint((x - zero)/scale), 0, 3) using the STORED bf16 zero/scale,
  *     code 0 when scale == 0;
@@ -107,6 +108,8 @@ void ora_quantize_row(const float *xr, int D, int g, float clip,
             if (xr[i] < mn) mn = xr[i];
             if (xr[i] > mx) mx = xr[i];
         }
+        mn = mn + 0.0f;                       /* a signed zero is read as +0 */
+        mx = mx + 0.0f;
         float lo = clip * mn;                 /* clipped range c·[min, max] */
         float hi = clip * mx;
         float diff = hi - lo;

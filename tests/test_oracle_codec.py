@@ -153,3 +153,12 @@ def test_demote_rows_equals_rotate_then_quantize():
     assert np.array_equal(rot, oracle.rotate_f32(x, R))
     p2, z2, s2 = oracle.quantize_rows(rot, 128, 0.96)
     assert np.array_equal(packed, p2) and np.array_equal(z, z2) and np.array_equal(s, s2)
+
+
+def test_quantizer_signed_zero_min_reads_as_plus_zero():
+    """A group whose minimum is zero gives zero point +0 (0x0000) whichever sign the zeros carry."""
+    for vals in ([-0.0, 0.0, 1.5, 3.0], [0.0, -0.0, 1.5, 3.0], [-0.0, -0.0, 3.0, 1.5]):
+        c, z, s = oracle.quantize_row_codes(np.array(vals, np.float32), 4, 1.0)
+        assert int(z[0]) == 0x0000
+        assert int(s[0]) == 0x3F80                      # (3 - 0)/3 = 1
+        assert list(c) == [0, 0, 2, 3] if vals[2] == 1.5 else True
