@@ -1,0 +1,252 @@
+// C ABI of liboscar.so: argument validation, the device status word, dispatch
+// to the kernels.  Declarations and contracts: include/oscar.h.
+
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "oscar_internal.cuh"
+
+namespace {
+
+thread_local std::string g_last_error = "no error";
+
+oscar_status_t fail(oscar_status_t code, const char *fmt, ...) __attribute__((format(printf, 2, 3)));
+oscar_status_t fail(oscar_status_t code, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return code;
+}
+
+oscar_status_t cuda_status(cudaError_t e, const char *what) {
+    if (e == cudaSuccess) return OSCAR_OK;
+    return fail(OSCAR_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+// Device status word (one per device that loads the library); kernels get its address.
+__device__ int32_t g_device_status;
+
+constexpr int kMaxDevices = 64;
+int32_t *g_status_ptr[kMaxDevices] = {nullptr};
+std::mutex g_status_mu;
+
+int32_t *status_ptr() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+    std::lock_guard<std::mutex> lk(g_status_mu);
+    if (!g_status_ptr[dev]) {
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return nullptr;
+        g_status_ptr[dev] = static_cast<int32_t *>(p);
+    }
+    return g_status_ptr[dev];
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+oscar_status_t check_layout(const oscar_layout_t *L) {
+    if (!L) return fail(OSCAR_ERR_INVALID_ARG, "layout is NULL");
+    if (L->head_dim != 128) return fail(OSCAR_ERR_UNSUPPORTED, "head_dim %d: only 128 is supported", L->head_dim);
+    if (L->n_kv_heads < 1 || L->n_kv_heads > 64)
+        return fail(OSCAR_ERR_UNSUPPORTED, "n_kv_heads %d outside 1..64", L->n_kv_heads);
+    if (L->gqa != 1 && L->gqa != 2 && L->gqa != 4 && L->gqa != 8)
+        return fail(OSCAR_ERR_UNSUPPORTED, "gqa %d: supported 1, 2, 4, 8", L->gqa);
+    if (L->page_size != 16 && L->page_size != 32 && L->page_size != 64)
+        return fail(OSCAR_ERR_UNSUPPORTED, "page_size %d: supported 16, 32, 64", L->page_size);
+    if (L->group != 32 && L->group != 64 && L->group != 128)
+        return fail(OSCAR_ERR_UNSUPPORTED, "group %d: supported 32, 64, 128", L->group);
+    if (L->sink < 0 || L->sink % L->page_size != 0)
+        return fail(OSCAR_ERR_INVALID_ARG, "sink %d must be >= 0 and a multiple of page_size %d", L->sink,
+                    L->page_size);
+    if (L->recent < 0) return fail(OSCAR_ERR_INVALID_ARG, "recent %d < 0", L->recent);
+    return OSCAR_OK;
+}
+
+oscar_status_t check_int2_pool(const oscar_int2_pool_t *p) {
+    if (!p) return fail(OSCAR_ERR_INVALID_ARG, "INT2 pool is NULL");
+    const void *ptrs[6] = {p->codes_k, p->codes_v, p->scale_k, p->zero_k, p->scale_v, p->zero_v};
+    for (const void *q : ptrs) {
+        if (!q) return fail(OSCAR_ERR_INVALID_ARG, "INT2 pool has a NULL array");
+        if (!aligned16(q)) return fail(OSCAR_ERR_INVALID_ARG, "INT2 pool array not 16-byte aligned");
+    }
+    if (p->n_pages < 1) return fail(OSCAR_ERR_INVALID_ARG, "INT2 pool n_pages %d < 1", p->n_pages);
+    return OSCAR_OK;
+}
+
+oscar_status_t check_bf16_pool(const oscar_bf16_pool_t *p) {
+    if (!p) return fail(OSCAR_ERR_INVALID_ARG, "BF16 pool is NULL");
+    if (!p->k || !p->v) return fail(OSCAR_ERR_INVALID_ARG, "BF16 pool has a NULL array");
+    if (!aligned16(p->k) || !aligned16(p->v)) return fail(OSCAR_ERR_INVALID_ARG, "BF16 pool not 16-byte aligned");
+    if (p->n_pages < 1) return fail(OSCAR_ERR_INVALID_ARG, "BF16 pool n_pages %d < 1", p->n_pages);
+    return OSCAR_OK;
+}
+
+oscar_status_t check_partials(const oscar_partials_t *p) {
+    if (!p) return fail(OSCAR_ERR_INVALID_ARG, "partials is NULL");
+    if (!p->m || !p->l || !p->acc) return fail(OSCAR_ERR_INVALID_ARG, "partials has a NULL array");
+    if (!aligned16(p->acc)) return fail(OSCAR_ERR_INVALID_ARG, "partials acc not 16-byte aligned");
+    if (p->n_splits < 1 || p->n_splits > 256)
+        return fail(OSCAR_ERR_INVALID_ARG, "n_splits %d outside 1..256", p->n_splits);
+    return OSCAR_OK;
+}
+
+#define TRY(x)                                \
+    do {                                      \
+        oscar_status_t s_ = (x);              \
+        if (s_ != OSCAR_OK) return s_;        \
+    } while (0)
+
+oscar::Int2PoolView int2_view(const oscar_int2_pool_t *p) {
+    return {p->codes_k, p->codes_v, p->scale_k, p->zero_k, p->scale_v, p->zero_v, p->n_pages};
+}
+oscar::Bf16PoolView bf16_view(const oscar_bf16_pool_t *p) { return {p->k, p->v, p->n_pages}; }
+oscar::PartialsView part_view(const oscar_partials_t *p) { return {p->m, p->l, p->acc, p->n_splits}; }
+
+}  // namespace
+
+extern "C" {
+
+size_t oscar_partials_ml_floats(const oscar_layout_t *L, int32_t batch, int32_t n_splits) {
+    if (!L || batch < 0 || n_splits < 0) return 0;
+    return (size_t)batch * L->n_kv_heads * L->gqa * (size_t)(n_splits + 1);
+}
+
+size_t oscar_partials_acc_floats(const oscar_layout_t *L, int32_t batch, int32_t n_splits) {
+    return oscar_partials_ml_floats(L, batch, n_splits) * (L ? (size_t)L->head_dim : 0);
+}
+
+int32_t oscar_suggest_splits(const oscar_layout_t *L, int32_t batch, int32_t max_hist_tokens, int32_t sm_count) {
+    if (!L || L->page_size <= 0 || batch <= 0 || sm_count <= 0) return 1;
+    const int pages = (max_hist_tokens + L->page_size - 1) / L->page_size;
+    long want = (2L * sm_count + (long)batch * L->n_kv_heads - 1) / ((long)batch * L->n_kv_heads);
+    if (want > pages) want = pages;
+    if (want < 1) want = 1;
+    if (want > 256) want = 256;
+    return (int32_t)want;
+}
+
+oscar_status_t oscar_demote(const oscar_layout_t *layout, const oscar_bf16_pool_t *src,
+                            const int32_t *bf16_page_table, const oscar_int2_pool_t *dst,
+                            const int32_t *int2_page_table, int32_t max_pages_per_req, int32_t batch,
+                            const int32_t *req_idx,
+                            const int32_t *positions, int32_t n, const float *R_K, const float *R_V, float c_K,
+                            float c_V, float *rotated_out, void *stream) {
+    TRY(check_layout(layout));
+    TRY(check_bf16_pool(src));
+    TRY(check_int2_pool(dst));
+    if (n < 0 || n > 65535 * 256) return fail(OSCAR_ERR_INVALID_ARG, "n %d outside 0..%d", n, 65535 * 256);
+    if (n == 0) return OSCAR_OK;
+    if (!bf16_page_table || !int2_page_table || !req_idx || !positions || !R_K || !R_V)
+        return fail(OSCAR_ERR_INVALID_ARG, "NULL page table, index or rotation");
+    if (max_pages_per_req < 1) return fail(OSCAR_ERR_INVALID_ARG, "max_pages_per_req %d < 1", max_pages_per_req);
+    if (batch < 1) return fail(OSCAR_ERR_INVALID_ARG, "batch %d < 1", batch);
+    if (!aligned16(R_K) || !aligned16(R_V)) return fail(OSCAR_ERR_INVALID_ARG, "R_K/R_V not 16-byte aligned");
+    if (!(c_K > 0.0f) || !(c_V > 0.0f)) return fail(OSCAR_ERR_INVALID_ARG, "clip ratios must be > 0");
+    return cuda_status(oscar::launch_demote(*layout, bf16_view(src), bf16_page_table, *dst, int2_page_table,
+                                            max_pages_per_req, batch, req_idx, positions, n, R_K, R_V, c_K, c_V,
+                                            rotated_out, status_ptr(), (cudaStream_t)stream),
+                       "oscar_demote launch");
+}
+
+oscar_status_t oscar_quantize_rotated(const oscar_layout_t *layout, const float *x_rot, int32_t n, float clip,
+                                      uint8_t *codes, uint16_t *scale, uint16_t *zero, void *stream) {
+    TRY(check_layout(layout));
+    if (n < 0 || n > 2147483647 / 128) return fail(OSCAR_ERR_INVALID_ARG, "n %d out of range", n);
+    if (n == 0) return OSCAR_OK;
+    if (!x_rot || !codes || !scale || !zero) return fail(OSCAR_ERR_INVALID_ARG, "NULL argument");
+    if (!(clip > 0.0f)) return fail(OSCAR_ERR_INVALID_ARG, "clip must be > 0");
+    return cuda_status(oscar::launch_quantize_rotated(*layout, x_rot, n, clip, codes, scale, zero,
+                                                      (cudaStream_t)stream),
+                       "oscar_quantize_rotated launch");
+}
+
+oscar_status_t oscar_rotate_q(const oscar_layout_t *layout, const uint16_t *q, const float *R_K, int32_t batch,
+                              float *q_rot, void *stream) {
+    TRY(check_layout(layout));
+    if (batch < 0) return fail(OSCAR_ERR_INVALID_ARG, "batch %d < 0", batch);
+    if (batch == 0) return OSCAR_OK;
+    if (!q || !R_K || !q_rot) return fail(OSCAR_ERR_INVALID_ARG, "NULL argument");
+    return cuda_status(oscar::launch_rotate_q(*layout, q, R_K, batch, q_rot, (cudaStream_t)stream),
+                       "oscar_rotate_q launch");
+}
+
+oscar_status_t oscar_decode_attention(const oscar_layout_t *layout, const uint16_t *q, const float *q_rot,
+                                      const oscar_bf16_pool_t *bf16_pool, const int32_t *bf16_page_table,
+                                      const oscar_int2_pool_t *int2_pool, const int32_t *int2_page_table,
+                                      int32_t max_pages_per_req, const int32_t *seq_len, const int32_t *hist_end,
+                                      int32_t batch, float sm_scale, const oscar_partials_t *partials,
+                                      void *stream) {
+    TRY(check_layout(layout));
+    TRY(check_bf16_pool(bf16_pool));
+    TRY(check_int2_pool(int2_pool));
+    TRY(check_partials(partials));
+    if (batch < 0) return fail(OSCAR_ERR_INVALID_ARG, "batch %d < 0", batch);
+    if (batch == 0) return OSCAR_OK;
+    if (!q || !q_rot || !bf16_page_table || !int2_page_table || !seq_len || !hist_end)
+        return fail(OSCAR_ERR_INVALID_ARG, "NULL argument");
+    if (!aligned16(q_rot) || !aligned16(q)) return fail(OSCAR_ERR_INVALID_ARG, "q/q_rot not 16-byte aligned");
+    if (max_pages_per_req < 1) return fail(OSCAR_ERR_INVALID_ARG, "max_pages_per_req %d < 1", max_pages_per_req);
+    if (batch > 65535) return fail(OSCAR_ERR_INVALID_ARG, "batch %d > 65535", batch);
+    int32_t *st = status_ptr();
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = oscar::launch_int2_attention(*layout, q_rot, int2_view(int2_pool), int2_page_table,
+                                                 max_pages_per_req, seq_len, hist_end, batch, sm_scale,
+                                                 part_view(partials), st, s);
+    if (e != cudaSuccess) return cuda_status(e, "INT2 attention launch");
+    e = oscar::launch_bf16_attention(*layout, q, bf16_view(bf16_pool), bf16_page_table, max_pages_per_req,
+                                     seq_len, hist_end, batch, sm_scale, part_view(partials), 0, st, s);
+    return cuda_status(e, "BF16 sink/recent attention launch");
+}
+
+oscar_status_t oscar_merge(const oscar_layout_t *layout, const oscar_partials_t *partials, const float *R_V,
+                           int32_t batch, uint16_t *out, float *out_f32, float *lse, void *stream) {
+    TRY(check_layout(layout));
+    TRY(check_partials(partials));
+    if (batch < 0 || batch > 65535) return fail(OSCAR_ERR_INVALID_ARG, "batch %d outside 0..65535", batch);
+    if (batch == 0) return OSCAR_OK;
+    if (!out && !out_f32) return fail(OSCAR_ERR_INVALID_ARG, "out and out_f32 are both NULL");
+    return cuda_status(oscar::launch_merge(*layout, part_view(partials), R_V, batch, out, out_f32, lse,
+                                           (cudaStream_t)stream),
+                       "oscar_merge launch");
+}
+
+oscar_status_t oscar_bf16_decode_attention(const oscar_layout_t *layout, const uint16_t *q,
+                                           const oscar_bf16_pool_t *pool, const int32_t *page_table,
+                                           int32_t max_pages_per_req, const int32_t *seq_len, int32_t batch,
+                                           float sm_scale, const oscar_partials_t *partials, void *stream) {
+    TRY(check_layout(layout));
+    TRY(check_bf16_pool(pool));
+    TRY(check_partials(partials));
+    if (batch < 0 || batch > 65535) return fail(OSCAR_ERR_INVALID_ARG, "batch %d outside 0..65535", batch);
+    if (batch == 0) return OSCAR_OK;
+    if (!q || !page_table || !seq_len) return fail(OSCAR_ERR_INVALID_ARG, "NULL argument");
+    if (max_pages_per_req < 1) return fail(OSCAR_ERR_INVALID_ARG, "max_pages_per_req %d < 1", max_pages_per_req);
+    return cuda_status(oscar::launch_bf16_attention(*layout, q, bf16_view(pool), page_table, max_pages_per_req,
+                                                    seq_len, nullptr, batch, sm_scale, part_view(partials), 1,
+                                                    status_ptr(), (cudaStream_t)stream),
+                       "BF16 attention launch");
+}
+
+oscar_status_t oscar_get_device_status(int32_t *status_bits, void *stream) {
+    if (!status_bits) return fail(OSCAR_ERR_INVALID_ARG, "status_bits is NULL");
+    int32_t *p = status_ptr();
+    if (!p) return fail(OSCAR_ERR_CUDA, "device status word unavailable");
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaMemcpyAsync(status_bits, p, sizeof(int32_t), cudaMemcpyDeviceToHost, s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(p, 0, sizeof(int32_t), s);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    return cuda_status(e, "reading device status");
+}
+
+const char *oscar_last_error_string(void) { return g_last_error.c_str(); }
+
+const char *oscar_version(void) { return "0.1.0"; }
+
+}  // extern "C"

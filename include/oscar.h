@@ -1,0 +1,265 @@
+/*
+ * oscar.h — C ABI of liboscar.so, the GB300 (sm_103a) implementation of the
+ * OSCAR INT2 KV-cache decode path.
+ *
+ * The method (cited by page title and section):
+ *   [news]  OSCAR news article (m.kljzs.com mirror), paragraph on the online
+ *           path: sink and recent tokens stay BF16, the long middle history is
+ *           rotated INT2; the oldest recent token is rotated, clipped,
+ *           quantized and packed (4 codes per byte) into the INT2 history; at
+ *           decode an INT2 kernel (unpack, scale/zero restore, float
+ *           accumulation) and a BF16 kernel (sink/recent) produce partial
+ *           results that an online-softmax merge combines.
+ *   [tai]   "Together AI 開源 OSCAR" (news.chathome.org), "OSCAR 的不同之處":
+ *           R_K = U_Q·H·P_br, R_V = U_S·H·P_br; "服務系統": first 64 tokens and
+ *           last 256 tokens in BF16, paged-attention compatible.
+ *   [notes] "OSCAR — 离线转个方向，把 KV Cache 压到 2-bit" (estelledc notes),
+ *           "核心要点" item 3: layout [BF16 sink] || [INT2 history] || [BF16
+ *           recent]; "案例 2": c_K ~ 0.96, c_V ~ 0.92.
+ *
+ * Conventions (row vectors): x_rot = x · R.  Keys/values in the INT2 history
+ * are stored rotated; a query is rotated by its kv head's R_K before it meets
+ * them (q_rot · k_rot = q · k), and the history part of the output is rotated
+ * back by R_V^T.  INT2 is asymmetric per group of `group` consecutive rotated
+ * channels: lo = c·min, hi = c·max, zero = bf16(lo), scale = bf16((hi-lo)/3),
+ * code = clamp(rint((x - zero)/scale), 0, 3), code 0 if scale == 0; code i of
+ * a row sits at bits 2·(i mod 4) of byte i/4.  Dequantized value:
+ * zero + code·scale.
+ *
+ * Regions of a request with seq_len T (current token included) and history
+ * end h (sink <= h <= T): positions [0, sink) and [h, T) are read from the
+ * BF16 pool, positions [sink, h) from the INT2 pool.  h is passed per call so
+ * that a demotion of position h may run concurrently with attention that
+ * still reads it from BF16.
+ *
+ * Memory: every pointer is a device pointer owned by the caller, except the
+ * layout/pool/partials descriptors themselves, which are host structs read
+ * during the call only.  The library allocates no memory on any call below.
+ * Every call is asynchronous on the CUDA stream passed as `stream`
+ * (a cudaStream_t; NULL = legacy default stream) and returns after enqueueing.
+ *
+ * Errors: host-side argument checks return OSCAR_ERR_INVALID_ARG or
+ * OSCAR_ERR_UNSUPPORTED before anything is enqueued; a failed launch returns
+ * OSCAR_ERR_CUDA.  oscar_last_error_string() gives a one-line reason (thread
+ * local).  Device-side checks (page ids outside [0, n_pages), seq_len or
+ * hist_end out of range, a pipeline wait that gave up) never trap: the
+ * offending page/request is skipped, a bit is set in a device status word,
+ * and oscar_get_device_status() reads and clears it.
+ */
+#ifndef OSCAR_H
+#define OSCAR_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define OSCAR_API __attribute__((visibility("default")))
+#else
+#define OSCAR_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    OSCAR_OK = 0,
+    OSCAR_ERR_INVALID_ARG = 1,
+    OSCAR_ERR_UNSUPPORTED = 2,
+    OSCAR_ERR_CUDA = 3,
+    OSCAR_ERR_DEVICE_FLAG = 4
+} oscar_status_t;
+
+/* Device status bits reported by oscar_get_device_status(). */
+#define OSCAR_DEV_BAD_INT2_PAGE 0x1   /* INT2 page id outside [0, n_pages) */
+#define OSCAR_DEV_BAD_BF16_PAGE 0x2   /* BF16 page id outside [0, n_pages) */
+#define OSCAR_DEV_BAD_LENGTH    0x4   /* seq_len/hist_end/position out of range (clamped) */
+#define OSCAR_DEV_WAIT_TIMEOUT  0x8   /* a bounded pipeline wait gave up */
+
+/*
+ * Model/cache shape shared by every call.
+ *   head_dim   D, must be 128.
+ *   n_kv_heads Hkv, 1..64.
+ *   gqa        G = query heads per kv head, one of 1, 2, 4, 8 (Hq = G·Hkv).
+ *   page_size  tokens per page: 16, 32 or 64, and sink % page_size == 0.
+ *   group      INT2 quantization group along the rotated channels: 32, 64, 128.
+ *   sink       BF16 sink tokens ([tai] "服務系統": 64).
+ *   recent     BF16 recent tokens ([tai] "服務系統": 256); informative only,
+ *              the per-request hist_end decides the regions.
+ */
+typedef struct {
+    int32_t head_dim;
+    int32_t n_kv_heads;
+    int32_t gqa;
+    int32_t page_size;
+    int32_t group;
+    int32_t sink;
+    int32_t recent;
+} oscar_layout_t;
+
+/*
+ * Paged INT2 pool of one layer (device memory, caller-owned):
+ *   codes_k, codes_v : uint8 [n_pages][page_size][n_kv_heads][head_dim/4]
+ *   scale_k, zero_k, scale_v, zero_v : bf16 bits [n_pages][page_size][n_kv_heads][head_dim/group]
+ * All six base addresses must be 16-byte aligned.
+ */
+typedef struct {
+    uint8_t *codes_k;
+    uint8_t *codes_v;
+    uint16_t *scale_k;
+    uint16_t *zero_k;
+    uint16_t *scale_v;
+    uint16_t *zero_v;
+    int32_t n_pages;
+} oscar_int2_pool_t;
+
+/* Paged BF16 pool of one layer: k, v bf16 bits [n_pages][page_size][n_kv_heads][head_dim], 16-byte aligned. */
+typedef struct {
+    uint16_t *k;
+    uint16_t *v;
+    int32_t n_pages;
+} oscar_bf16_pool_t;
+
+/*
+ * Flash-decoding partials (device scratch, caller-owned), base-2 domain:
+ *   m   fp32 [batch][Hq][n_splits + 1]   running max of sm_scale·logit·log2(e)
+ *   l   fp32 [batch][Hq][n_splits + 1]   sum of 2^(t - m)
+ *   acc fp32 [batch][Hq][n_splits + 1][head_dim]  sum of 2^(t - m)·value
+ * Slots 0..n_splits-1 are history splits in ascending token order (values in
+ * the ROTATED basis); slot n_splits is the BF16 partial (unrotated).  An empty
+ * slot has m = -inf, l = 0, acc = 0.  n_splits in 1..256.
+ */
+typedef struct {
+    float *m;
+    float *l;
+    float *acc;
+    int32_t n_splits;
+} oscar_partials_t;
+
+/* Number of floats in m, l and acc for a batch (sizes for the caller's allocation). */
+OSCAR_API size_t oscar_partials_ml_floats(const oscar_layout_t *layout, int32_t batch, int32_t n_splits);
+OSCAR_API size_t oscar_partials_acc_floats(const oscar_layout_t *layout, int32_t batch, int32_t n_splits);
+
+/*
+ * A split count that fills the GPU for `batch` requests whose longest history
+ * spans max_hist_tokens tokens: about two waves of CTAs over `sm_count` SMs,
+ * at least one history page per split, clamped to [1, 256].
+ */
+OSCAR_API int32_t oscar_suggest_splits(const oscar_layout_t *layout, int32_t batch, int32_t max_hist_tokens,
+                             int32_t sm_count);
+
+/*
+ * Demotion ([news] online path: "rotate / clip / quantize / pack"; [notes]
+ * "核心要点" item 3).  For each i < n, request b = req_idx[i] and position
+ * p = positions[i]: for every kv head h, the BF16 key row at
+ * (bf16_page_table[b·max_pages_per_req + p/ps], p % ps, h) is rotated by
+ * R_K[h] (fp32 accumulation, one fused multiply-add per term in ascending
+ * input-channel order), clipped with c_K, quantized and packed into the INT2
+ * pool at (int2_page_table[b·max_pages_per_req + p/ps], p % ps, h); the value
+ * row likewise with R_V[h] and c_V.
+ *   R_K, R_V       fp32 [n_kv_heads][head_dim][head_dim], row-major R[i][j].
+ *   batch          rows of both page tables ([batch][max_pages_per_req]).
+ *   req_idx, positions  int32 [n] device arrays; an entry with req_idx outside
+ *                  [0, batch) or a position outside the page table is skipped
+ *                  and flagged (OSCAR_DEV_BAD_LENGTH).
+ *   rotated_out    NULL or fp32 [n][2][n_kv_heads][head_dim]: the rotated
+ *                  rows (index 0 = K, 1 = V) before quantization.
+ * n may be large (bulk demotion of a whole prompt); n = 0 is a no-op.
+ * Rows that two entries of (req_idx, positions) map to the same INT2 slot
+ * race; callers demote each position once.
+ */
+OSCAR_API oscar_status_t oscar_demote(const oscar_layout_t *layout,
+                            const oscar_bf16_pool_t *src, const int32_t *bf16_page_table,
+                            const oscar_int2_pool_t *dst, const int32_t *int2_page_table,
+                            int32_t max_pages_per_req, int32_t batch,
+                            const int32_t *req_idx, const int32_t *positions, int32_t n,
+                            const float *R_K, const float *R_V, float c_K, float c_V,
+                            float *rotated_out, void *stream);
+
+/*
+ * The codec alone: quantize n fp32 rows x_rot [n][head_dim] that are already
+ * rotated, with clip ratio `clip`, into codes [n][head_dim/4] and bf16
+ * scale/zero [n][head_dim/group].  Bit-exact contract: given the same fp32
+ * input rows, codes, scale and zero equal the definition above bit for bit.
+ */
+OSCAR_API oscar_status_t oscar_quantize_rotated(const oscar_layout_t *layout, const float *x_rot, int32_t n,
+                                      float clip, uint8_t *codes, uint16_t *scale, uint16_t *zero,
+                                      void *stream);
+
+/*
+ * Query rotation q_rot = q · R_K[h / gqa] for every query head h of every
+ * request ("q pre-rotated by R_K" so that q_rot · k_rot = q · k, [tai]
+ * "OSCAR 的不同之處").  q: bf16 [batch][Hq][head_dim]; q_rot: fp32, same shape;
+ * fp32 fused multiply-add chain in ascending input-channel order.
+ */
+OSCAR_API oscar_status_t oscar_rotate_q(const oscar_layout_t *layout, const uint16_t *q, const float *R_K,
+                              int32_t batch, float *q_rot, void *stream);
+
+/*
+ * Decode attention partials for one layer ([news] INT2 kernel + BF16 kernel).
+ *   q        bf16 [batch][Hq][head_dim], unrotated (meets the BF16 rows)
+ *   q_rot    fp32 [batch][Hq][head_dim] = q · R_K (meets the INT2 history)
+ *   bf16_pool / bf16_page_table   sink and recent rows
+ *   int2_pool / int2_page_table   history rows
+ *   page tables: int32 [batch][max_pages_per_req], logical page -> physical page
+ *   seq_len  int32 [batch] T (current token included), 1 <= T <= max_pages_per_req·page_size
+ *   hist_end int32 [batch] h, sink <= h <= T (values outside are clamped and flagged)
+ *   sm_scale softmax scale (1/sqrt(head_dim) for standard attention)
+ * Writes every slot of `partials` for every (request, query head):
+ * history [sink, h) cut into partials->n_splits page-aligned splits of
+ * ceil(pages / n_splits) pages, and the BF16 partial over [0, sink) ∪ [h, T).
+ */
+OSCAR_API oscar_status_t oscar_decode_attention(const oscar_layout_t *layout,
+                                      const uint16_t *q, const float *q_rot,
+                                      const oscar_bf16_pool_t *bf16_pool, const int32_t *bf16_page_table,
+                                      const oscar_int2_pool_t *int2_pool, const int32_t *int2_page_table,
+                                      int32_t max_pages_per_req,
+                                      const int32_t *seq_len, const int32_t *hist_end, int32_t batch,
+                                      float sm_scale, const oscar_partials_t *partials, void *stream);
+
+/*
+ * Online-softmax merge ([news] "online softmax merge"): per (request, query
+ * head), fold history slots 0..S-1 in ascending order, rotate that
+ * accumulator back by R_V[h / gqa]^T, fold the BF16 slot S, divide by the
+ * total weight.  The fold is the ordered fp32 sequence
+ *   M' = max(M, m_i); a = 2^(M - M'); b = 2^(m_i - M');
+ *   L = fma(L, a, l_i·b); A_d = fma(A_d, a, acc_i,d·b)
+ * with 2^x computed by Cody–Waite reduction and a degree-7 Taylor polynomial
+ * (not the hardware approximation), so that equal partials give equal bits.
+ *   R_V  fp32 [n_kv_heads][head_dim][head_dim], or NULL for an all-BF16
+ *        cache (then no slot is rotated).
+ *   out      NULL or bf16 [batch][Hq][head_dim]: o rounded to nearest even.
+ *   out_f32  NULL or fp32 [batch][Hq][head_dim]: o before that rounding.
+ *            At least one of out / out_f32 must be given.
+ *   lse      NULL or fp32 [batch][Hq]: natural log-sum-exp of sm_scale·logits.
+ */
+OSCAR_API oscar_status_t oscar_merge(const oscar_layout_t *layout, const oscar_partials_t *partials,
+                           const float *R_V, int32_t batch, uint16_t *out, float *out_f32, float *lse,
+                           void *stream);
+
+/*
+ * Comparison kernel: decode attention over an all-BF16 paged cache (no INT2
+ * history, no rotation), same split-K structure.  Positions [0, T) are cut
+ * into partials->n_splits page-aligned splits written to slots 0..S-1; slot
+ * S is written empty.  Merge with oscar_merge(..., R_V = NULL, ...).
+ */
+OSCAR_API oscar_status_t oscar_bf16_decode_attention(const oscar_layout_t *layout, const uint16_t *q,
+                                           const oscar_bf16_pool_t *pool, const int32_t *page_table,
+                                           int32_t max_pages_per_req, const int32_t *seq_len,
+                                           int32_t batch, float sm_scale,
+                                           const oscar_partials_t *partials, void *stream);
+
+/* Read and clear the device status word of the current device (synchronizes `stream`). */
+OSCAR_API oscar_status_t oscar_get_device_status(int32_t *status_bits, void *stream);
+
+/* One-line reason for the last non-OK status returned on this thread. */
+OSCAR_API const char *oscar_last_error_string(void);
+
+/* Library version, e.g. "0.1.0". */
+OSCAR_API const char *oscar_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* OSCAR_H */

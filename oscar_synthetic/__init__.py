@@ -190,10 +190,11 @@ class PageLayout:
     n_int2_pages: int
     n_bf16_pages: int
     seq_len: np.ndarray      # int32 [B]
-    hist_end: np.ndarray     # int32 [B]  (context - recent, at least sink)
+    hist_end: np.ndarray     # int32 [B]  (context - recent, clamped to [min(sink, context), context])
 
 
-def page_layout(w: Workload, seq_len: Sequence[int], bf16_slack: int = 1, shuffle: bool = True) -> PageLayout:
+def page_layout(w: Workload, seq_len: Sequence[int], bf16_slack: int = 1, shuffle: bool = True,
+                hist_end: Optional[Sequence[int]] = None) -> PageLayout:
     ps = w.page_size
     B = len(seq_len)
     max_pages = max((t + ps - 1) // ps for t in seq_len)
@@ -201,7 +202,9 @@ def page_layout(w: Workload, seq_len: Sequence[int], bf16_slack: int = 1, shuffl
     bf = -np.ones((B, max_pages), dtype=np.int32)
     n_int2 = n_bf = 0
     shared_pages = w.shared_prefix // ps
-    hist_end = np.array([max(w.sink, t - w.recent) for t in seq_len], dtype=np.int32)
+    if hist_end is None:
+        hist_end = [min(t, max(w.sink, t - w.recent)) for t in seq_len]
+    hist_end = np.asarray(hist_end, dtype=np.int32)
     for b, t in enumerate(seq_len):
         n_log = (t + ps - 1) // ps
         for lp in range(n_log):

@@ -1,0 +1,247 @@
+"""CUDA path vs the oracle, through the C ABI (liboscar.so).
+
+Bars: codes / scale / zero / rotated rows / q_rot / merge bit-exact; attention
+outputs (fp32, before the bf16 rounding) within relative L2 1e-3 and
+max |err| <= 2e-3 * max |o_ref|; the bf16 output equal to the round-to-nearest-
+even of the fp32 one.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import oscar_synthetic as syn
+from bit_kv_cache_oscar_gb300 import binding as ob
+from tests import scenario as sc
+from tests.helpers import bf16_bits
+
+pytestmark = pytest.mark.gpu
+D = 128
+
+
+@pytest.mark.parametrize("group", [32, 64, 128])
+@pytest.mark.parametrize("clip", [1.0, 0.96, 0.92])
+def test_quantize_rotated_bit_exact(group, clip):
+    x = syn.rotated_rows(7, 300)
+    x[3, :] = 0.0
+    x[4, ::3] = -0.0
+    x[5] = np.float32(np.round(x[5] * 4) / 4)             # many values on a coarse grid: exact ties
+    L = ob.Layout(1, 1, 16, group)
+    xd = torch.from_numpy(x).cuda()
+    codes = torch.empty((300, D // 4), dtype=torch.uint8, device="cuda")
+    scale = torch.empty((300, D // group), dtype=torch.bfloat16, device="cuda")
+    zero = torch.empty_like(scale)
+    ob.oscar_quantize_rotated(L, xd, clip, codes, scale, zero)
+    torch.cuda.synchronize()
+    p, z, s = oracle.quantize_rows(x, group, clip)
+    assert np.array_equal(codes.cpu().numpy(), p)
+    assert np.array_equal(bf16_bits(scale), s)
+    assert np.array_equal(bf16_bits(zero), z)
+
+
+def test_rotate_q_bit_exact():
+    case = sc.make_case(n_kv=2, gqa=4, seq=(500, 300))
+    sc.upload(case, demote_history=False)
+    L = case.layout
+    q_rot = torch.empty((2, L.n_q_heads, D), dtype=torch.float32, device="cuda")
+    ob.oscar_rotate_q(L, case.dev["q"], case.dev["RK"], q_rot)
+    torch.cuda.synchronize()
+    qb = bf16_bits(case.q)
+    got = q_rot.cpu().numpy()
+    for b in range(2):
+        for hq in range(L.n_q_heads):
+            ref = oracle.rotate_f32(qb[b, hq][None], case.RK[hq // L.gqa])[0]
+            assert np.array_equal(got[b, hq], ref)
+
+
+@pytest.mark.parametrize("group,page_size", [(128, 16), (32, 64)])
+def test_demote_bit_exact(group, page_size):
+    case = sc.make_case(n_kv=2, gqa=4, page_size=page_size, group=group, seq=(1024, 777))
+    dev = sc.upload(case)
+    torch.cuda.synchronize()
+    rot = dev["rotated"].cpu().numpy()
+    req = dev["demote_req"].cpu().numpy()
+    pos = dev["demote_pos"].cpu().numpy()
+    L = case.layout
+    for b in range(2):
+        he = int(case.hist_end[b])
+        sel = np.flatnonzero(req == b)
+        assert list(pos[sel]) == list(range(L.sink, he))
+        for h in range(L.n_kv_heads):
+            kb = bf16_bits(case.K[b][L.sink:he, h])
+            vb = bf16_bits(case.V[b][L.sink:he, h])
+            rk, pk, zk, sk = oracle.demote_rows(kb, case.RK[h], group, oracle.C_K)
+            rv, pv, zv, sv = oracle.demote_rows(vb, case.RV[h], group, oracle.C_V)
+            assert np.array_equal(rot[sel, 0, h], rk)
+            assert np.array_equal(rot[sel, 1, h], rv)
+            ck, cv, gzk, gsk, gzv, gsv = sc.gather_int2(case, b, h)
+            assert np.array_equal(ck[L.sink:he], pk)
+            assert np.array_equal(cv[L.sink:he], pv)
+            assert np.array_equal(gzk[L.sink:he], zk) and np.array_equal(gsk[L.sink:he], sk)
+            assert np.array_equal(gzv[L.sink:he], zv) and np.array_equal(gsv[L.sink:he], sv)
+
+
+def _check_outputs(case, out, out32, lse, pairs=None):
+    ref = sc.oracle_outputs(case, pairs)
+    o32 = out32.cpu().numpy()
+    ob16 = bf16_bits(out)
+    lse_g = lse.cpu().numpy()
+    got = np.stack([o32[b, hq] for (b, hq) in ref])
+    exp = np.stack([ref[k][0] for k in ref])
+    ok, r, m = sc.tolerance_ok(got, exp)
+    assert ok, f"rel-L2 {r:.3e}, max-abs frac {m:.3e}"
+    for (b, hq), (o, l) in ref.items():
+        one_ok, r1, m1 = sc.tolerance_ok(o32[b, hq], o)
+        assert one_ok, f"head {(b, hq)}: rel-L2 {r1:.3e}, max-abs {m1:.3e}"
+        assert abs(lse_g[b, hq] - l) <= 1e-4 * max(1.0, abs(l))
+        assert np.array_equal(ob16[b, hq], oracle.f32_to_bf16(o32[b, hq]))
+
+
+@pytest.mark.parametrize("n_splits", [1, 3, 16])
+def test_decode_tiny_parity(n_splits):
+    """1 layer, 8 q / 2 kv heads, 1,024 tokens = 64 sink + 704 history + 256 recent, 16-token pages."""
+    case = sc.make_case(n_kv=2, gqa=4, page_size=16, seq=(1024,))
+    sc.upload(case)
+    out, out32, lse, _ = sc.run_decode(case, n_splits)
+    _check_outputs(case, out, out32, lse)
+    assert ob.oscar_get_device_status() == 0
+
+
+def test_partials_per_split_match_oracle():
+    """Each split's (m, l, acc) against the oracle's fp64 partial over the documented page-aligned range."""
+    S = 5
+    case = sc.make_case(n_kv=2, gqa=4, page_size=16, seq=(1024, 613))
+    sc.upload(case)
+    _, _, _, part = sc.run_decode(case, S)
+    L = case.layout
+    m, l, acc = part.m.cpu().numpy(), part.l.cpu().numpy(), part.acc.cpu().numpy()
+    qb = bf16_bits(case.q)
+    for b, T in enumerate(case.seq):
+        he = int(case.hist_end[b])
+        first, last = L.sink // L.page_size, -(-he // L.page_size)
+        per = -(-(last - first) // S)
+        for h in range(L.n_kv_heads):
+            cache = sc.oracle_head_cache(case, b, h)
+            for g in range(L.gqa):
+                hq = h * L.gqa + g
+                for s in range(S + 1):
+                    if s < S:
+                        lo = max(L.sink, (first + s * per) * L.page_size)
+                        hi = min(he, (first + (s + 1) * per) * L.page_size)
+                        ranges = [(lo, hi)] if lo < hi else []
+                    else:
+                        ranges = [(0, L.sink), (he, T)]
+                    rm, rl, racc = oracle.partial(qb[b, hq], case.RK[h], cache, case.sm_scale, ranges)
+                    if rl == 0.0:
+                        assert m[b, hq, s] == -np.inf and l[b, hq, s] == 0.0 and not acc[b, hq, s].any()
+                        continue
+                    assert abs(m[b, hq, s] - rm) <= 1e-4 * max(1.0, abs(rm))
+                    assert abs(l[b, hq, s] - rl) <= 1e-4 * rl
+                    err = np.linalg.norm(acc[b, hq, s] - racc) / np.linalg.norm(racc)
+                    assert err <= 1e-4, (b, hq, s, err)
+
+
+@pytest.mark.parametrize("S,empty", [(1, ()), (7, (2, 3)), (64, (0, 63)), (5, (5,))])
+def test_merge_bit_exact(S, empty):
+    """Equal partials -> equal bits: the merge against the oracle's ordered fp32 fold."""
+    L = ob.Layout(2, 4, 16)
+    B = 2
+    part = ob.Partials.empty(L, B, S)
+    m = np.empty((B, L.n_q_heads, S + 1), np.float32)
+    l = np.empty_like(m)
+    acc = np.empty((B, L.n_q_heads, S + 1, D), np.float32)
+    for b in range(B):
+        for hq in range(L.n_q_heads):
+            m[b, hq], l[b, hq], acc[b, hq] = syn.split_partials(1000 * b + hq + 17 * S, S, D, empty)
+    part.m.copy_(torch.from_numpy(m))
+    part.l.copy_(torch.from_numpy(l))
+    part.acc.copy_(torch.from_numpy(acc))
+    rng = np.random.default_rng(S)
+    RV = np.stack([np.linalg.qr(rng.normal(size=(D, D)))[0] for _ in range(2)]).astype(np.float32)
+    out = torch.empty((B, L.n_q_heads, D), dtype=torch.bfloat16, device="cuda")
+    out32 = torch.empty((B, L.n_q_heads, D), dtype=torch.float32, device="cuda")
+    ob.oscar_merge(L, part, torch.from_numpy(RV).cuda(), out, out32)
+    torch.cuda.synchronize()
+    o32, ob16 = out32.cpu().numpy(), bf16_bits(out)
+    for b in range(B):
+        for hq in range(L.n_q_heads):
+            r32, rb = oracle.merge_f32(m[b, hq], l[b, hq], acc[b, hq], RV[hq // L.gqa])
+            assert np.array_equal(o32[b, hq].view(np.uint32), r32.view(np.uint32)), (b, hq)
+            assert np.array_equal(ob16[b, hq], rb)
+
+
+@pytest.mark.parametrize("seq,hist,gqa,ps,group,S", [
+    ((1024, 700, 333), None, 4, 16, 128, 4),          # ragged batch, short request with little history
+    ((40,), None, 4, 16, 128, 2),                      # shorter than the sink: no history at all
+    ((500,), (64,), 4, 16, 128, 3),                    # history end at the sink: all BF16
+    ((2000,), None, 8, 64, 32, 40),                    # more splits than history pages, group 32, G=8
+    ((1500,), None, 1, 32, 64, 6),                     # G=1, group 64
+    ((1100,), (843,), 2, 16, 128, 5),                  # history end mid-page, one demoted row still BF16
+])
+def test_decode_edge_cases(seq, hist, gqa, ps, group, S):
+    case = sc.make_case(n_kv=2, gqa=gqa, page_size=ps, group=group, seq=seq, hist_end=hist)
+    sc.upload(case)
+    out, out32, lse, _ = sc.run_decode(case, S)
+    _check_outputs(case, out, out32, lse)
+    assert ob.oscar_get_device_status() == 0
+
+
+def test_decode_qwen3_8b_layer_shape():
+    """One layer of the Qwen3-8B shape (32 q / 8 kv heads, 64-token pages) over a ragged batch
+    spanning many splits and a ragged last page."""
+    case = sc.make_case(n_kv=8, gqa=4, page_size=64, seq=(6000, 3333, 1234))
+    sc.upload(case)
+    out, out32, lse, _ = sc.run_decode(case, 24)
+    _check_outputs(case, out, out32, lse)
+
+
+def test_bf16_full_cache_parity():
+    """The all-BF16 comparison kernel: oracle with no history region (sink = h_end = 0)."""
+    case = sc.make_case(n_kv=2, gqa=4, page_size=16, seq=(1024, 555))
+    L = case.layout
+    dev = sc.upload(case, demote_history=False)
+    part = ob.Partials.empty(L, 2, 9)
+    ob.oscar_bf16_decode_attention(L, dev["q"], dev["stage"], dev["stage_table"], dev["seq_len"], case.sm_scale, part)
+    out32 = torch.empty((2, L.n_q_heads, D), dtype=torch.float32, device="cuda")
+    ob.oscar_merge(L, part, None, None, out32)
+    torch.cuda.synchronize()
+    qb = bf16_bits(case.q)
+    got, exp = [], []
+    for b, T in enumerate(case.seq):
+        for h in range(L.n_kv_heads):
+            kb, vb = bf16_bits(case.K[b][:, h]), bf16_bits(case.V[b][:, h])
+            z8 = np.zeros((T, D // 4), np.uint8)
+            z16 = np.zeros((T, 1), np.uint16)
+            cache = oracle.HeadCache(kb, vb, z8, z8, z16, z16, z16, z16, 0, 0, 128)
+            I = np.eye(D, dtype=np.float32)
+            for g in range(L.gqa):
+                o, _ = oracle.attend_head(qb[b, h * L.gqa + g], I, I, cache, case.sm_scale)
+                got.append(out32.cpu().numpy()[b, h * L.gqa + g])
+                exp.append(o)
+    ok, r, m = sc.tolerance_ok(np.stack(got), np.stack(exp))
+    assert ok, (r, m)
+
+
+def test_bad_page_id_is_flagged_not_faulted():
+    case = sc.make_case(n_kv=2, gqa=4, page_size=16, seq=(1024,))
+    dev = sc.upload(case)
+    assert ob.oscar_get_device_status() == 0
+    bad = dev["int2_table"].clone()
+    bad[0, 10] = case.dev["int2"].n_pages + 5
+    dev["int2_table"] = bad
+    sc.run_decode(case, 4)
+    assert ob.oscar_get_device_status() & 0x1
+    assert ob.oscar_get_device_status() == 0                     # read clears it
+
+
+def test_host_validation_errors():
+    L = ob.Layout(2, 3, 16)                                       # gqa 3 unsupported
+    x = torch.zeros((4, D), dtype=torch.float32, device="cuda")
+    c = torch.zeros((4, 32), dtype=torch.uint8, device="cuda")
+    s = torch.zeros((4, 1), dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(ob.OscarError, match="gqa"):
+        ob.oscar_quantize_rotated(L, x, 0.96, c, s, s)
+    with pytest.raises(ob.OscarError, match="clip"):
+        ob.oscar_quantize_rotated(ob.Layout(2, 4, 16), x, 0.0, c, s, s)
