@@ -1,0 +1,508 @@
+#!/usr/bin/env python
+"""Decode-attention benchmark of the OSCAR INT2 KV-cache path on GB300.
+
+One step = the attention of one decode token for every layer of the model:
+per layer, q -> q·R_K (oscar_rotate_q), INT2 history + BF16 sink/recent
+partials (oscar_decode_attention), online-softmax merge with R_V^T
+(oscar_merge); for workloads that demote every step, the demotion of the
+token leaving the recent window runs on a side stream in the same step.
+Steps are captured in a CUDA graph and timed with CUDA events.
+
+Prints one JSON line (rank 0).  Default workload: Qwen3-8B shape at 100,000
+tokens of context, batch 1, 36 layers.  `--impl reference` times the CPU
+oracle on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import oscar_synthetic as syn  # noqa: E402
+
+METRIC = "INT2-history decode-attn tokens/s and HBM GB/s (% of roofline) at 100K ctx"
+FALLBACK_HBM_GBS = 6800.0
+D = 128
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["oscar", "reference"], default="oscar")
+    ap.add_argument("--workload", default="qwen3_8b_100k", choices=sorted(syn.WORKLOADS))
+    ap.add_argument("--splits", type=int, default=0, help="history splits per request (0 = library suggestion)")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-bf16", action="store_true", help="skip the all-BF16 cache comparison")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU seconds of the oracle sample")
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------------ helpers --
+
+def workload_text(w: syn.Workload) -> str:
+    ctx = f"contexts U{{{w.ragged[0]}..{w.ragged[1]}}}" if w.ragged else f"context {w.context}"
+    extra = f", {w.shared_prefix}-token shared prefix" if w.shared_prefix else ""
+    dem = ", one demotion per request/layer/kv head per step (side stream)" if w.demote_per_step else ""
+    return (f"{w.name}: {w.layers} layers, {w.n_q_heads} q / {w.n_kv_heads} kv heads, head_dim {w.head_dim}, "
+            f"batch {w.batch}, {ctx} ({w.sink} BF16 sink + INT2 history + {w.recent} BF16 recent){extra}, "
+            f"page {w.page_size}, group {w.group}{dem}")
+
+
+def bytes_per_step(w: syn.Workload, seq, hist_end) -> dict:
+    """Algorithmic bytes of one step: INT2 codes + scale/zero of the history, BF16 windows, q and out."""
+    per_tok_int2 = w.n_kv_heads * (2 * w.head_dim // 4 + 4 * 2 * (w.head_dim // w.group))
+    per_tok_bf16 = w.n_kv_heads * 2 * w.head_dim * 2
+    hist = sum(max(0, int(h) - w.sink) for h in hist_end)
+    bf = sum(int(t) - max(0, int(h) - w.sink) for t, h in zip(seq, hist_end))
+    qo = w.batch * w.n_q_heads * w.head_dim * 2 * 2
+    per_layer = hist * per_tok_int2 + bf * per_tok_bf16 + qo
+    return {"int2_per_layer": hist * per_tok_int2, "bf16_per_layer": bf * per_tok_bf16, "qo_per_layer": qo,
+            "per_layer": per_layer, "per_step": per_layer * w.layers,
+            "bf16_cache_per_step": (sum(seq) * per_tok_bf16 + qo) * w.layers}
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
+
+
+def stored_traffic(kernel: str, workload: str):
+    """dram read+write bytes per launch from a committed ncu capture, if the kernel source is unchanged."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel, {}).get(workload)
+    if not e:
+        return None
+    if e.get("source_sha256") != source_hash():
+        return None
+    return e.get("bytes_per_launch")
+
+
+def source_hash() -> str:
+    h = hashlib.sha256()
+    cs = os.path.join(ROOT, "bit_kv_cache_oscar_gb300", "csrc")
+    for f in sorted(os.listdir(cs)):
+        with open(os.path.join(cs, f), "rb") as fh:
+            h.update(f.encode() + fh.read())
+    return h.hexdigest()
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms while the timed region runs."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.t.join(timeout=2)
+
+    def summary(self) -> dict:
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx or None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------ GPU: setup ----
+
+class Model:
+    """Caches, rotations and buffers of every layer for one batch (device memory)."""
+
+    def __init__(self, w: syn.Workload, device, n_splits: int, with_bf16_cache: bool):
+        import torch
+        from bit_kv_cache_oscar_gb300 import binding as ob
+        from bit_kv_cache_oscar_gb300 import calibrate
+
+        self.w, self.dev = w, device
+        L = self.L = ob.Layout(w.n_kv_heads, w.gqa, w.page_size, w.group, w.sink, w.recent)
+        self.seq = syn.context_lengths(w)
+        self.demote = w.demote_per_step
+        # With per-step demotion, attention still reads the demoted token from BF16 this step.
+        hist = [min(t, max(w.sink, t - w.recent - (1 if self.demote else 0))) for t in self.seq]
+        self.pages = syn.page_layout(w, self.seq, hist_end=hist)
+        self.hist_end = self.pages.hist_end
+        B, ps = w.batch, w.page_size
+        self.sm_scale = 1.0 / math.sqrt(w.head_dim)
+        max_hist = max(int(h) - w.sink for h in self.hist_end)
+        sms = torch.cuda.get_device_properties(device).multi_processor_count
+        self.S = n_splits or ob.oscar_suggest_splits(L, B, max_hist, sms)
+        self.int2_table = torch.from_numpy(self.pages.int2_table).to(device)
+        self.bf16_table = torch.from_numpy(self.pages.bf16_table).to(device)
+        self.seq_len = torch.tensor(self.seq, dtype=torch.int32, device=device)
+        self.hist_dev = torch.from_numpy(self.hist_end.astype(np.int32)).to(device)
+        self.q_all = torch.empty((w.layers, B, w.n_q_heads, D), dtype=torch.bfloat16, device=device)
+        self.out_all = torch.empty((w.layers, B, w.n_q_heads, D), dtype=torch.bfloat16, device=device)
+        self.q_rot = torch.empty((B, w.n_q_heads, D), dtype=torch.float32, device=device)
+        self.part = ob.Partials.empty(L, B, self.S, device)
+        self.layers = []
+        self.bf16_full = [] if with_bf16_cache else None
+        max_pages = self.pages.int2_table.shape[1]
+        if with_bf16_cache:
+            self.full_table = torch.arange(B * max_pages, dtype=torch.int32, device=device).view(B, max_pages)
+            self.S_full = ob.oscar_suggest_splits(L, B, max(self.seq), sms)
+            self.part_full = ob.Partials.empty(L, B, self.S_full, device)
+            self.out_full = torch.empty((w.layers, B, w.n_q_heads, D), dtype=torch.bfloat16, device=device)
+        # per-step demotion: position hist_end of each request (left the recent window this step)
+        self.dem_req = torch.arange(B, dtype=torch.int32, device=device)
+        self.dem_pos = torch.from_numpy(self.hist_end.astype(np.int32)).to(device)
+        for l in range(w.layers):
+            prof = syn.channel_profile(w.seed, l, w.n_kv_heads)
+            qc, kc, vc = syn.calibration_set(w.seed, l, w.gqa, prof, device=device)
+            RK, RV = calibrate.rotations(qc, kc, vc, self.sm_scale)
+            del qc, kc, vc
+            i2 = ob.Int2Pool.empty(L, self.pages.n_int2_pages, device)
+            bf = ob.Bf16Pool.empty(L, self.pages.n_bf16_pages, device)
+            full = ob.Bf16Pool.empty(L, B * max_pages, device) if with_bf16_cache else None
+            for b, T in enumerate(self.seq):
+                k, v = syn.kv_rows(w.seed, l, b, 0, T, prof, device=device, shared_prefix=w.shared_prefix)
+                n_log = (T + ps - 1) // ps
+                stage = ob.Bf16Pool.empty(L, n_log, device)
+                stage.k.view(-1, w.n_kv_heads, D)[:T] = k
+                stage.v.view(-1, w.n_kv_heads, D)[:T] = v
+                if full is not None:
+                    full.k[b * max_pages:b * max_pages + n_log] = stage.k
+                    full.v[b * max_pages:b * max_pages + n_log] = stage.v
+                st_table = torch.full((1, max_pages), -1, dtype=torch.int32, device=device)
+                st_table[0, :n_log] = torch.arange(n_log, dtype=torch.int32, device=device)
+                start = w.sink if b == 0 else max(w.sink, w.shared_prefix)
+                stop = int(self.hist_end[b]) + (1 if self.demote else 0)
+                if stop > start:
+                    pos = torch.arange(start, stop, dtype=torch.int32, device=device)
+                    req = torch.zeros_like(pos)
+                    ob.oscar_demote(L, stage, st_table, i2, self.int2_table[b:b + 1].contiguous(), req, pos,
+                                    RK, RV, 0.96, 0.92)
+                for lp in range(n_log):
+                    pg = int(self.pages.bf16_table[b, lp])
+                    if pg >= 0:
+                        bf.k[pg] = stage.k[lp]
+                        bf.v[pg] = stage.v[lp]
+                del k, v, stage
+            self.q_all[l] = syn.queries(w.seed, l, B, w.gqa, prof, device=device)
+            self.layers.append({"RK": RK, "RV": RV, "int2": i2, "bf16": bf})
+            if full is not None:
+                self.bf16_full.append(full)
+        torch.cuda.synchronize()
+        assert ob.oscar_get_device_status() == 0
+
+    # one decode step over all layers (the path); optional events bracket each decode call
+    def step(self, events=None, side=None):
+        import torch
+        from bit_kv_cache_oscar_gb300 import binding as ob
+        L, w = self.L, self.w
+        cur = torch.cuda.current_stream()
+        if self.demote and side is not None:
+            side.wait_stream(cur)
+            with torch.cuda.stream(side):
+                for st in self.layers:
+                    ob.oscar_demote(L, st["bf16"], self.bf16_table, st["int2"], self.int2_table, self.dem_req,
+                                    self.dem_pos, st["RK"], st["RV"], 0.96, 0.92, stream=side)
+        for l, st in enumerate(self.layers):
+            ob.oscar_rotate_q(L, self.q_all[l], st["RK"], self.q_rot)
+            if events is not None:
+                events[l][0].record()
+            ob.oscar_decode_attention(L, self.q_all[l], self.q_rot, st["bf16"], self.bf16_table, st["int2"],
+                                      self.int2_table, self.seq_len, self.hist_dev, self.sm_scale, self.part)
+            if events is not None:
+                events[l][1].record()
+            ob.oscar_merge(L, self.part, st["RV"], self.out_all[l])
+        if self.demote and side is not None:
+            cur.wait_stream(side)
+
+    def step_bf16(self):
+        from bit_kv_cache_oscar_gb300 import binding as ob
+        for l, full in enumerate(self.bf16_full):
+            ob.oscar_bf16_decode_attention(self.L, self.q_all[l], full, self.full_table, self.seq_len,
+                                           self.sm_scale, self.part_full)
+            ob.oscar_merge(self.L, self.part_full, None, self.out_full[l])
+
+    def launches_per_step(self) -> int:
+        return self.w.layers * (4 + (1 if self.demote else 0))
+
+
+def capture(fn, steps: int = 1):
+    import torch
+    fn()                                  # eager warm-up (first-launch attribute set-up)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(steps):
+            fn()
+    torch.cuda.synchronize()
+    return g
+
+
+def time_graph(g, K: int, W: int, dist=None) -> float:
+    """Seconds for K replays (after W warm-up replays), barrier + sync on both sides, max over ranks."""
+    import torch
+    for _ in range(W):
+        g.replay()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(K):
+        g.replay()
+    e.record()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    t = s.elapsed_time(e) / 1e3
+    if dist:
+        tt = torch.tensor([t], dtype=torch.float64, device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        t = float(tt.item())
+    return t
+
+
+# ---------------------------------------------------------- CPU baseline ----
+
+def oracle_sample(w: syn.Workload, target_s: float, device_for_inputs="cpu") -> dict:
+    """Time the oracle's fp64 decode attention for the query heads of kv head 0 of layer 0 of
+    request 0 (its own demotion of that head's history beforehand, untimed); extrapolate to one
+    step (all query heads, all layers, all requests)."""
+    import torch
+    import oracle
+
+    def bf16_bits(t):
+        return t.contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+    oracle.build()
+    prof = syn.channel_profile(w.seed, 0, w.n_kv_heads)
+    qc, kc, vc = syn.calibration_set(w.seed, 0, w.gqa, prof)
+    sm = 1.0 / math.sqrt(w.head_dim)
+    q0 = oracle.bf16_to_f64(bf16_bits(qc[0]))
+    RK = oracle.rotation_from_covariance(oracle.query_covariance(q0)).astype(np.float32)
+    RV = oracle.rotation_from_covariance(oracle.score_weighted_value_covariance(
+        q0, oracle.bf16_to_f64(bf16_bits(kc[0])), oracle.bf16_to_f64(bf16_bits(vc[0])), sm)).astype(np.float32)
+    seq = syn.context_lengths(w)
+    T = seq[0]
+    he = min(T, max(w.sink, T - w.recent))
+    k, v = syn.kv_rows(w.seed, 0, 0, 0, T, prof)
+    kb, vb = bf16_bits(k[:, 0]), bf16_bits(v[:, 0])
+    g = w.group
+    ck = np.zeros((T, D // 4), np.uint8)
+    cv = np.zeros((T, D // 4), np.uint8)
+    zk, sk, zv, sv = (np.zeros((T, D // g), np.uint16) for _ in range(4))
+    _, ck[w.sink:he], zk[w.sink:he], sk[w.sink:he] = oracle.demote_rows(kb[w.sink:he], RK, g, 0.96)
+    _, cv[w.sink:he], zv[w.sink:he], sv[w.sink:he] = oracle.demote_rows(vb[w.sink:he], RV, g, 0.92)
+    cache = oracle.HeadCache(kb, vb, ck, cv, zk, sk, zv, sv, w.sink, he, g)
+    qb = bf16_bits(syn.queries(w.seed, 0, 1, w.gqa, prof))
+    n, t0 = 0, time.perf_counter()
+    while True:
+        oracle.attend_head(qb[0, n % w.gqa], RK, RV, cache, sm)
+        n += 1
+        el = time.perf_counter() - t0
+        if el >= target_s and n >= w.gqa:
+            break
+    per_head = el / n
+    heads_per_step = w.n_q_heads * w.layers * w.batch
+    step_s = per_head * heads_per_step * (sum(seq) / (T * w.batch))
+    return {"value": w.batch / step_s, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+            "sample": (f"{n} fp64 query-head attentions (layer 0, kv head 0, T={T}) in {el:.1f} s on 1 host "
+                       f"core; one step = {heads_per_step} query-head attentions, scaled by per-head time "
+                       f"and context length"),
+            "seconds": el, "step_s": step_s}
+
+
+def run_reference(args, w, rank):
+    if rank != 0:
+        return
+    vals = []
+    per = max(1.0, args.cpu_seconds / max(1, args.steps))
+    for _ in range(args.steps):
+        vals.append(oracle_sample(w, per))
+    v = statistics.median(x["value"] for x in vals)
+    cpu = dict(vals[-1])
+    cpu["value"] = v
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * w.batch / v,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": {"workload": workload_text(w)},
+            "cpu_baseline": {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")},
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------- main ----
+
+def main():
+    args = parse_args()
+    w = syn.WORKLOADS[args.workload]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        return run_reference(args, w, rank)
+
+    import torch
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    from bit_kv_cache_oscar_gb300 import binding as ob
+    ob.lib()
+
+    model = Model(w, torch.device("cuda", local), args.splits, with_bf16_cache=not args.no_bf16)
+    bts = bytes_per_step(w, model.seq, model.hist_end)
+    side = torch.cuda.Stream()
+
+    # headline: one-step graph replayed K times
+    g = capture(lambda: model.step(side=side))
+    with ClockSampler(local) as clk:
+        t = time_graph(g, args.steps, args.warmup, dist)
+    ms_step = 1e3 * t / args.steps
+    value = world * w.batch / (t / args.steps)
+
+    # roofline: per-launch durations of the decode-attention call, events captured in a K-step graph
+    evs = [[(torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
+            for _ in range(w.layers)] for _ in range(args.steps)]
+    gp = capture(lambda: model.step(events=evs[0], side=side))
+    gk = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gk):
+        for k in range(args.steps):
+            model.step(events=evs[k], side=side)
+    for _ in range(args.warmup):
+        gp.replay()
+    torch.cuda.synchronize()
+    gk.replay()
+    torch.cuda.synchronize()
+    durs = [evs[k][l][0].elapsed_time(evs[k][l][1]) / 1e3 for k in range(args.steps) for l in range(w.layers)]
+    dur = statistics.mean(durs)
+    peaks = measured_peaks()
+    unit_bytes = bts["per_layer"]
+    achieved = unit_bytes / dur / 1e9
+    traffic = stored_traffic("decode_attention", w.name)
+
+    # e2e: q from pinned host memory -> step -> out to pinned host memory, every step
+    q_host = [torch.empty_like(model.q_all, device="cpu").pin_memory() for _ in range(2)]
+    for qh in q_host:
+        qh.copy_(model.q_all)
+    out_host = [torch.empty_like(model.out_all, device="cpu").pin_memory() for _ in range(2)]
+    for k in range(args.warmup):
+        model.q_all.copy_(q_host[k % 2], non_blocking=True)
+        g.replay()
+        out_host[k % 2].copy_(model.out_all, non_blocking=True)
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for k in range(args.steps):
+        model.q_all.copy_(q_host[k % 2], non_blocking=True)
+        g.replay()
+        out_host[k % 2].copy_(model.out_all, non_blocking=True)
+    e.record()
+    torch.cuda.synchronize()
+    te = s.elapsed_time(e) / 1e3
+    if dist:
+        tt = torch.tensor([te], dtype=torch.float64, device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        te = float(tt.item())
+    e2e = {"value": world * w.batch / (te / args.steps), "unit": "tokens/s",
+           "h2d_bytes_per_step": model.q_all.numel() * 2, "d2h_bytes_per_step": model.out_all.numel() * 2}
+
+    bf16 = None
+    if model.bf16_full is not None:
+        gb = capture(model.step_bf16)
+        tb = time_graph(gb, args.steps, args.warmup, dist)
+        vb = world * w.batch / (tb / args.steps)
+        bf16 = {"value": vb, "unit": "tokens/s", "ms_per_step": 1e3 * tb / args.steps,
+                "bytes_per_step": bts["bf16_cache_per_step"], "int2_speedup": value / vb,
+                "gbs": bts["bf16_cache_per_step"] / (tb / args.steps) / 1e9}
+    assert ob.oscar_get_device_status() == 0
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = oracle_sample(w, args.cpu_seconds)
+        cpu = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "fp32", "data": "synthetic",
+            "config": {"workload": workload_text(w), "batch": w.batch, "layers": w.layers,
+                       "history_splits": model.S,
+                       "l2": f"inputs larger than L2: {bts['per_step'] / 1e9:.2f} GB read per step, 129 MB L2",
+                       "kv_storage": "INT2 history (codes + bf16 scale/zero per group) + BF16 sink/recent",
+                       "timing": "CUDA graph of one step, CUDA events, K replays"},
+            "hbm_gbs": bts["per_step"] / (t / args.steps) / 1e9 * world,
+            "bytes_per_step": bts["per_step"],
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                         "kernel": "oscar_decode_attention (INT2 history split-K + BF16 sink/recent)",
+                         "bytes_per_launch": unit_bytes, "launch_us": dur * 1e6,
+                         "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs copy bandwidth)"},
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": model.launches_per_step() * args.steps,
+            "clocks": clk.summary(), "bf16_cache": bf16,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -5,7 +5,7 @@ Runs once per model, before serving, and is not part of the decode path
 C_Q = (1/N) sum q^T q and C_S = (1/N) V^T S^T S V estimated on a calibration
 set, eigenvectors as the rotation basis; estelledc notes "核心要点" item 2:
 computed offline once and fixed at inference).  It uses torch's dense linear
-algebra on the device (matmul, softmax, a symmetric eigensolver) in float64;
+algebra (device matmul and softmax in float64, a host symmetric eigensolver);
 the output is the fp32 R that the decode kernels consume.
 
 Conventions: eigenvectors as columns sorted by descending eigenvalue, each
@@ -35,8 +35,12 @@ def _bitrev_perm(n: int, device) -> torch.Tensor:
 
 
 def _basis(C: torch.Tensor) -> torch.Tensor:
-    """Batched descending eigenbasis with the sign convention above. C: [..., D, D] float64."""
-    w, U = torch.linalg.eigh(C)
+    """Batched descending eigenbasis with the sign convention above. C: [..., D, D] float64.
+
+    The 128 x 128 eigenproblems are solved on the host (LAPACK through torch's CPU
+    backend) and the basis is moved back to C's device."""
+    w, U = torch.linalg.eigh(C.cpu())
+    w, U = w.to(C.device), U.to(C.device)
     order = torch.argsort(-w, dim=-1, stable=True)
     U = torch.gather(U, -1, order.unsqueeze(-2).expand_as(U))
     idx = U.abs().argmax(dim=-2, keepdim=True)
