@@ -48,6 +48,7 @@ EXPORTS = [
     "oscar_partials_ml_floats", "oscar_partials_acc_floats", "oscar_suggest_splits", "oscar_demote",
     "oscar_quantize_rotated", "oscar_rotate_q", "oscar_decode_attention", "oscar_merge",
     "oscar_bf16_decode_attention", "oscar_get_device_status", "oscar_last_error_string", "oscar_version",
+    "oscar_decode_attention_noalloc",
 ]
 
 
@@ -82,6 +83,9 @@ def lib():
     L.oscar_bf16_decode_attention.argtypes = [P(LayoutC), vp, P(Bf16PoolC), vp, i32, vp, i32, ctypes.c_float,
                                               P(PartialsC), vp]
     L.oscar_bf16_decode_attention.restype = st
+    L.oscar_decode_attention_noalloc.argtypes = [P(LayoutC), vp, vp, P(Bf16PoolC), vp, P(Int2PoolC), vp, i32, vp,
+                                                 vp, i32, ctypes.c_float, i32, vp, vp, vp, vp, vp]
+    L.oscar_decode_attention_noalloc.restype = st
     L.oscar_get_device_status.argtypes = [P(i32), vp]
     L.oscar_get_device_status.restype = st
     L.oscar_last_error_string.argtypes = []
@@ -254,6 +258,20 @@ def oscar_bf16_decode_attention(layout: Layout, q: torch.Tensor, pool: Bf16Pool,
     _check("oscar_bf16_decode_attention", lib().oscar_bf16_decode_attention(
         ctypes.byref(layout.c()), _ptr(q), ctypes.byref(pool.c()), _ptr(page_table), int(page_table.shape[-1]),
         _ptr(seq_len), int(q.shape[0]), float(sm_scale), ctypes.byref(partials.c()), _stream(stream)))
+
+
+def oscar_decode_attention_noalloc(layout: Layout, q: torch.Tensor, q_rot: torch.Tensor, bf16_pool: Bf16Pool,
+                                   bf16_page_table: torch.Tensor, int2_pool: Int2Pool,
+                                   int2_page_table: torch.Tensor, seq_len: torch.Tensor, hist_end: torch.Tensor,
+                                   sm_scale: float, n_splits: int, R_V: torch.Tensor,
+                                   out: Optional[torch.Tensor], out_f32: Optional[torch.Tensor] = None,
+                                   lse: Optional[torch.Tensor] = None, stream=None):
+    """Decode attention + merge with the partials in the library's own device array (no caller scratch)."""
+    _check("oscar_decode_attention_noalloc", lib().oscar_decode_attention_noalloc(
+        ctypes.byref(layout.c()), _ptr(q), _ptr(q_rot), ctypes.byref(bf16_pool.c()), _ptr(bf16_page_table),
+        ctypes.byref(int2_pool.c()), _ptr(int2_page_table), int(int2_page_table.shape[-1]), _ptr(seq_len),
+        _ptr(hist_end), int(q.shape[0]), float(sm_scale), int(n_splits), _ptr(R_V), _ptr(out), _ptr(out_f32),
+        _ptr(lse), _stream(stream)))
 
 
 def oscar_get_device_status(stream=None) -> int:

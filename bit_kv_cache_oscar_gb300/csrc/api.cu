@@ -110,6 +110,8 @@ oscar::PartialsView part_view(const oscar_partials_t *p) { return {p->m, p->l, p
 
 }  // namespace
 
+oscar_status_t oscar::set_last_error(oscar_status_t code, const char *msg) { return fail(code, "%s", msg); }
+
 extern "C" {
 
 size_t oscar_partials_ml_floats(const oscar_layout_t *L, int32_t batch, int32_t n_splits) {

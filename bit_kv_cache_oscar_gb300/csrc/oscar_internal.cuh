@@ -73,6 +73,9 @@ __device__ __forceinline__ void read_lengths(const int32_t *seq_len, const int32
     if (bad && threadIdx.x == 0) flag_status(status, OSCAR_DEV_BAD_LENGTH);
 }
 
+// Record the one-line reason returned by oscar_last_error_string() and return `code`.
+oscar_status_t set_last_error(oscar_status_t code, const char *msg);
+
 // ---------------------------------------------------------------- launches --
 
 struct Int2PoolView {

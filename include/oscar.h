@@ -249,6 +249,30 @@ OSCAR_API oscar_status_t oscar_bf16_decode_attention(const oscar_layout_t *layou
                                            int32_t batch, float sm_scale,
                                            const oscar_partials_t *partials, void *stream);
 
+/*
+ * Decode attention and merge in one call with no caller scratch (this entry
+ * point has no counterpart on the pages; it exists for callers that cannot
+ * allocate device memory, e.g. code inside a host framework that owns every
+ * device allocation and offers no workspace, or a loop that must never call
+ * an allocator).  Same inputs and outputs as oscar_decode_attention followed
+ * by oscar_merge, with n_splits history splits; the partials live in a
+ * library-owned device array of OSCAR_NOALLOC_SCRATCH_BYTES per device
+ * (allocated statically when the library is loaded, held until exit; this
+ * call allocates nothing).  Limit: 2*ceil64(batch*Hq*(n_splits+1)) +
+ * batch*Hq*(n_splits+1)*head_dim floats must fit, else
+ * OSCAR_ERR_INVALID_ARG.  The first call on a device looks up the array's
+ * device address (make that first call before any stream capture).  All
+ * calls share the array: calls whose GPU work overlaps race and must be
+ * serialised by the caller.  Every slot is written before it is read, so no
+ * state carries over between calls.
+ */
+#define OSCAR_NOALLOC_SCRATCH_BYTES (4u << 20)
+OSCAR_API oscar_status_t oscar_decode_attention_noalloc(
+    const oscar_layout_t *layout, const uint16_t *q, const float *q_rot, const oscar_bf16_pool_t *bf16_pool,
+    const int32_t *bf16_page_table, const oscar_int2_pool_t *int2_pool, const int32_t *int2_page_table,
+    int32_t max_pages_per_req, const int32_t *seq_len, const int32_t *hist_end, int32_t batch, float sm_scale,
+    int32_t n_splits, const float *R_V, uint16_t *out, float *out_f32, float *lse, void *stream);
+
 /* Read and clear the device status word of the current device (synchronizes `stream`). */
 OSCAR_API oscar_status_t oscar_get_device_status(int32_t *status_bits, void *stream);
 
