@@ -49,6 +49,7 @@ def parse_args():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-bf16", action="store_true", help="skip the all-BF16 cache comparison")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU seconds of the oracle sample")
+    ap.add_argument("--layers", type=int, default=0, help="profiling aid: run only this many layers (0 = all)")
     return ap.parse_args()
 
 
@@ -199,7 +200,8 @@ class Model:
         max_pages = self.pages.int2_table.shape[1]
         if with_bf16_cache:
             self.full_table = torch.arange(B * max_pages, dtype=torch.int32, device=device).view(B, max_pages)
-            self.S_full = ob.oscar_suggest_splits(L, B, max(self.seq), sms)
+            # the all-BF16 kernel runs one CTA per split, one resident CTA per SM
+            self.S_full = max(1, min(1024, sms // B))
             self.part_full = ob.Partials.empty(L, B, self.S_full, device)
             self.out_full = torch.empty((w.layers, B, w.n_q_heads, D), dtype=torch.bfloat16, device=device)
         # per-step demotion: position hist_end of each request (left the recent window this step)
@@ -244,8 +246,10 @@ class Model:
         torch.cuda.synchronize()
         assert ob.oscar_get_device_status() == 0
 
-    # one decode step over all layers (the path); optional events bracket each decode call
-    def step(self, events=None, side=None):
+    # One decode step over all layers (the path).  Per layer the BF16 sink/recent half runs on
+    # a second stream next to q rotation + the INT2 history half; the merge joins them.
+    # Optional events bracket each INT2 history launch.
+    def step(self, events=None, side=None, win=None):
         import torch
         from bit_kv_cache_oscar_gb300 import binding as ob
         L, w = self.L, self.w
@@ -257,13 +261,23 @@ class Model:
                     ob.oscar_demote(L, st["bf16"], self.bf16_table, st["int2"], self.int2_table, self.dem_req,
                                     self.dem_pos, st["RK"], st["RV"], 0.96, 0.92, stream=side)
         for l, st in enumerate(self.layers):
+            if win is not None:
+                win.wait_stream(cur)
+                with torch.cuda.stream(win):
+                    ob.oscar_decode_attention_window(L, self.q_all[l], st["bf16"], self.bf16_table, self.seq_len,
+                                                     self.hist_dev, self.sm_scale, self.part, stream=win)
+            else:
+                ob.oscar_decode_attention_window(L, self.q_all[l], st["bf16"], self.bf16_table, self.seq_len,
+                                                 self.hist_dev, self.sm_scale, self.part)
             ob.oscar_rotate_q(L, self.q_all[l], st["RK"], self.q_rot)
             if events is not None:
                 events[l][0].record()
-            ob.oscar_decode_attention(L, self.q_all[l], self.q_rot, st["bf16"], self.bf16_table, st["int2"],
-                                      self.int2_table, self.seq_len, self.hist_dev, self.sm_scale, self.part)
+            ob.oscar_decode_attention_history(L, self.q_rot, st["int2"], self.int2_table, self.seq_len,
+                                              self.hist_dev, self.sm_scale, self.part)
             if events is not None:
                 events[l][1].record()
+            if win is not None:
+                cur.wait_stream(win)
             ob.oscar_merge(L, self.part, st["RV"], self.out_all[l])
         if self.demote and side is not None:
             cur.wait_stream(side)
@@ -276,6 +290,7 @@ class Model:
             ob.oscar_merge(self.L, self.part_full, None, self.out_full[l])
 
     def launches_per_step(self) -> int:
+        # rotate_q, INT2 history, BF16 window, merge per layer (+ the demotion)
         return self.w.layers * (4 + (1 if self.demote else 0))
 
 
@@ -289,6 +304,21 @@ def capture(fn, steps: int = 1):
             fn()
     torch.cuda.synchronize()
     return g
+
+
+def max_over_ranks(t: float, dist=None, device="cuda") -> float:
+    """The largest of the ranks' values (the slowest rank sets the step time)."""
+    if not dist:
+        return t
+    import torch
+    tt = torch.tensor([t], dtype=torch.float64, device=device)
+    dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+    return float(tt.item())
+
+
+def job_throughput(world: int, batch: int, seconds: float, steps: int) -> float:
+    """Whole-job tokens/s: every rank decodes `batch` tokens per step (weak scaling)."""
+    return world * batch / (seconds / steps)
 
 
 def time_graph(g, K: int, W: int, dist=None) -> float:
@@ -308,12 +338,7 @@ def time_graph(g, K: int, W: int, dist=None) -> float:
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
-    t = s.elapsed_time(e) / 1e3
-    if dist:
-        tt = torch.tensor([t], dtype=torch.float64, device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        t = float(tt.item())
-    return t
+    return max_over_ranks(s.elapsed_time(e) / 1e3, dist)
 
 
 # ---------------------------------------------------------- CPU baseline ----
@@ -390,6 +415,9 @@ def run_reference(args, w, rank):
 def main():
     args = parse_args()
     w = syn.WORKLOADS[args.workload]
+    if args.layers:
+        import dataclasses
+        w = dataclasses.replace(w, layers=args.layers)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
@@ -408,22 +436,23 @@ def main():
     model = Model(w, torch.device("cuda", local), args.splits, with_bf16_cache=not args.no_bf16)
     bts = bytes_per_step(w, model.seq, model.hist_end)
     side = torch.cuda.Stream()
+    win = torch.cuda.Stream()
 
     # headline: one-step graph replayed K times
-    g = capture(lambda: model.step(side=side))
+    g = capture(lambda: model.step(side=side, win=win))
     with ClockSampler(local) as clk:
         t = time_graph(g, args.steps, args.warmup, dist)
     ms_step = 1e3 * t / args.steps
-    value = world * w.batch / (t / args.steps)
+    value = job_throughput(world, w.batch, t, args.steps)
 
     # roofline: per-launch durations of the decode-attention call, events captured in a K-step graph
     evs = [[(torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
             for _ in range(w.layers)] for _ in range(args.steps)]
-    gp = capture(lambda: model.step(events=evs[0], side=side))
+    gp = capture(lambda: model.step(events=evs[0], side=side, win=win))
     gk = torch.cuda.CUDAGraph()
     with torch.cuda.graph(gk):
         for k in range(args.steps):
-            model.step(events=evs[k], side=side)
+            model.step(events=evs[k], side=side, win=win)
     for _ in range(args.warmup):
         gp.replay()
     torch.cuda.synchronize()
@@ -432,9 +461,9 @@ def main():
     durs = [evs[k][l][0].elapsed_time(evs[k][l][1]) / 1e3 for k in range(args.steps) for l in range(w.layers)]
     dur = statistics.mean(durs)
     peaks = measured_peaks()
-    unit_bytes = bts["per_layer"]
+    unit_bytes = bts["int2_per_layer"] + w.batch * w.n_q_heads * w.head_dim * 4   # history + q_rot
     achieved = unit_bytes / dur / 1e9
-    traffic = stored_traffic("decode_attention", w.name)
+    traffic = stored_traffic("int2_history", w.name)
 
     # e2e: q from pinned host memory -> step -> out to pinned host memory, every step
     q_host = [torch.empty_like(model.q_all, device="cpu").pin_memory() for _ in range(2)]
@@ -456,19 +485,15 @@ def main():
         out_host[k % 2].copy_(model.out_all, non_blocking=True)
     e.record()
     torch.cuda.synchronize()
-    te = s.elapsed_time(e) / 1e3
-    if dist:
-        tt = torch.tensor([te], dtype=torch.float64, device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        te = float(tt.item())
-    e2e = {"value": world * w.batch / (te / args.steps), "unit": "tokens/s",
+    te = max_over_ranks(s.elapsed_time(e) / 1e3, dist)
+    e2e = {"value": job_throughput(world, w.batch, te, args.steps), "unit": "tokens/s",
            "h2d_bytes_per_step": model.q_all.numel() * 2, "d2h_bytes_per_step": model.out_all.numel() * 2}
 
     bf16 = None
     if model.bf16_full is not None:
         gb = capture(model.step_bf16)
         tb = time_graph(gb, args.steps, args.warmup, dist)
-        vb = world * w.batch / (tb / args.steps)
+        vb = job_throughput(world, w.batch, tb, args.steps)
         bf16 = {"value": vb, "unit": "tokens/s", "ms_per_step": 1e3 * tb / args.steps,
                 "bytes_per_step": bts["bf16_cache_per_step"], "int2_speedup": value / vb,
                 "gbs": bts["bf16_cache_per_step"] / (tb / args.steps) / 1e9}
@@ -493,7 +518,7 @@ def main():
             "bytes_per_step": bts["per_step"],
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                         "kernel": "oscar_decode_attention (INT2 history split-K + BF16 sink/recent)",
+                         "kernel": "oscar_decode_attention_history (INT2 history split-K, one layer)",
                          "bytes_per_launch": unit_bytes, "launch_us": dur * 1e6,
                          "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs copy bandwidth)"},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": model.launches_per_step() * args.steps,

@@ -48,7 +48,7 @@ EXPORTS = [
     "oscar_partials_ml_floats", "oscar_partials_acc_floats", "oscar_suggest_splits", "oscar_demote",
     "oscar_quantize_rotated", "oscar_rotate_q", "oscar_decode_attention", "oscar_merge",
     "oscar_bf16_decode_attention", "oscar_get_device_status", "oscar_last_error_string", "oscar_version",
-    "oscar_decode_attention_noalloc",
+    "oscar_decode_attention_noalloc", "oscar_decode_attention_history", "oscar_decode_attention_window",
 ]
 
 
@@ -78,6 +78,12 @@ def lib():
     L.oscar_decode_attention.argtypes = [P(LayoutC), vp, vp, P(Bf16PoolC), vp, P(Int2PoolC), vp, i32, vp, vp,
                                          i32, ctypes.c_float, P(PartialsC), vp]
     L.oscar_decode_attention.restype = st
+    L.oscar_decode_attention_history.argtypes = [P(LayoutC), vp, P(Int2PoolC), vp, i32, vp, vp, i32,
+                                                 ctypes.c_float, P(PartialsC), vp]
+    L.oscar_decode_attention_history.restype = st
+    L.oscar_decode_attention_window.argtypes = [P(LayoutC), vp, P(Bf16PoolC), vp, i32, vp, vp, i32,
+                                                ctypes.c_float, P(PartialsC), vp]
+    L.oscar_decode_attention_window.restype = st
     L.oscar_merge.argtypes = [P(LayoutC), P(PartialsC), vp, i32, vp, vp, vp, vp]
     L.oscar_merge.restype = st
     L.oscar_bf16_decode_attention.argtypes = [P(LayoutC), vp, P(Bf16PoolC), vp, i32, vp, i32, ctypes.c_float,
@@ -243,6 +249,24 @@ def oscar_decode_attention(layout: Layout, q: torch.Tensor, q_rot: torch.Tensor,
         ctypes.byref(layout.c()), _ptr(q), _ptr(q_rot), ctypes.byref(bf16_pool.c()), _ptr(bf16_page_table),
         ctypes.byref(int2_pool.c()), _ptr(int2_page_table), int(int2_page_table.shape[-1]), _ptr(seq_len),
         _ptr(hist_end), int(q.shape[0]), float(sm_scale), ctypes.byref(partials.c()), _stream(stream)))
+
+
+def oscar_decode_attention_history(layout: Layout, q_rot: torch.Tensor, int2_pool: Int2Pool,
+                                   int2_page_table: torch.Tensor, seq_len: torch.Tensor, hist_end: torch.Tensor,
+                                   sm_scale: float, partials: Partials, stream=None):
+    _check("oscar_decode_attention_history", lib().oscar_decode_attention_history(
+        ctypes.byref(layout.c()), _ptr(q_rot), ctypes.byref(int2_pool.c()), _ptr(int2_page_table),
+        int(int2_page_table.shape[-1]), _ptr(seq_len), _ptr(hist_end), int(q_rot.shape[0]), float(sm_scale),
+        ctypes.byref(partials.c()), _stream(stream)))
+
+
+def oscar_decode_attention_window(layout: Layout, q: torch.Tensor, bf16_pool: Bf16Pool,
+                                  bf16_page_table: torch.Tensor, seq_len: torch.Tensor, hist_end: torch.Tensor,
+                                  sm_scale: float, partials: Partials, stream=None):
+    _check("oscar_decode_attention_window", lib().oscar_decode_attention_window(
+        ctypes.byref(layout.c()), _ptr(q), ctypes.byref(bf16_pool.c()), _ptr(bf16_page_table),
+        int(bf16_page_table.shape[-1]), _ptr(seq_len), _ptr(hist_end), int(q.shape[0]), float(sm_scale),
+        ctypes.byref(partials.c()), _stream(stream)))
 
 
 def oscar_merge(layout: Layout, partials: Partials, R_V: Optional[torch.Tensor], out: Optional[torch.Tensor],

@@ -91,8 +91,8 @@ oscar_status_t check_partials(const oscar_partials_t *p) {
     if (!p) return fail(OSCAR_ERR_INVALID_ARG, "partials is NULL");
     if (!p->m || !p->l || !p->acc) return fail(OSCAR_ERR_INVALID_ARG, "partials has a NULL array");
     if (!aligned16(p->acc)) return fail(OSCAR_ERR_INVALID_ARG, "partials acc not 16-byte aligned");
-    if (p->n_splits < 1 || p->n_splits > 256)
-        return fail(OSCAR_ERR_INVALID_ARG, "n_splits %d outside 1..256", p->n_splits);
+    if (p->n_splits < 1 || p->n_splits > 1024)
+        return fail(OSCAR_ERR_INVALID_ARG, "n_splits %d outside 1..1024", p->n_splits);
     return OSCAR_OK;
 }
 
@@ -125,11 +125,21 @@ size_t oscar_partials_acc_floats(const oscar_layout_t *L, int32_t batch, int32_t
 
 int32_t oscar_suggest_splits(const oscar_layout_t *L, int32_t batch, int32_t max_hist_tokens, int32_t sm_count) {
     if (!L || L->page_size <= 0 || batch <= 0 || sm_count <= 0) return 1;
-    const int pages = (max_hist_tokens + L->page_size - 1) / L->page_size;
-    long want = (2L * sm_count + (long)batch * L->n_kv_heads - 1) / ((long)batch * L->n_kv_heads);
-    if (want > pages) want = pages;
+    const int tiles = (max_hist_tokens + 15) / 16;
+    long want;
+    int active = 0;
+    if (oscar::int2_mma_supported(*L)) {
+        // one split = a cluster of C CTAs (all kv heads each): as many splits as clusters fit at once
+        const int c = oscar::int2_mma_cluster_size(*L, &active);
+        if (active <= 0) active = (2 * sm_count) / c;
+        want = active / batch;
+    } else {
+        // one CTA per (split, kv head): about two resident CTAs per SM
+        want = (2L * sm_count + (long)batch * L->n_kv_heads - 1) / ((long)batch * L->n_kv_heads);
+    }
+    if (want > tiles) want = tiles;
     if (want < 1) want = 1;
-    if (want > 256) want = 256;
+    if (want > 1024) want = 1024;
     return (int32_t)want;
 }
 
@@ -204,6 +214,43 @@ oscar_status_t oscar_decode_attention(const oscar_layout_t *layout, const uint16
     e = oscar::launch_bf16_attention(*layout, q, bf16_view(bf16_pool), bf16_page_table, max_pages_per_req,
                                      seq_len, hist_end, batch, sm_scale, part_view(partials), 0, st, s);
     return cuda_status(e, "BF16 sink/recent attention launch");
+}
+
+oscar_status_t oscar_decode_attention_history(const oscar_layout_t *layout, const float *q_rot,
+                                              const oscar_int2_pool_t *int2_pool, const int32_t *int2_page_table,
+                                              int32_t max_pages_per_req, const int32_t *seq_len,
+                                              const int32_t *hist_end, int32_t batch, float sm_scale,
+                                              const oscar_partials_t *partials, void *stream) {
+    TRY(check_layout(layout));
+    TRY(check_int2_pool(int2_pool));
+    TRY(check_partials(partials));
+    if (batch < 0 || batch > 65535) return fail(OSCAR_ERR_INVALID_ARG, "batch %d outside 0..65535", batch);
+    if (batch == 0) return OSCAR_OK;
+    if (!q_rot || !int2_page_table || !seq_len || !hist_end) return fail(OSCAR_ERR_INVALID_ARG, "NULL argument");
+    if (!aligned16(q_rot)) return fail(OSCAR_ERR_INVALID_ARG, "q_rot not 16-byte aligned");
+    if (max_pages_per_req < 1) return fail(OSCAR_ERR_INVALID_ARG, "max_pages_per_req %d < 1", max_pages_per_req);
+    return cuda_status(oscar::launch_int2_attention(*layout, q_rot, int2_view(int2_pool), int2_page_table,
+                                                    max_pages_per_req, seq_len, hist_end, batch, sm_scale,
+                                                    part_view(partials), status_ptr(), (cudaStream_t)stream),
+                       "INT2 attention launch");
+}
+
+oscar_status_t oscar_decode_attention_window(const oscar_layout_t *layout, const uint16_t *q,
+                                             const oscar_bf16_pool_t *bf16_pool, const int32_t *bf16_page_table,
+                                             int32_t max_pages_per_req, const int32_t *seq_len,
+                                             const int32_t *hist_end, int32_t batch, float sm_scale,
+                                             const oscar_partials_t *partials, void *stream) {
+    TRY(check_layout(layout));
+    TRY(check_bf16_pool(bf16_pool));
+    TRY(check_partials(partials));
+    if (batch < 0 || batch > 65535) return fail(OSCAR_ERR_INVALID_ARG, "batch %d outside 0..65535", batch);
+    if (batch == 0) return OSCAR_OK;
+    if (!q || !bf16_page_table || !seq_len || !hist_end) return fail(OSCAR_ERR_INVALID_ARG, "NULL argument");
+    if (max_pages_per_req < 1) return fail(OSCAR_ERR_INVALID_ARG, "max_pages_per_req %d < 1", max_pages_per_req);
+    return cuda_status(oscar::launch_bf16_attention(*layout, q, bf16_view(bf16_pool), bf16_page_table,
+                                                    max_pages_per_req, seq_len, hist_end, batch, sm_scale,
+                                                    part_view(partials), 0, status_ptr(), (cudaStream_t)stream),
+                       "BF16 sink/recent attention launch");
 }
 
 oscar_status_t oscar_merge(const oscar_layout_t *layout, const oscar_partials_t *partials, const float *R_V,

@@ -1,0 +1,728 @@
+// INT2-history decode-attention partials on the tensor cores (sm_103a).
+//
+// Method: OSCAR news article (m.kljzs.com mirror), online-path paragraph — the
+// INT2 kernel unpacks the 2-bit codes, restores scale/zero and accumulates in
+// floating point; "Together AI 開源 OSCAR" (news.chathome.org), "OSCAR 的不同之處"
+// — queries meet the rotated keys as q·R_K, values stay rotated until the merge.
+//
+// Design (one CTA = one history split of one request, all kv heads <= 8):
+//  * a producer warp copies 16-token tiles (codes for all heads + bf16
+//    scale/zero) into a ring of shared-memory stages with cp.async, head-major
+//    ([head][token][32 B]), and signals an mbarrier per stage; 8 consumer warps
+//    each own one kv head (and a share of the tiles when there are fewer heads);
+//  * q·k_hat = scale * (q_rot · code) + zero * sum(q_rot) per group, and
+//    sum_t p_t v_hat_t = sum_t p_t zero_t + sum_t (p_t scale_t) code_t: both
+//    contractions run on mma.sync m16n8k16 (f16 in, fp32 accumulate) with the
+//    code matrix as the A operand;
+//  * a 2-bit code c placed in a f16 mantissa with no exponent bits is the
+//    subnormal c * 2^(2k) * 2^-24 (k = its position), so unpacking is a
+//    byte permute plus an AND; the power-of-two factors are folded into the
+//    other operand or the output;
+//  * the other operand (q_rot, and p*scale) is split into f16 hi + lo parts
+//    that fill the 8 MMA columns (4 query heads x {hi, lo}), giving ~22-bit
+//    operands at no extra MMA cost for GQA 4;
+//  * online softmax in the base-2 domain; the per-tile P operand is moved
+//    from the QK accumulator layout to the PV operand layout through a small
+//    per-warp shared buffer; each warp takes two 16-token tiles per pass.
+// Every wait is bounded: a wait that gives up sets OSCAR_DEV_WAIT_TIMEOUT.
+
+#include <cuda_fp16.h>
+
+#include "oscar_internal.cuh"
+#include "ptx.cuh"
+
+namespace oscar {
+namespace {
+
+constexpr int kCW = 8;                       // consumer warps
+constexpr int kThreads = (kCW + 1) * 32;     // + producer warp
+constexpr int kTilesPerStage = 4;
+constexpr int kStageTok = kTileTokens * kTilesPerStage;
+constexpr int kMaxStages = 4;
+
+constexpr uint32_t kM0 = 0x00030003u, kM1 = 0x000C000Cu, kM2 = 0x00300030u, kM3 = 0x00C000C0u,
+                   kM4 = 0x03000300u;
+constexpr float kTwo24 = 16777216.0f;
+
+__device__ __forceinline__ uint32_t pack2(__half lo, __half hi) {
+    return (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
+}
+
+// f16 hi part (part == 0) or lo part (part == 1) of v.
+__device__ __forceinline__ __half split_part(float v, int part) {
+    const __half h = __float2half_rn(v);
+    return part ? __float2half_rn(v - __half2float(h)) : h;
+}
+
+// QK operand: register r (0..7) of one token's 16-channel word w (channels 16W + r in the low
+// half, 16W + 8 + r in the high half), value code * kQF[r] * 2^-24.
+__device__ __forceinline__ uint32_t qk_reg(uint32_t w, uint32_t wb, int r) {
+    switch (r) {
+        case 0: return w & kM0;
+        case 1: return w & kM1;
+        case 2: return w & kM2;
+        case 3: return w & kM3;
+        case 4: return w & kM4;
+        case 5: return wb & kM1;
+        case 6: return wb & kM2;
+        default: return wb & kM3;
+    }
+}
+// factors of registers 0..7: 1, 4, 16, 64, 256, 4, 16, 64
+__device__ __host__ constexpr float qk_factor(int r) { return r == 4 ? 256.f : (float)(1 << (2 * (r & 3))); }
+
+// PV operand: register i (0..15) of the pair (token x, token y) for channel 16W + i, from the
+// byte permutes P1..P4 of their words; value code * pv_factor(i) * 2^-24.
+__device__ __forceinline__ uint32_t pv_reg(uint32_t P1, uint32_t P2, uint32_t P3, uint32_t P4, int i) {
+    switch (i) {
+        case 0: return P1 & kM0;
+        case 1: return P1 & kM1;
+        case 2: return P1 & kM2;
+        case 3: return P1 & kM3;
+        case 4: return P1 & kM4;
+        case 5: return P2 & kM1;
+        case 6: return P2 & kM2;
+        case 7: return P2 & kM3;
+        case 8: return P2 & kM4;
+        case 9: return P3 & kM1;
+        case 10: return P3 & kM2;
+        case 11: return P3 & kM3;
+        case 12: return P3 & kM4;
+        case 13: return P4 & kM1;
+        case 14: return P4 & kM2;
+        default: return P4 & kM3;
+    }
+}
+// factors of registers 0..15: 1, 4, 16, 64, 256, 4, 16, 64, 256, 4, 16, 64, 256, 4, 16, 64
+__device__ __host__ constexpr float pv_factor(int i) {
+    return i == 0 ? 1.f : (i % 4 == 0 ? 256.f : (float)(1 << (2 * (i % 4))));
+}
+
+struct MmaArgs {
+    const float *q_rot;
+    Int2PoolView pool;
+    const int32_t *pt;
+    int max_pages, page_size, n_kv, sink;
+    const int32_t *seq_len, *hist_end;
+    float scale2;
+    PartialsView out;
+    int32_t *status;
+    int stages, stage_bytes, off_v, off_s, arr_bytes, ws_bytes, stage_off;
+    int csize;        // CTAs per cluster; each cluster writes one partial slot
+    int res_off;      // byte offset (from the first stage) of the per-CTA result area
+};
+
+// Cluster reduction: every CTA of a cluster holds (m, l, acc) for each query head of its
+// sub-split in shared memory; CTA `rank` combines query heads rank, rank + C, ... over the
+// C CTAs in rank order and writes partial slot blockIdx.x / C.  Every thread calls this once.
+__device__ __forceinline__ void cluster_combine(const MmaArgs &a, const float *res, int Hq, int b) {
+    const int C = a.csize;
+    cluster_sync_all();
+    const int rank = (int)cluster_ctarank();
+    const int slot = blockIdx.x / C;
+    const size_t S1 = (size_t)a.out.S + 1;
+    const int mine = (Hq - rank + C - 1) / C;
+    const uint32_t rm = saddr(res), rl = rm + Hq * 4, ra = rm + 2 * Hq * 4;
+    for (int e = threadIdx.x; e < mine * kHeadDim; e += blockDim.x) {
+        const int hq = rank + (e / kHeadDim) * C, d = e % kHeadDim;
+        float M = -INFINITY;
+        for (int q = 0; q < C; ++q) M = fmaxf(M, ld_dsmem_f32(rm + hq * 4, q));
+        float L = 0.f, A = 0.f;
+        if (M != -INFINITY) {
+            for (int q = 0; q < C; ++q) {
+                const float mq = ld_dsmem_f32(rm + hq * 4, q);
+                const float f = exp2f(mq - M);
+                L = fmaf(ld_dsmem_f32(rl + hq * 4, q), f, L);
+                A = fmaf(ld_dsmem_f32(ra + (hq * kHeadDim + d) * 4, q), f, A);
+            }
+        }
+        const size_t row = ((size_t)b * Hq + hq) * S1 + slot;
+        a.out.acc[row * kHeadDim + d] = A;
+        if (d == 0) {
+            a.out.m[row] = M;
+            a.out.l[row] = L;
+        }
+    }
+    cluster_sync_all();                 // no CTA leaves while its shared memory is being read
+}
+
+// token position within a 16-token tile -> PV k-column (the K permutation shared by A and B)
+__device__ __forceinline__ int kpos(int tok) { return (tok & 8) + 2 * (tok & 3) + ((tok >> 2) & 1); }
+
+template <int G, int NGRP>
+__global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2)) int2_mma_kernel(MmaArgs a) {
+    constexpr int NT = (G == 8) ? 2 : 1;      // n-tiles of 8 columns: 4 heads x {hi, lo} each
+    constexpr int NCOL = 8 * NT;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem);   // full[0..3], empty[4..7]
+    int *masks = reinterpret_cast<int *>(smem + 64);        // per stage: bit j = tile j holds data
+    uint8_t *stage0 = smem + a.stage_off;
+
+    const int s = blockIdx.x, b = blockIdx.y;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int Hkv = a.n_kv, Hq = Hkv * G, S = a.out.S;
+    int T, he;
+    read_lengths(a.seq_len, a.hist_end, b, a.sink, a.max_pages * a.page_size, a.status, T, he);
+    const SplitRange r = history_split(a.sink, he, (int)gridDim.x, s);   // C sub-splits per slot
+    const int n_iters = (r.tile_hi - r.tile_lo + kTilesPerStage - 1) / kTilesPerStage;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < a.stages; ++i) {
+            mbar_init(saddr(&bars[i]), 33);      // 32 copy-completion arrivals + the mask arrival
+            mbar_init(saddr(&bars[4 + i]), kCW);
+        }
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+
+    // ------------------------------------------------------------ producer --
+    if (warp == kCW) {
+        const int lgH = Hkv == 1 ? 0 : Hkv == 2 ? 1 : Hkv == 4 ? 2 : 3;
+        // lanes 0..3 hold the page ids of the stage's 4 tiles, loaded one stage ahead
+        auto page_of = [&](int it) -> int {
+            const int tile = r.tile_lo + it * kTilesPerStage + lane;
+            return (lane < kTilesPerStage && tile < r.tile_hi)
+                       ? a.pt[(size_t)b * a.max_pages + tile * kTileTokens / a.page_size] : -1;
+        };
+        int pg_next = page_of(0);
+        bool ok = true;
+        for (int it = 0; it < n_iters && ok; ++it) {
+            const int pg_mine = pg_next;
+            pg_next = page_of(it + 1);
+            const int st = it % a.stages;
+            if (it >= a.stages && !mbar_wait(saddr(&bars[4 + st]), ((it / a.stages) - 1) & 1)) {
+                if (lane == 0) flag_status(a.status, OSCAR_DEV_WAIT_TIMEOUT);
+                ok = false;
+                break;
+            }
+            uint8_t *sb = stage0 + st * a.stage_bytes;
+            int mask = 0;
+            for (int j = 0; j < kTilesPerStage; ++j) {
+                const int tile = r.tile_lo + it * kTilesPerStage + j;
+                if (tile >= r.tile_hi) break;
+                const int pos0 = tile * kTileTokens;
+                const int page = __shfl_sync(0xffffffffu, pg_mine, j);
+                if (page < 0 || page >= a.pool.n_pages) {
+                    if (lane == 0) flag_status(a.status, OSCAR_DEV_BAD_INT2_PAGE);
+                    continue;
+                }
+                mask |= 1 << j;
+                const size_t row0 = (size_t)page * a.page_size + (pos0 % a.page_size);
+                const uint8_t *srck = a.pool.codes_k + row0 * Hkv * 32;
+                const uint8_t *srcv = a.pool.codes_v + row0 * Hkv * 32;
+                const int nck = 32 << lgH;              // 16-byte chunks: [slot][head][2 halves]
+                const uint32_t tile_dst = saddr(sb) + j * kTileTokens * 32;
+                for (int c = lane; c < nck; c += 32) {
+                    const int slot = c >> (lgH + 1), head = (c >> 1) & (Hkv - 1), half = c & 1;
+                    const uint32_t dst = tile_dst + head * 2048 + slot * 32 + half * 16;
+                    cp_async16(dst, srck + c * 16);
+                    cp_async16(dst + a.off_v, srcv + c * 16);
+                }
+                const int nsc = (2 * NGRP) << lgH;      // 16-byte chunks of one scale/zero array
+                const size_t soff = row0 * Hkv * NGRP;
+                const uint32_t sdst = saddr(sb + a.off_s) + j * nsc * 16;
+                for (int c = lane; c < nsc; c += 32) {
+                    cp_async16(sdst + c * 16, reinterpret_cast<const uint8_t *>(a.pool.scale_k + soff) + c * 16);
+                    cp_async16(sdst + a.arr_bytes + c * 16, reinterpret_cast<const uint8_t *>(a.pool.zero_k + soff) + c * 16);
+                    cp_async16(sdst + 2 * a.arr_bytes + c * 16,
+                               reinterpret_cast<const uint8_t *>(a.pool.scale_v + soff) + c * 16);
+                    cp_async16(sdst + 3 * a.arr_bytes + c * 16,
+                               reinterpret_cast<const uint8_t *>(a.pool.zero_v + soff) + c * 16);
+                }
+            }
+            if (lane == 0) masks[st] = mask;
+            cp_async_arrive(saddr(&bars[st]));
+            if (lane == 0) mbar_arrive(saddr(&bars[st]));
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        if (a.csize > 1) cluster_combine(a, reinterpret_cast<const float *>(stage0 + a.res_off), Hq, b);
+        return;
+    }
+
+    // ----------------------------------------------------------- consumers --
+    const int h = warp % Hkv, sub = warp / Hkv, nsub = kCW / Hkv;
+    const int gid = lane >> 2, t = lane & 3;
+
+    // B operand of QK: q_rot split into f16 hi/lo, divided by the code factor of its k-row.
+    uint32_t bq[NT][8][2];
+    float qz[NT][NGRP];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        const int hh = nt * 4 + (gid >> 1), part = gid & 1;
+        const bool valid = hh < G;
+        const float *qr = a.q_rot + ((size_t)b * Hq + h * G + (valid ? hh : 0)) * kHeadDim;
+#pragma unroll
+        for (int kap = 0; kap < 2; ++kap)
+#pragma unroll
+            for (int sg = 0; sg < 4; ++sg)
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int rr = 2 * sg + e, W = 2 * t + kap;
+                    const float inv = 1.0f / qk_factor(rr);
+                    const float v0 = valid ? qr[16 * W + rr] * inv : 0.f;
+                    const float v1 = valid ? qr[16 * W + 8 + rr] * inv : 0.f;
+                    bq[nt][kap * 4 + sg][e] = pack2(split_part(v0, part), split_part(v1, part));
+                }
+    }
+    // per-group sums of q_rot for the zero-point term, for the head this thread owns (nt*4 + t)
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int jg = 0; jg < NGRP; ++jg) qz[nt][jg] = 0.f;
+    for (int hh = 0; hh < G; ++hh) {
+        const float4 v = reinterpret_cast<const float4 *>(a.q_rot + ((size_t)b * Hq + h * G + hh) * kHeadDim)[lane];
+        const float sum4 = (v.x + v.y) + (v.z + v.w);
+        const int lg = (4 * lane) * NGRP / kHeadDim;
+#pragma unroll
+        for (int jg = 0; jg < NGRP; ++jg) {
+            float x = lg == jg ? sum4 : 0.f;
+#pragma unroll
+            for (int o = 16; o; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+                if (hh == nt * 4 + t) qz[nt][jg] = x * a.scale2;
+        }
+    }
+    const float csc = a.scale2 * kTwo24;
+    const int rs = Hkv * NGRP;                  // scale/zero elements per token row in a stage
+    const int arr_el = a.arr_bytes / 2;
+    __half *Ws = reinterpret_cast<__half *>(smem + 128 + warp * a.ws_bytes);
+
+    float m_run[NT], l_run[NT], zs[NT][NGRP];
+    float oacc[NT][8][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        m_run[nt] = -INFINITY;
+        l_run[nt] = 0.f;
+#pragma unroll
+        for (int jg = 0; jg < NGRP; ++jg) zs[nt][jg] = 0.f;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) oacc[nt][mt][c] = 0.f;
+    }
+
+    for (int it = 0; it < n_iters; ++it) {
+        const int st = it % a.stages;
+        if (!mbar_wait(saddr(&bars[st]), (it / a.stages) & 1)) {
+            if (lane == 0) flag_status(a.status, OSCAR_DEV_WAIT_TIMEOUT);
+            break;
+        }
+        const uint8_t *sb = stage0 + st * a.stage_bytes;
+        const int mask = masks[st];
+        // this warp's tiles of the stage: sub, sub + nsub, ...; taken two at a time (32 tokens)
+        for (int ja = sub; ja < kTilesPerStage; ja += 2 * nsub) {
+            const int jb_raw = ja + nsub;
+            const bool ua = (mask >> ja) & 1;
+            const bool ub = jb_raw < kTilesPerStage && ((mask >> jb_raw) & 1);
+            if (!ua && !ub) continue;
+            const int jt[2] = {ja, jb_raw < kTilesPerStage ? jb_raw : ja};
+            const bool uok[2] = {ua, ub};
+
+            // ---- S = K_codes . q_rot for both tiles (rows = tokens gid, gid+8; cols = 4 heads x hi/lo)
+            float sacc[2][NT][NGRP][4];
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int jg = 0; jg < NGRP; ++jg)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) sacc[u][nt][jg][c] = 0.f;
+            uint2 kw0[2], kw1[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const uint8_t *Kc = sb + h * 2048 + jt[u] * kTileTokens * 32;
+                kw0[u] = *reinterpret_cast<const uint2 *>(Kc + gid * 32 + 8 * t);
+                kw1[u] = *reinterpret_cast<const uint2 *>(Kc + (gid + 8) * 32 + 8 * t);
+            }
+#pragma unroll
+            for (int kap = 0; kap < 2; ++kap) {
+                const int gk = (2 * t + kap) * NGRP / 8;
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const uint32_t w0 = kap ? kw0[u].y : kw0[u].x, w1 = kap ? kw1[u].y : kw1[u].x;
+                    const uint32_t w0b = __byte_perm(w0, 0, 0x3321), w1b = __byte_perm(w1, 0, 0x3321);
+#pragma unroll
+                    for (int sg = 0; sg < 4; ++sg) {
+                        const uint32_t a0 = qk_reg(w0, w0b, 2 * sg), a1 = qk_reg(w1, w1b, 2 * sg);
+                        const uint32_t a2 = qk_reg(w0, w0b, 2 * sg + 1), a3 = qk_reg(w1, w1b, 2 * sg + 1);
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                            for (int jg = 0; jg < NGRP; ++jg) {
+                                const bool on = NGRP == 1 || gk == jg;
+                                mma16816(sacc[u][nt][jg], a0, a1, a2, a3, on ? bq[nt][kap * 4 + sg][0] : 0u,
+                                         on ? bq[nt][kap * 4 + sg][1] : 0u);
+                            }
+                    }
+                }
+            }
+
+            // ---- logits of 4 tokens per thread, online softmax over the 32 tokens, P*scale -> Ws
+            float alpha[NT];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                float tv[2][2];
+                bool vok[2][2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const uint16_t *sk = reinterpret_cast<const uint16_t *>(sb + a.off_s) +
+                                         jt[u] * kTileTokens * rs + h * NGRP;
+                    const int pos0 = (r.tile_lo + it * kTilesPerStage + jt[u]) * kTileTokens;
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int tok = gid + 8 * e, p = pos0 + tok;
+                        float tt = 0.f;
+#pragma unroll
+                        for (int jg = 0; jg < NGRP; ++jg) {
+                            const float sc = bf16_to_f32(sk[tok * rs + jg]), zc = bf16_to_f32(sk[arr_el + tok * rs + jg]);
+                            const float dot = sacc[u][nt][jg][2 * e] + sacc[u][nt][jg][2 * e + 1];
+                            tt += fmaf(sc * csc, dot, zc * qz[nt][jg]);
+                        }
+                        vok[u][e] = uok[u] && p >= r.lo && p < r.hi;
+                        tv[u][e] = vok[u][e] ? tt : -INFINITY;
+                    }
+                }
+                float mx = fmaxf(fmaxf(tv[0][0], tv[0][1]), fmaxf(tv[1][0], tv[1][1]));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                const float mn = fmaxf(m_run[nt], mx);
+                float pv[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, al = 1.f;
+                if (mn != -INFINITY) {
+                    al = exp2f(m_run[nt] - mn);
+#pragma unroll
+                    for (int u = 0; u < 2; ++u)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) pv[u][e] = exp2f(tv[u][e] - mn);
+                }
+                alpha[nt] = al;
+                m_run[nt] = mn;
+                l_run[nt] = fmaf(l_run[nt], al, (pv[0][0] + pv[0][1]) + (pv[1][0] + pv[1][1]));
+#pragma unroll
+                for (int jg = 0; jg < NGRP; ++jg) {
+                    float zadd = 0.f;
+                    __half *Wg = Ws + jg * NCOL * 32;
+                    const int c_hi = nt * 8 + 2 * t;
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const uint16_t *sk = reinterpret_cast<const uint16_t *>(sb + a.off_s) +
+                                             jt[u] * kTileTokens * rs + h * NGRP;
+#pragma unroll
+                        for (int e = 0; e < 2; ++e) {
+                            const int tok = gid + 8 * e;
+                            const float svv = bf16_to_f32(sk[2 * arr_el + tok * rs + jg]);
+                            const float zvv = bf16_to_f32(sk[3 * arr_el + tok * rs + jg]);
+                            const float w = vok[u][e] ? pv[u][e] * svv : 0.f;
+                            zadd += vok[u][e] ? pv[u][e] * zvv : 0.f;
+                            const int kc = u * 16 + kpos(tok);
+                            Wg[c_hi * 32 + kc] = split_part(w, 0);
+                            Wg[(c_hi + 1) * 32 + kc] = split_part(w, 1);
+                        }
+                    }
+                    zs[nt][jg] = fmaf(zs[nt][jg], al, zadd);
+                }
+            }
+            bool any = false;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) any |= alpha[nt] != 1.f;
+            if (__any_sync(0xffffffffu, any)) {
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) oacc[nt][mt][c] *= alpha[nt];
+            }
+            __syncwarp();
+
+            // ---- O += V_codes^T . (P*scale)  (rows = channels 16*gid + i, k = tokens, cols = heads x hi/lo)
+            const int gv = gid * NGRP / 8;
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                const uint8_t *Vc = sb + a.off_v + h * 2048 + jt[u] * kTileTokens * 32;
+                const uint32_t X = *reinterpret_cast<const uint32_t *>(Vc + t * 32 + 4 * gid);
+                const uint32_t Y = *reinterpret_cast<const uint32_t *>(Vc + (t + 4) * 32 + 4 * gid);
+                const uint32_t X2 = *reinterpret_cast<const uint32_t *>(Vc + (t + 8) * 32 + 4 * gid);
+                const uint32_t Y2 = *reinterpret_cast<const uint32_t *>(Vc + (t + 12) * 32 + 4 * gid);
+                const uint32_t P1 = __byte_perm(X, Y, 0x5410), P2 = __byte_perm(X, Y, 0x6521);
+                const uint32_t P3 = __byte_perm(X, Y, 0x7632), P4 = __byte_perm(X, Y, 0x7733);
+                const uint32_t Q1 = __byte_perm(X2, Y2, 0x5410), Q2 = __byte_perm(X2, Y2, 0x6521);
+                const uint32_t Q3 = __byte_perm(X2, Y2, 0x7632), Q4 = __byte_perm(X2, Y2, 0x7733);
+                uint32_t bw[NGRP][NT][2];
+#pragma unroll
+                for (int jg = 0; jg < NGRP; ++jg)
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) {
+                        const __half *col = Ws + jg * NCOL * 32 + (nt * 8 + gid) * 32 + u * 16;
+                        bw[jg][nt][0] = *reinterpret_cast<const uint32_t *>(col + 2 * t);
+                        bw[jg][nt][1] = *reinterpret_cast<const uint32_t *>(col + 2 * t + 8);
+                    }
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt) {
+                    const uint32_t a0 = pv_reg(P1, P2, P3, P4, 2 * mt), a1 = pv_reg(P1, P2, P3, P4, 2 * mt + 1);
+                    const uint32_t a2 = pv_reg(Q1, Q2, Q3, Q4, 2 * mt), a3 = pv_reg(Q1, Q2, Q3, Q4, 2 * mt + 1);
+#pragma unroll
+                    for (int jg = 0; jg < NGRP; ++jg) {
+                        const bool on = NGRP == 1 || gv == jg;
+#pragma unroll
+                        for (int nt = 0; nt < NT; ++nt)
+                            mma16816(oacc[nt][mt], on ? a0 : 0u, on ? a1 : 0u, on ? a2 : 0u, on ? a3 : 0u,
+                                     bw[jg][nt][0], bw[jg][nt][1]);
+                    }
+                }
+            }
+            __syncwarp();
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(saddr(&bars[4 + st]));
+    }
+
+    // ---- finish: reduce the per-thread sums over the 8 lanes of a column, scale the outputs
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+        for (int o = 4; o < 32; o <<= 1) {
+            l_run[nt] += __shfl_xor_sync(0xffffffffu, l_run[nt], o);
+#pragma unroll
+            for (int jg = 0; jg < NGRP; ++jg) zs[nt][jg] += __shfl_xor_sync(0xffffffffu, zs[nt][jg], o);
+        }
+    }
+    const int gv = gid * NGRP / 8;
+    float outv[NT][16];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        float z = zs[nt][0];
+#pragma unroll
+        for (int jg = 1; jg < NGRP; ++jg)
+            if (gv == jg) z = zs[nt][jg];
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            outv[nt][2 * mt] = fmaf(oacc[nt][mt][0] + oacc[nt][mt][1], kTwo24 / pv_factor(2 * mt), z);
+            outv[nt][2 * mt + 1] = fmaf(oacc[nt][mt][2] + oacc[nt][mt][3], kTwo24 / pv_factor(2 * mt + 1), z);
+        }
+    }
+
+    const size_t S1 = (size_t)S + 1;
+    // destination of this CTA's result: the partial slot (no cluster) or the shared result area
+    float *res = reinterpret_cast<float *>(stage0 + a.res_off);   // [Hq] m, [Hq] l, [Hq][128] acc
+    const bool to_res = a.csize > 1;
+    if (nsub == 1) {
+        if (to_res) consumer_sync();            // the result area overlaps the stages
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int hh = nt * 4 + t;
+            if (hh < G) {
+                const int hq = h * G + hh;
+                const size_t row = ((size_t)b * Hq + hq) * S1 + s;
+                float4 *dst = reinterpret_cast<float4 *>(to_res ? res + 2 * Hq + hq * kHeadDim + 16 * gid
+                                                                : a.out.acc + row * kHeadDim + 16 * gid);
+#pragma unroll
+                for (int q4 = 0; q4 < 4; ++q4)
+                    dst[q4] = make_float4(outv[nt][4 * q4], outv[nt][4 * q4 + 1], outv[nt][4 * q4 + 2],
+                                          outv[nt][4 * q4 + 3]);
+                if (gid == 0) {
+                    (to_res ? res + hq : a.out.m + row)[0] = m_run[nt];
+                    (to_res ? res + Hq + hq : a.out.l + row)[0] = l_run[nt];
+                }
+            }
+        }
+        if (to_res) cluster_combine(a, res, Hq, b);
+        return;
+    }
+
+    // several warps share a kv head: combine them in a fixed order (sub 0, 1, ...)
+    consumer_sync();                            // every consumer is done with the stages
+    float *cm = reinterpret_cast<float *>(stage0);               // [warp][NT*4] m
+    float *cl = cm + kCW * NT * 4;                               // [warp][NT*4] l
+    float *ca = cl + kCW * NT * 4;                               // [warp][NT*4][128] acc
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        if (gid == 0) {
+            cm[warp * NT * 4 + nt * 4 + t] = m_run[nt];
+            cl[warp * NT * 4 + nt * 4 + t] = l_run[nt];
+        }
+#pragma unroll
+        for (int i = 0; i < 16; ++i) ca[(warp * NT * 4 + nt * 4 + t) * kHeadDim + 16 * gid + i] = outv[nt][i];
+    }
+    consumer_sync();
+    if (sub == 0) {
+        // this warp (kv head h) combines warps h, h + Hkv, h + 2 Hkv, ...; lane = (head slot, channel block)
+        for (int e = lane; e < NT * 4 * kHeadDim / 4; e += 32) {
+            const int slot = e / (kHeadDim / 4), c4 = (e % (kHeadDim / 4)) * 4;
+            const int nt = slot / 4, hh = slot % 4 + nt * 4;
+            if (hh >= G) continue;
+            float M = -INFINITY;
+            for (int w = h; w < kCW; w += Hkv) M = fmaxf(M, cm[w * NT * 4 + slot]);
+            float L = 0.f, A0 = 0.f, A1 = 0.f, A2 = 0.f, A3 = 0.f;
+            if (M != -INFINITY) {
+                for (int w = h; w < kCW; w += Hkv) {
+                    const float f = exp2f(cm[w * NT * 4 + slot] - M);
+                    const float *src = ca + (w * NT * 4 + slot) * kHeadDim + c4;
+                    L = fmaf(cl[w * NT * 4 + slot], f, L);
+                    A0 = fmaf(src[0], f, A0);
+                    A1 = fmaf(src[1], f, A1);
+                    A2 = fmaf(src[2], f, A2);
+                    A3 = fmaf(src[3], f, A3);
+                }
+            }
+            const int hq = h * G + hh;
+            const size_t row = ((size_t)b * Hq + hq) * S1 + s;
+            *reinterpret_cast<float4 *>(to_res ? res + 2 * Hq + hq * kHeadDim + c4 : a.out.acc + row * kHeadDim + c4) =
+                make_float4(A0, A1, A2, A3);
+            if (c4 == 0) {
+                (to_res ? res + hq : a.out.m + row)[0] = M;
+                (to_res ? res + Hq + hq : a.out.l + row)[0] = L;
+            }
+        }
+    }
+    if (to_res) cluster_combine(a, res, Hq, b);
+}
+
+// Largest cluster size C in {8, 4, 2} whose co-resident clusters still occupy at least 90% of
+// the CTA slots of the GPU (clusters must fit inside one GPC); 1 if none does.  *active gets
+// the number of clusters (or CTAs when C = 1) that are resident at once.  Cached per kernel.
+int int2_cluster_size(const void *kern, int smem, int threads, int *active = nullptr) {
+    struct Entry { const void *k; int smem, dev, c, active; };
+    static thread_local Entry cache[32];
+    static thread_local int n_cache = 0;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    for (int i = 0; i < n_cache; ++i)
+        if (cache[i].k == kern && cache[i].smem == smem && cache[i].dev == dev) {
+            if (active) *active = cache[i].active;
+            return cache[i].c;
+        }
+    int best = 1, best_active = 1;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess) {
+        int sms = 0, per_sm = 0;
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
+        best_active = per_sm * sms > 0 ? per_sm * sms : 1;
+        for (int c = 8; c >= 2 && best == 1; c /= 2) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3(c * 64);
+            cfg.blockDim = dim3(threads);
+            cfg.dynamicSmemBytes = smem;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = c;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int ncl = 0;
+            if (cudaOccupancyMaxActiveClusters(&ncl, kern, &cfg) == cudaSuccess && 10 * ncl * c >= 9 * per_sm * sms) {
+                best = c;
+                best_active = ncl;
+            }
+        }
+        cudaGetLastError();
+    }
+    if (n_cache < 32) cache[n_cache++] = {kern, smem, dev, best, best_active};
+    if (active) *active = best_active;
+    return best;
+}
+
+// Shared-memory carve-up of the kernel for a layout; returns the dynamic smem bytes.
+template <int G, int NGRP>
+int mma_smem_plan(const oscar_layout_t &L, MmaArgs &a) {
+    constexpr int NT = (G == 8) ? 2 : 1;
+    const int Hkv = L.n_kv_heads, Hq = Hkv * G;
+    a.off_v = Hkv * 2048;
+    a.arr_bytes = kStageTok * Hkv * NGRP * 2;
+    a.off_s = 2 * a.off_v;
+    a.stage_bytes = (a.off_s + 4 * a.arr_bytes + 127) & ~127;
+    a.ws_bytes = NGRP * 8 * NT * 32 * 2;
+    a.stage_off = 128 + ((kCW * a.ws_bytes + 127) & ~127);
+    const int budget = (G == 8 ? 200 : 110) * 1024;    // two CTAs per SM below G = 8
+    int stages = kMaxStages;
+    while (stages > 2 && a.stage_off + stages * a.stage_bytes > budget) --stages;
+    a.stages = stages;
+    const int combine = (kCW / Hkv > 1) ? kCW * NT * 4 * (2 + kHeadDim) * 4 : 0;
+    a.res_off = combine;
+    const int tail = combine + Hq * (2 + kHeadDim) * 4;
+    return a.stage_off + (stages * a.stage_bytes > tail ? stages * a.stage_bytes : tail);
+}
+
+template <int G, int NGRP>
+int mma_cluster_size(const oscar_layout_t &L, int *active) {
+    MmaArgs a{};
+    const int smem = mma_smem_plan<G, NGRP>(L, a);
+    return int2_cluster_size(reinterpret_cast<const void *>(int2_mma_kernel<G, NGRP>), smem, kThreads, active);
+}
+
+template <int G, int NGRP>
+cudaError_t launch_mma(const oscar_layout_t &L, MmaArgs a, int batch, cudaStream_t st) {
+    const int smem = mma_smem_plan<G, NGRP>(L, a);
+    auto kern = int2_mma_kernel<G, NGRP>;
+    a.csize = int2_cluster_size(reinterpret_cast<const void *>(kern), smem, kThreads);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.out.S * a.csize, batch);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = a.csize;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a);
+}
+
+}  // namespace
+
+int int2_mma_cluster_size(const oscar_layout_t &L, int *active) {
+    int n = 0;
+    if (cudaGetDeviceCount(&n) != cudaSuccess || n == 0) {
+        cudaGetLastError();
+        if (active) *active = 0;
+        return 8;
+    }
+    const int ngrp = kHeadDim / L.group;
+#define OSCAR_CL_CASE(GG, NN) \
+    if (L.gqa == GG && ngrp == NN) return mma_cluster_size<GG, NN>(L, active);
+    OSCAR_CL_CASE(1, 1) OSCAR_CL_CASE(2, 1) OSCAR_CL_CASE(4, 1) OSCAR_CL_CASE(8, 1)
+    OSCAR_CL_CASE(1, 2) OSCAR_CL_CASE(2, 2) OSCAR_CL_CASE(4, 2) OSCAR_CL_CASE(8, 2)
+    OSCAR_CL_CASE(1, 4) OSCAR_CL_CASE(2, 4) OSCAR_CL_CASE(4, 4) OSCAR_CL_CASE(8, 4)
+#undef OSCAR_CL_CASE
+    return 1;
+}
+
+bool int2_mma_supported(const oscar_layout_t &L) {
+    const int H = L.n_kv_heads;
+    return (H == 1 || H == 2 || H == 4 || H == 8) && L.head_dim == kHeadDim;
+}
+
+cudaError_t launch_int2_attention_mma(const oscar_layout_t &L, const float *q_rot, Int2PoolView pool,
+                                      const int32_t *pt, int max_pages, const int32_t *seq_len,
+                                      const int32_t *hist_end, int batch, float sm_scale, PartialsView out,
+                                      int32_t *status, cudaStream_t st) {
+    if (batch <= 0) return cudaSuccess;
+    MmaArgs a{};
+    a.q_rot = q_rot;
+    a.pool = pool;
+    a.pt = pt;
+    a.max_pages = max_pages;
+    a.page_size = L.page_size;
+    a.n_kv = L.n_kv_heads;
+    a.sink = L.sink;
+    a.seq_len = seq_len;
+    a.hist_end = hist_end;
+    a.scale2 = sm_scale * kLog2e;
+    a.out = out;
+    a.status = status;
+    const int ngrp = kHeadDim / L.group;
+#define OSCAR_MMA_CASE(GG, NN) \
+    if (L.gqa == GG && ngrp == NN) return launch_mma<GG, NN>(L, a, batch, st);
+    OSCAR_MMA_CASE(1, 1) OSCAR_MMA_CASE(2, 1) OSCAR_MMA_CASE(4, 1) OSCAR_MMA_CASE(8, 1)
+    OSCAR_MMA_CASE(1, 2) OSCAR_MMA_CASE(2, 2) OSCAR_MMA_CASE(4, 2) OSCAR_MMA_CASE(8, 2)
+    OSCAR_MMA_CASE(1, 4) OSCAR_MMA_CASE(2, 4) OSCAR_MMA_CASE(4, 4) OSCAR_MMA_CASE(8, 4)
+#undef OSCAR_MMA_CASE
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace oscar

@@ -111,7 +111,7 @@ __global__ void __launch_bounds__(128) int2_split_kernel(Int2Args a) {
     const int n_q_heads = a.n_kv * G, S = a.out.S;
     int T, he;
     read_lengths(a.seq_len, a.hist_end, b, a.sink, a.max_pages * a.page_size, a.status, T, he);
-    const SplitRange r = history_split(a.sink, he, a.page_size, S, s);
+    const SplitRange r = history_split(a.sink, he, S, s);
 
     float q[G][4];
 #pragma unroll
@@ -177,7 +177,7 @@ __global__ void __launch_bounds__(128) bf16_split_kernel(Bf16Args a) {
         lo0 = 0; hi0 = min(a.sink, T);
         lo1 = max(he, hi0); hi1 = T;
     } else {
-        const SplitRange r = full_split(T, a.page_size, S, s);
+        const SplitRange r = full_split(T, S, s);
         lo0 = r.lo; hi0 = r.hi; lo1 = hi1 = 0;
     }
     float q[G][4];
@@ -251,6 +251,9 @@ cudaError_t launch_int2_attention(const oscar_layout_t &L, const float *q_rot, I
                                   const int32_t *hist_end, int batch, float sm_scale, PartialsView out,
                                   int32_t *status, cudaStream_t st) {
     if (batch <= 0) return cudaSuccess;
+    if (int2_mma_supported(L))
+        return launch_int2_attention_mma(L, q_rot, pool, pt, max_pages, seq_len, hist_end, batch, sm_scale, out,
+                                         status, st);
     Int2Args a{q_rot, pool, pt, max_pages, L.page_size, L.n_kv_heads, L.group, L.sink, seq_len, hist_end,
                sm_scale * kLog2e, out, status};
     return launch_g<Int2Launcher>(L.gqa, dim3(out.S, L.n_kv_heads, batch), a, st);
@@ -261,6 +264,9 @@ cudaError_t launch_bf16_attention(const oscar_layout_t &L, const uint16_t *q, Bf
                                   const int32_t *hist_end, int batch, float sm_scale, PartialsView out,
                                   int mode, int32_t *status, cudaStream_t st) {
     if (batch <= 0) return cudaSuccess;
+    if (bf16_mma_supported(L, mode))
+        return launch_bf16_attention_mma(L, q, pool, pt, max_pages, seq_len, hist_end, batch, sm_scale, out, mode,
+                                         status, st);
     Bf16Args a{q, pool, pt, max_pages, L.page_size, L.n_kv_heads, L.sink, seq_len, hist_end,
                sm_scale * kLog2e, out, mode, status};
     return launch_g<Bf16Launcher>(L.gqa, dim3(mode == 0 ? 1 : out.S, L.n_kv_heads, batch), a, st);

@@ -184,18 +184,29 @@ __global__ void __launch_bounds__(kThreads) quantize_rows_kernel(const float *x,
                        zero + (size_t)r * gpr, red);
 }
 
-// grid.x = batch * Hq; thread j computes q_rot[j] = fma-chain_i q[i] * R[i][j].
-__global__ void __launch_bounds__(kThreads) rotate_q_kernel(const uint16_t *q, const float *RK, int n_q_heads,
-                                                            int gqa, float *q_rot) {
-    __shared__ float qs[kHeadDim];
-    const int row = blockIdx.x, hq = row % n_q_heads, j = threadIdx.x;
-    qs[j] = bf16_to_f32(q[(size_t)row * kHeadDim + j]);
+// grid.x = batch * n_kv * 4 (a quarter of the 128 output channels per CTA), 32*G threads;
+// thread (g, j) computes q_rot[g][c] = fma-chain_i q[g][i] * R[i][c] for c = 32*quarter + j.
+// The CTA first stages its 128 x 32 block of R in shared memory with independent vector loads.
+template <int G>
+__global__ void __launch_bounds__(32 * G) rotate_q_kernel(const uint16_t *q, const float *RK, int n_kv,
+                                                         float *q_rot) {
+    __shared__ float qs[G][kHeadDim];
+    __shared__ __align__(16) float Rs[kHeadDim][32];
+    const int quarter = blockIdx.x & 3, bh = blockIdx.x >> 2;
+    const int b = bh / n_kv, h = bh % n_kv;
+    const int tid = threadIdx.x, g = tid >> 5, j = tid & 31;
+    const size_t row0 = ((size_t)b * n_kv + h) * G;        // first query row of this kv head
+    const float *R = RK + (size_t)h * kHeadDim * kHeadDim + quarter * 32;
+    for (int e = tid; e < kHeadDim * 8; e += 32 * G) {       // 128 rows x 8 float4
+        const int i = e >> 3, c4 = e & 7;
+        reinterpret_cast<float4 *>(&Rs[i][0])[c4] = __ldg(reinterpret_cast<const float4 *>(R + i * kHeadDim) + c4);
+    }
+    for (int e = tid; e < G * kHeadDim; e += 32 * G) qs[e / kHeadDim][e % kHeadDim] = bf16_to_f32(q[row0 * kHeadDim + e]);
     __syncthreads();
-    const float *R = RK + (size_t)(hq / gqa) * kHeadDim * kHeadDim;
     float acc = 0.0f;
-#pragma unroll 8
-    for (int i = 0; i < kHeadDim; ++i) acc = __fmaf_rn(qs[i], __ldg(R + i * kHeadDim + j), acc);
-    q_rot[(size_t)row * kHeadDim + j] = acc;
+#pragma unroll 16
+    for (int i = 0; i < kHeadDim; ++i) acc = __fmaf_rn(qs[g][i], Rs[i][j], acc);
+    q_rot[(row0 + g) * kHeadDim + quarter * 32 + j] = acc;
 }
 
 }  // namespace
@@ -254,9 +265,15 @@ cudaError_t launch_quantize_rotated(const oscar_layout_t &L, const float *x, int
 
 cudaError_t launch_rotate_q(const oscar_layout_t &L, const uint16_t *q, const float *RK, int batch,
                             float *q_rot, cudaStream_t st) {
-    const int hq = L.n_kv_heads * L.gqa;
     if (batch <= 0) return cudaSuccess;
-    rotate_q_kernel<<<batch * hq, kThreads, 0, st>>>(q, RK, hq, L.gqa, q_rot);
+    const dim3 grid(batch * L.n_kv_heads * 4);
+    switch (L.gqa) {
+        case 1: rotate_q_kernel<1><<<grid, 32, 0, st>>>(q, RK, L.n_kv_heads, q_rot); break;
+        case 2: rotate_q_kernel<2><<<grid, 64, 0, st>>>(q, RK, L.n_kv_heads, q_rot); break;
+        case 4: rotate_q_kernel<4><<<grid, 128, 0, st>>>(q, RK, L.n_kv_heads, q_rot); break;
+        case 8: rotate_q_kernel<8><<<grid, 256, 0, st>>>(q, RK, L.n_kv_heads, q_rot); break;
+        default: return cudaErrorInvalidValue;
+    }
     return cudaGetLastError();
 }
 

@@ -7,12 +7,14 @@
 // stored rotated by R_V = U_S·H·P_br, so the history part of the output is
 // brought back with R_V^T.
 //
-// The fold is an ordered fp32 sequence with explicit round-to-nearest
+// The combination is an ordered fp32 computation with explicit round-to-nearest
 // intrinsics and its own 2^x, so that equal partials give equal output bits:
-//   M' = max(M, m_i); a = 2^(M - M'); b = 2^(m_i - M');
-//   L = fma(L, a, l_i*b); A_d = fma(A_d, a, acc_i,d*b)
-// history slots 0..S-1 in ascending order, then A'_j = fma-chain_i A_i*R_V[j][i],
-// then the BF16 slot S, then o = A'/L (IEEE division), rounded to bf16.
+//   M = max of m_i over the non-empty partials (history and BF16), w_i = 2^(m_i - M);
+//   L = fma(l_i, w_i, L), A_d = fma(acc_i,d, w_i, A_d) over history slots 0..S-1 ascending;
+//   A'_j = fma-chain_i A_i * R_V[j][i]; then the BF16 slot S with its weight;
+//   o = A'/L (IEEE division), rounded to bf16.
+// Taking the global maximum first (rather than a running one) keeps the weights
+// independent, so they are computed in parallel and the sums are plain FMA chains.
 
 #include "oscar_internal.cuh"
 
@@ -42,58 +44,73 @@ __device__ __forceinline__ float exp2_taylor(float x) {
 
 constexpr int kPad = kHeadDim + 1;   // R_V rows padded: thread j reads row j conflict-free
 
-// grid = (n_kv, batch); 128 threads, thread j owns output channel j.
-__global__ void __launch_bounds__(128) merge_kernel(PartialsView p, const float *RV, int n_kv, int gqa,
+// grid = (Hq, batch); 128 threads, thread j owns output channel j of one query head.
+// Dynamic smem: [R_V 128 x 129 if RV] [A 128] [w S+1] [l S+1] [red 8].
+__global__ void __launch_bounds__(128) merge_kernel(PartialsView p, const float *RV, int n_q_heads, int gqa,
                                                     uint16_t *out, float *out_f32, float *lse) {
     extern __shared__ __align__(16) float smem[];
-    float *Rs = smem;                                  // [128][129] if RV
-    float *As = smem + (RV ? kHeadDim * kPad : 0);     // [128]
-    const int kvh = blockIdx.x, b = blockIdx.y, j = threadIdx.x;
-    const int S = p.S, n_q_heads = n_kv * gqa;
+    const int hq = blockIdx.x, b = blockIdx.y, j = threadIdx.x;
+    const int S = p.S;
+    float *Rs = smem;
+    float *As = smem + (RV ? kHeadDim * kPad : 0);
+    float *ws = As + kHeadDim;
+    float *ls = ws + (S + 1);
+    float *red = ls + (S + 1);
+    const size_t row0 = ((size_t)b * n_q_heads + hq) * (S + 1);
+
+    float mloc = -INFINITY;
+    for (int i = j; i <= S; i += 128) {
+        const float li = p.l[row0 + i], mi = p.m[row0 + i];
+        ls[i] = li;
+        ws[i] = mi;
+        if (li > 0.0f && mi > mloc) mloc = mi;
+    }
+#pragma unroll
+    for (int o = 16; o; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
+    if ((j & 31) == 0) red[j >> 5] = mloc;
     if (RV) {
-        const float *R = RV + (size_t)kvh * kHeadDim * kHeadDim;
-        for (int i = 0; i < kHeadDim; ++i) Rs[i * kPad + j] = __ldg(R + i * kHeadDim + j);
-    }
-    for (int g = 0; g < gqa; ++g) {
-        const size_t row0 = ((size_t)b * n_q_heads + kvh * gqa + g) * (S + 1);
-        float M = -INFINITY, L = 0.0f, A = 0.0f;
-        for (int i = 0; i < S; ++i) {
-            const float li = p.l[row0 + i];
-            if (!(li > 0.0f)) continue;
-            const float mi = p.m[row0 + i];
-            const float Mn = mi > M ? mi : M;
-            const float a = exp2_taylor(__fsub_rn(M, Mn));
-            const float bb = exp2_taylor(__fsub_rn(mi, Mn));
-            L = __fmaf_rn(L, a, __fmul_rn(li, bb));
-            A = __fmaf_rn(A, a, __fmul_rn(p.acc[(row0 + i) * kHeadDim + j], bb));
-            M = Mn;
-        }
-        float Ar = A;
-        if (RV) {
-            __syncthreads();
-            As[j] = A;
-            __syncthreads();
-            float r = 0.0f;
+        const float4 *R = reinterpret_cast<const float4 *>(RV + (size_t)(hq / gqa) * kHeadDim * kHeadDim);
 #pragma unroll 8
-            for (int i = 0; i < kHeadDim; ++i) r = __fmaf_rn(As[i], Rs[j * kPad + i], r);
-            Ar = r;
+        for (int e = j; e < kHeadDim * kHeadDim / 4; e += 128) {
+            const float4 v = __ldg(R + e);
+            float *dst = Rs + (e >> 5) * kPad + (e & 31) * 4;
+            dst[0] = v.x; dst[1] = v.y; dst[2] = v.z; dst[3] = v.w;
         }
-        const float lS = p.l[row0 + S];
-        if (lS > 0.0f) {
-            const float mS = p.m[row0 + S];
-            const float Mn = mS > M ? mS : M;
-            const float a = exp2_taylor(__fsub_rn(M, Mn));
-            const float bb = exp2_taylor(__fsub_rn(mS, Mn));
-            L = __fmaf_rn(L, a, __fmul_rn(lS, bb));
-            Ar = __fmaf_rn(Ar, a, __fmul_rn(p.acc[(row0 + S) * kHeadDim + j], bb));
-            M = Mn;
-        }
-        const float o = L > 0.0f ? __fdiv_rn(Ar, L) : 0.0f;
-        const size_t orow = (size_t)b * n_q_heads + kvh * gqa + g;
-        if (out) out[orow * kHeadDim + j] = f32_to_bf16_rn(o);
-        if (out_f32) out_f32[orow * kHeadDim + j] = o;
-        if (lse && j == 0) lse[orow] = L > 0.0f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
     }
+    __syncthreads();
+    const float M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+    for (int i = j; i <= S; i += 128) ws[i] = ls[i] > 0.0f ? exp2_taylor(__fsub_rn(ws[i], M)) : 0.0f;
+    __syncthreads();
+
+    float L = 0.0f, A = 0.0f;
+    const float *acc = p.acc + row0 * kHeadDim + j;
+#pragma unroll 8
+    for (int i = 0; i < S; ++i) {            // empty slots are skipped by select, so loads issue early
+        const float li = ls[i], w = ws[i];
+        const float x = acc[(size_t)i * kHeadDim];
+        const bool on = li > 0.0f;
+        L = on ? __fmaf_rn(li, w, L) : L;
+        A = on ? __fmaf_rn(x, w, A) : A;
+    }
+    float Ar = A;
+    if (RV) {
+        As[j] = A;
+        __syncthreads();
+        float r = 0.0f;
+#pragma unroll 8
+        for (int i = 0; i < kHeadDim; ++i) r = __fmaf_rn(As[i], Rs[j * kPad + i], r);
+        Ar = r;
+    }
+    if (ls[S] > 0.0f) {
+        const float w = ws[S];
+        L = __fmaf_rn(ls[S], w, L);
+        Ar = __fmaf_rn(acc[(size_t)S * kHeadDim], w, Ar);
+    }
+    const float o = L > 0.0f ? __fdiv_rn(Ar, L) : 0.0f;
+    const size_t orow = (size_t)b * n_q_heads + hq;
+    if (out) out[orow * kHeadDim + j] = f32_to_bf16_rn(o);
+    if (out_f32) out_f32[orow * kHeadDim + j] = o;
+    if (lse && j == 0) lse[orow] = L > 0.0f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
 }
 
 }  // namespace
@@ -101,17 +118,17 @@ __global__ void __launch_bounds__(128) merge_kernel(PartialsView p, const float 
 cudaError_t launch_merge(const oscar_layout_t &L, PartialsView p, const float *RV, int batch, uint16_t *out,
                          float *out_f32, float *lse, cudaStream_t st) {
     if (batch <= 0) return cudaSuccess;
-    const size_t smem = sizeof(float) * ((RV ? kHeadDim * kPad : 0) + kHeadDim);
-    static thread_local int configured_device = -1;
+    const int hq = L.n_kv_heads * L.gqa;
+    const size_t smem = sizeof(float) * ((RV ? kHeadDim * kPad : 0) + kHeadDim + 2 * (p.S + 1) + 8);
+    static thread_local int configured[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
-    if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)(sizeof(float) * (kHeadDim * kPad + kHeadDim)));
+    if (dev < 64 && configured[dev] < (int)smem) {
+        cudaError_t e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        configured_device = dev;
+        configured[dev] = (int)smem;
     }
-    merge_kernel<<<dim3(L.n_kv_heads, batch), 128, smem, st>>>(p, RV, L.n_kv_heads, L.gqa, out, out_f32, lse);
+    merge_kernel<<<dim3(hq, batch), 128, smem, st>>>(p, RV, hq, L.gqa, out, out_f32, lse);
     return cudaGetLastError();
 }
 

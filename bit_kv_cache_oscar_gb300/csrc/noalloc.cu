@@ -56,8 +56,8 @@ extern "C" oscar_status_t oscar_decode_attention_noalloc(
     int32_t max_pages_per_req, const int32_t *seq_len, const int32_t *hist_end, int32_t batch, float sm_scale,
     int32_t n_splits, const float *R_V, uint16_t *out, float *out_f32, float *lse, void *stream) {
     if (!layout) return oscar::set_last_error(OSCAR_ERR_INVALID_ARG, "layout is NULL");
-    if (batch < 0 || n_splits < 1 || n_splits > 256)
-        return oscar::set_last_error(OSCAR_ERR_INVALID_ARG, "batch < 0 or n_splits outside 1..256");
+    if (batch < 0 || n_splits < 1 || n_splits > 1024)
+        return oscar::set_last_error(OSCAR_ERR_INVALID_ARG, "batch < 0 or n_splits outside 1..1024");
     if (batch == 0) return OSCAR_OK;
     const size_t ml = oscar_partials_ml_floats(layout, batch, n_splits);
     const size_t acc = oscar_partials_acc_floats(layout, batch, n_splits);

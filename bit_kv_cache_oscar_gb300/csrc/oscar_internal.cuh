@@ -23,39 +23,38 @@ __device__ __forceinline__ void flag_status(int32_t *status, int32_t bit) {
     if (status) atomicOr(status, bit);
 }
 
-// Page-aligned split of the history [sink, h_end) of one request: split s of S
-// covers logical pages [first + s*per, first + (s+1)*per) clipped to the history.
+constexpr int kTileTokens = 16;   // split granularity: 16-token tiles at absolute positions 16i..16i+15
+
+// Balanced split of [lo_tok, hi_tok) into S parts of whole tiles: with first = lo_tok/16 and
+// n = ceil(hi_tok/16) - first tiles, part s covers tiles [first + floor(s*n/S), first +
+// floor((s+1)*n/S)), clipped to [lo_tok, hi_tok).  lo_tok must be a multiple of 16.
 struct SplitRange {
     int lo, hi;   // token range [lo, hi), empty if lo >= hi
+    int tile_lo, tile_hi;
 };
 
-__device__ __forceinline__ SplitRange history_split(int sink, int h_end, int page_size, int S, int s) {
-    int first = sink / page_size;
-    int last = (h_end + page_size - 1) / page_size;
-    int n = last - first;
-    SplitRange r{0, 0};
+__device__ __forceinline__ SplitRange tile_split(int lo_tok, int hi_tok, int S, int s) {
+    SplitRange r{0, 0, 0, 0};
+    const int first = lo_tok / kTileTokens;
+    const int n = (hi_tok + kTileTokens - 1) / kTileTokens - first;
     if (n <= 0) return r;
-    int per = (n + S - 1) / S;
-    int a = (first + s * per) * page_size;
-    int b = (first + (s + 1) * per) * page_size;
-    r.lo = a > sink ? a : sink;
-    r.hi = b < h_end ? b : h_end;
-    if (r.lo >= r.hi) r.lo = r.hi = 0;
+    const int a = first + (int)(((long long)s * n) / S);
+    const int b = first + (int)(((long long)(s + 1) * n) / S);
+    r.lo = a * kTileTokens > lo_tok ? a * kTileTokens : lo_tok;
+    r.hi = b * kTileTokens < hi_tok ? b * kTileTokens : hi_tok;
+    r.tile_lo = a;
+    r.tile_hi = b;
+    if (r.lo >= r.hi) r.lo = r.hi = r.tile_lo = r.tile_hi = 0;
     return r;
+}
+
+// History split s of S of one request: [sink, h_end) (sink is a multiple of 16).
+__device__ __forceinline__ SplitRange history_split(int sink, int h_end, int S, int s) {
+    return tile_split(sink, h_end, S, s);
 }
 
 // Same rule over [0, T) for the all-BF16 comparison kernel.
-__device__ __forceinline__ SplitRange full_split(int T, int page_size, int S, int s) {
-    int n = (T + page_size - 1) / page_size;
-    SplitRange r{0, 0};
-    if (n <= 0) return r;
-    int per = (n + S - 1) / S;
-    r.lo = s * per * page_size;
-    int b = (s + 1) * per * page_size;
-    r.hi = b < T ? b : T;
-    if (r.lo >= r.hi) r.lo = r.hi = 0;
-    return r;
-}
+__device__ __forceinline__ SplitRange full_split(int T, int S, int s) { return tile_split(0, T, S, s); }
 
 // Clamp the per-request lengths the way every kernel reads them; flags bad input.
 __device__ __forceinline__ void read_lengths(const int32_t *seq_len, const int32_t *hist_end, int b, int sink,
@@ -110,6 +109,23 @@ cudaError_t launch_int2_attention(const oscar_layout_t &L, const float *q_rot, I
                                   const int32_t *pt, int max_pages, const int32_t *seq_len,
                                   const int32_t *hist_end, int batch, float sm_scale, PartialsView out,
                                   int32_t *status, cudaStream_t st);
+
+// Tensor-core INT2 kernel (n_kv_heads in {1, 2, 4, 8}); launch_int2_attention dispatches to it.
+bool int2_mma_supported(const oscar_layout_t &L);
+// CTAs per cluster the tensor-core INT2 kernel will use for this layout (8 if no device is
+// visible); *active (optional) gets how many such clusters are resident at once (0 if unknown).
+int int2_mma_cluster_size(const oscar_layout_t &L, int *active = nullptr);
+cudaError_t launch_int2_attention_mma(const oscar_layout_t &L, const float *q_rot, Int2PoolView pool,
+                                      const int32_t *pt, int max_pages, const int32_t *seq_len,
+                                      const int32_t *hist_end, int batch, float sm_scale, PartialsView out,
+                                      int32_t *status, cudaStream_t st);
+
+// Tensor-core BF16 kernel (mode 0 any n_kv_heads; mode 1 n_kv_heads in {1, 2, 4, 8}).
+bool bf16_mma_supported(const oscar_layout_t &L, int mode);
+cudaError_t launch_bf16_attention_mma(const oscar_layout_t &L, const uint16_t *q, Bf16PoolView pool,
+                                      const int32_t *pt, int max_pages, const int32_t *seq_len,
+                                      const int32_t *hist_end, int batch, float sm_scale, PartialsView out,
+                                      int mode, int32_t *status, cudaStream_t st);
 
 // mode 0: sink + recent of each request into slot S; mode 1: all of [0, T) split S ways.
 cudaError_t launch_bf16_attention(const oscar_layout_t &L, const uint16_t *q, Bf16PoolView pool,

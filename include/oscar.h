@@ -127,7 +127,7 @@ typedef struct {
  *   acc fp32 [batch][Hq][n_splits + 1][head_dim]  sum of 2^(t - m)·value
  * Slots 0..n_splits-1 are history splits in ascending token order (values in
  * the ROTATED basis); slot n_splits is the BF16 partial (unrotated).  An empty
- * slot has m = -inf, l = 0, acc = 0.  n_splits in 1..256.
+ * slot has m = -inf, l = 0, acc = 0.  n_splits in 1..1024.
  */
 typedef struct {
     float *m;
@@ -142,8 +142,12 @@ OSCAR_API size_t oscar_partials_acc_floats(const oscar_layout_t *layout, int32_t
 
 /*
  * A split count that fills the GPU for `batch` requests whose longest history
- * spans max_hist_tokens tokens: about two waves of CTAs over `sm_count` SMs,
- * at least one history page per split, clamped to [1, 256].
+ * spans max_hist_tokens tokens, in one wave: each split is computed by a
+ * cluster of up to 8 CTAs that combine their results before writing the
+ * split's partial, and the count is the number of such clusters the current
+ * device keeps resident at once divided by `batch` (sm_count is used when no
+ * device is visible); at least one 16-token history tile per split, clamped
+ * to [1, 1024].
  */
 OSCAR_API int32_t oscar_suggest_splits(const oscar_layout_t *layout, int32_t batch, int32_t max_hist_tokens,
                              int32_t sm_count);
@@ -205,9 +209,12 @@ OSCAR_API oscar_status_t oscar_rotate_q(const oscar_layout_t *layout, const uint
  *   seq_len  int32 [batch] T (current token included), 1 <= T <= max_pages_per_req·page_size
  *   hist_end int32 [batch] h, sink <= h <= T (values outside are clamped and flagged)
  *   sm_scale softmax scale (1/sqrt(head_dim) for standard attention)
- * Writes every slot of `partials` for every (request, query head):
- * history [sink, h) cut into partials->n_splits page-aligned splits of
- * ceil(pages / n_splits) pages, and the BF16 partial over [0, sink) ∪ [h, T).
+ * Writes every slot of `partials` for every (request, query head): the
+ * history [sink, h) is cut into partials->n_splits contiguous splits of whole
+ * 16-token tiles (tile i = positions 16i..16i+15): with first = sink/16 and
+ * n = ceil(h/16) - first, split s covers tiles [first + floor(s·n/S),
+ * first + floor((s+1)·n/S)) clipped to [sink, h); the BF16 partial covers
+ * [0, sink) ∪ [h, T).
  */
 OSCAR_API oscar_status_t oscar_decode_attention(const oscar_layout_t *layout,
                                       const uint16_t *q, const float *q_rot,
@@ -218,14 +225,35 @@ OSCAR_API oscar_status_t oscar_decode_attention(const oscar_layout_t *layout,
                                       float sm_scale, const oscar_partials_t *partials, void *stream);
 
 /*
+ * The two halves of oscar_decode_attention, for callers that run them on two
+ * streams so that they overlap (they write disjoint slots of `partials`):
+ * _history writes the history slots 0..S-1 from the INT2 pool and q_rot;
+ * _window writes the BF16 slot S (sink + recent) from the BF16 pool and q.
+ * Arguments as for oscar_decode_attention.
+ */
+OSCAR_API oscar_status_t oscar_decode_attention_history(const oscar_layout_t *layout, const float *q_rot,
+                                                        const oscar_int2_pool_t *int2_pool,
+                                                        const int32_t *int2_page_table, int32_t max_pages_per_req,
+                                                        const int32_t *seq_len, const int32_t *hist_end,
+                                                        int32_t batch, float sm_scale,
+                                                        const oscar_partials_t *partials, void *stream);
+OSCAR_API oscar_status_t oscar_decode_attention_window(const oscar_layout_t *layout, const uint16_t *q,
+                                                       const oscar_bf16_pool_t *bf16_pool,
+                                                       const int32_t *bf16_page_table, int32_t max_pages_per_req,
+                                                       const int32_t *seq_len, const int32_t *hist_end,
+                                                       int32_t batch, float sm_scale,
+                                                       const oscar_partials_t *partials, void *stream);
+
+/*
  * Online-softmax merge ([news] "online softmax merge"): per (request, query
- * head), fold history slots 0..S-1 in ascending order, rotate that
- * accumulator back by R_V[h / gqa]^T, fold the BF16 slot S, divide by the
- * total weight.  The fold is the ordered fp32 sequence
- *   M' = max(M, m_i); a = 2^(M - M'); b = 2^(m_i - M');
- *   L = fma(L, a, l_i·b); A_d = fma(A_d, a, acc_i,d·b)
+ * head), combine history slots 0..S-1 in ascending order, rotate that
+ * accumulator back by R_V[h / gqa]^T, add the BF16 slot S, divide by the
+ * total weight.  The fixed fp32 order (equal partials give equal bits):
+ *   M = max m_i over non-empty slots (l_i > 0), w_i = 2^(m_i - M);
+ *   L = fma(l_i, w_i, L); A_d = fma(acc_i,d, w_i, A_d) for i = 0..S-1;
+ *   A'_j = fma-chain over i of A_i·R_V[j][i]; then slot S with w_S; o = A'/L,
  * with 2^x computed by Cody–Waite reduction and a degree-7 Taylor polynomial
- * (not the hardware approximation), so that equal partials give equal bits.
+ * (not the hardware approximation).
  *   R_V  fp32 [n_kv_heads][head_dim][head_dim], or NULL for an all-BF16
  *        cache (then no slot is rotated).
  *   out      NULL or bf16 [batch][Hq][head_dim]: o rounded to nearest even.
@@ -240,8 +268,9 @@ OSCAR_API oscar_status_t oscar_merge(const oscar_layout_t *layout, const oscar_p
 /*
  * Comparison kernel: decode attention over an all-BF16 paged cache (no INT2
  * history, no rotation), same split-K structure.  Positions [0, T) are cut
- * into partials->n_splits page-aligned splits written to slots 0..S-1; slot
- * S is written empty.  Merge with oscar_merge(..., R_V = NULL, ...).
+ * into partials->n_splits splits of whole 16-token tiles by the rule of
+ * oscar_decode_attention (with first = 0) into slots 0..S-1; slot S is
+ * written empty.  Merge with oscar_merge(..., R_V = NULL, ...).
  */
 OSCAR_API oscar_status_t oscar_bf16_decode_attention(const oscar_layout_t *layout, const uint16_t *q,
                                            const oscar_bf16_pool_t *pool, const int32_t *page_table,

@@ -397,14 +397,16 @@ float ora_exp2f(float x) {
 }
 
 /*
- * The merge as an ordered fp32 fold, the exact sequence of roundings that the
- * CUDA merge kernel must reproduce:
- *   M = -inf, L = 0, A = 0
- *   for i = 0..S-1 with l_i > 0 (history splits in ascending token order):
- *       M' = max(M, m_i); a = 2^(M - M'); b = 2^(m_i - M')
- *       L = fma(L, a, l_i*b);  A_d = fma(A_d, a, acc_i,d * b);  M = M'
+ * The merge as an ordered fp32 computation, the exact sequence of roundings
+ * that the CUDA merge kernel must reproduce (a fixed order of the online-
+ * softmax combination: global maximum first, so that the weights are
+ * independent of each other):
+ *   M = max of m_i over the non-empty partials (l_i > 0), i = 0..S
+ *   w_i = 2^(m_i - M)
+ *   L = 0, A = 0; for i = 0..S-1 with l_i > 0 (history splits, ascending):
+ *       L = fma(l_i, w_i, L);  A_d = fma(acc_i,d, w_i, A_d)
  *   if RV: A'_j = fma-chain over i ascending of A_i * RV[j][i] (A · R_V^T), else A' = A
- *   BF16 partial (index S), if l_S > 0: same fold step on (L, A', M)
+ *   BF16 partial (index S), if l_S > 0: L = fma(l_S, w_S, L); A'_d = fma(acc_S,d, w_S, A'_d)
  *   o_j = A'_j / L (IEEE division), out_bf16 = bf16_rne(o_j)
  * 2^x is ora_exp2f.  If every l is 0 the output is 0.
  */
@@ -413,14 +415,13 @@ void ora_merge_f32(int D, int S, const float *m2, const float *l, const float *a
     float M = -INFINITY, L = 0.0f;
     float *A = (float *)calloc(D, sizeof(float));
     float *Ar = (float *)calloc(D, sizeof(float));
+    for (int i = 0; i <= S; ++i)
+        if (l[i] > 0.0f && m2[i] > M) M = m2[i];
     for (int i = 0; i < S; ++i) {
         if (!(l[i] > 0.0f)) continue;
-        float Mn = m2[i] > M ? m2[i] : M;
-        float a = ora_exp2f(M - Mn);
-        float b = ora_exp2f(m2[i] - Mn);
-        L = fmaf(L, a, l[i] * b);
-        for (int d = 0; d < D; ++d) A[d] = fmaf(A[d], a, acc[(size_t)i * D + d] * b);
-        M = Mn;
+        float w = ora_exp2f(m2[i] - M);
+        L = fmaf(l[i], w, L);
+        for (int d = 0; d < D; ++d) A[d] = fmaf(acc[(size_t)i * D + d], w, A[d]);
     }
     if (RV) {
         for (int j = 0; j < D; ++j) {
@@ -432,12 +433,9 @@ void ora_merge_f32(int D, int S, const float *m2, const float *l, const float *a
         memcpy(Ar, A, sizeof(float) * D);
     }
     if (l[S] > 0.0f) {
-        float Mn = m2[S] > M ? m2[S] : M;
-        float a = ora_exp2f(M - Mn);
-        float b = ora_exp2f(m2[S] - Mn);
-        L = fmaf(L, a, l[S] * b);
-        for (int d = 0; d < D; ++d) Ar[d] = fmaf(Ar[d], a, acc[(size_t)S * D + d] * b);
-        M = Mn;
+        float w = ora_exp2f(m2[S] - M);
+        L = fmaf(l[S], w, L);
+        for (int d = 0; d < D; ++d) Ar[d] = fmaf(acc[(size_t)S * D + d], w, Ar[d]);
     }
     for (int j = 0; j < D; ++j) {
         float o = (L > 0.0f) ? Ar[j] / L : 0.0f;

@@ -39,7 +39,7 @@ def test_sizes_and_split_suggestion(lib):
     assert ob.oscar_partials_ml_floats(L, 2, 7) == 2 * 32 * 8
     assert ob.oscar_partials_acc_floats(L, 2, 7) == 2 * 32 * 8 * 128
     s = ob.oscar_suggest_splits(L, 1, 99680, 152)
-    assert 1 <= s <= 256
+    assert 1 <= s <= 1024
     assert ob.oscar_suggest_splits(L, 1, 100, 152) >= 1
     assert ob.oscar_version() == "0.1.0"
 

@@ -110,7 +110,7 @@ def test_decode_tiny_parity(n_splits):
 
 
 def test_partials_per_split_match_oracle():
-    """Each split's (m, l, acc) against the oracle's fp64 partial over the documented page-aligned range."""
+    """Each split's (m, l, acc) against the oracle's fp64 partial over the documented tile-balanced range."""
     S = 5
     case = sc.make_case(n_kv=2, gqa=4, page_size=16, seq=(1024, 613))
     sc.upload(case)
@@ -120,16 +120,16 @@ def test_partials_per_split_match_oracle():
     qb = bf16_bits(case.q)
     for b, T in enumerate(case.seq):
         he = int(case.hist_end[b])
-        first, last = L.sink // L.page_size, -(-he // L.page_size)
-        per = -(-(last - first) // S)
+        first = L.sink // 16
+        n = -(-he // 16) - first
         for h in range(L.n_kv_heads):
             cache = sc.oracle_head_cache(case, b, h)
             for g in range(L.gqa):
                 hq = h * L.gqa + g
                 for s in range(S + 1):
                     if s < S:
-                        lo = max(L.sink, (first + s * per) * L.page_size)
-                        hi = min(he, (first + (s + 1) * per) * L.page_size)
+                        lo = max(L.sink, (first + s * n // S) * 16)
+                        hi = min(he, (first + (s + 1) * n // S) * 16)
                         ranges = [(lo, hi)] if lo < hi else []
                     else:
                         ranges = [(0, L.sink), (he, T)]
@@ -188,6 +188,15 @@ def test_decode_edge_cases(seq, hist, gqa, ps, group, S):
     assert ob.oscar_get_device_status() == 0
 
 
+def test_decode_cuda_core_kernel_three_kv_heads():
+    """3 kv heads (not a divisor of 8): the CUDA-core split kernel serves this shape."""
+    case = sc.make_case(n_kv=3, gqa=2, page_size=16, seq=(900, 500))
+    sc.upload(case)
+    out, out32, lse, _ = sc.run_decode(case, 4)
+    _check_outputs(case, out, out32, lse)
+    assert ob.oscar_get_device_status() == 0
+
+
 def test_decode_qwen3_8b_layer_shape():
     """One layer of the Qwen3-8B shape (32 q / 8 kv heads, 64-token pages) over a ragged batch
     spanning many splits and a ragged last page."""
@@ -195,6 +204,28 @@ def test_decode_qwen3_8b_layer_shape():
     sc.upload(case)
     out, out32, lse, _ = sc.run_decode(case, 24)
     _check_outputs(case, out, out32, lse)
+
+
+def test_halves_on_two_streams_equal_the_combined_call():
+    """History and window halves launched on two streams write exactly what the combined call writes."""
+    case = sc.make_case(n_kv=8, gqa=4, page_size=64, seq=(3000, 1800))
+    sc.upload(case)
+    L, dev = case.layout, case.dev
+    _, _, _, ref = sc.run_decode(case, 6)
+    part = ob.Partials.empty(L, 2, 6)
+    part.m.fill_(float("nan"))
+    part.acc.fill_(float("nan"))
+    side = torch.cuda.Stream()
+    main = torch.cuda.current_stream()
+    side.wait_stream(main)
+    with torch.cuda.stream(side):
+        ob.oscar_decode_attention_window(L, dev["q"], dev["bf16"], dev["bf16_table"], dev["seq_len"],
+                                         dev["hist_end"], case.sm_scale, part, stream=side)
+    ob.oscar_decode_attention_history(L, dev["q_rot"], dev["int2"], dev["int2_table"], dev["seq_len"],
+                                      dev["hist_end"], case.sm_scale, part)
+    main.wait_stream(side)
+    torch.cuda.synchronize()
+    assert torch.equal(part.m, ref.m) and torch.equal(part.l, ref.l) and torch.equal(part.acc, ref.acc)
 
 
 def test_bf16_full_cache_parity():
