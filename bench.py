@@ -50,6 +50,8 @@ def parse_args():
     ap.add_argument("--no-bf16", action="store_true", help="skip the all-BF16 cache comparison")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU seconds of the oracle sample")
     ap.add_argument("--layers", type=int, default=0, help="profiling aid: run only this many layers (0 = all)")
+    ap.add_argument("--no-overlap", action="store_true",
+                    help="launch every kernel after the previous one completes (no programmatic dependent launch)")
     return ap.parse_args()
 
 
@@ -432,8 +434,12 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     from bit_kv_cache_oscar_gb300 import binding as ob
     ob.lib()
-
     model = Model(w, torch.device("cuda", local), args.splits, with_bf16_cache=not args.no_bf16)
+    torch.cuda.synchronize()
+    # The step's kernels read pools, tables and lengths that no kernel of the step writes
+    # (the per-step demotion runs on its own stream and writes positions the step does not
+    # read from INT2), so consecutive kernels may overlap.
+    ob.oscar_set_launch_overlap(not args.no_overlap)
     bts = bytes_per_step(w, model.seq, model.hist_end)
     side = torch.cuda.Stream()
     win = torch.cuda.Stream()

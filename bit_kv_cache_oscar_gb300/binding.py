@@ -49,6 +49,7 @@ EXPORTS = [
     "oscar_quantize_rotated", "oscar_rotate_q", "oscar_decode_attention", "oscar_merge",
     "oscar_bf16_decode_attention", "oscar_get_device_status", "oscar_last_error_string", "oscar_version",
     "oscar_decode_attention_noalloc", "oscar_decode_attention_history", "oscar_decode_attention_window",
+    "oscar_set_launch_overlap", "oscar_get_launch_overlap",
 ]
 
 
@@ -98,6 +99,10 @@ def lib():
     L.oscar_last_error_string.restype = ctypes.c_char_p
     L.oscar_version.argtypes = []
     L.oscar_version.restype = ctypes.c_char_p
+    L.oscar_set_launch_overlap.argtypes = [i32]
+    L.oscar_set_launch_overlap.restype = st
+    L.oscar_get_launch_overlap.argtypes = []
+    L.oscar_get_launch_overlap.restype = i32
     _lib = L
     return L
 
@@ -306,3 +311,13 @@ def oscar_get_device_status(stream=None) -> int:
 
 def oscar_version() -> str:
     return lib().oscar_version().decode()
+
+
+def oscar_set_launch_overlap(enabled: bool) -> None:
+    """Programmatic dependent launch between consecutive decode kernels (see oscar.h for the
+    caller's guarantee: the kernel before a decode call writes no pool, table, length or R)."""
+    _check("oscar_set_launch_overlap", lib().oscar_set_launch_overlap(1 if enabled else 0))
+
+
+def oscar_get_launch_overlap() -> bool:
+    return bool(lib().oscar_get_launch_overlap())

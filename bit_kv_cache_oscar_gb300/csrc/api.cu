@@ -1,6 +1,7 @@
 // C ABI of liboscar.so: argument validation, the device status word, dispatch
 // to the kernels.  Declarations and contracts: include/oscar.h.
 
+#include <atomic>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -111,6 +112,12 @@ oscar::PartialsView part_view(const oscar_partials_t *p) { return {p->m, p->l, p
 }  // namespace
 
 oscar_status_t oscar::set_last_error(oscar_status_t code, const char *msg) { return fail(code, "%s", msg); }
+
+namespace {
+std::atomic<int> g_overlap{0};
+}  // namespace
+
+bool oscar::launch_overlap() { return g_overlap.load(std::memory_order_relaxed) != 0; }
 
 extern "C" {
 
@@ -297,5 +304,12 @@ oscar_status_t oscar_get_device_status(int32_t *status_bits, void *stream) {
 const char *oscar_last_error_string(void) { return g_last_error.c_str(); }
 
 const char *oscar_version(void) { return "0.1.0"; }
+
+oscar_status_t oscar_set_launch_overlap(int32_t enabled) {
+    g_overlap.store(enabled ? 1 : 0, std::memory_order_relaxed);
+    return OSCAR_OK;
+}
+
+int32_t oscar_get_launch_overlap(void) { return g_overlap.load(std::memory_order_relaxed); }
 
 }  // extern "C"

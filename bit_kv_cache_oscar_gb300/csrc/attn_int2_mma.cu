@@ -161,6 +161,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2)) int2_mma_kernel(Mm
     const int s = blockIdx.x, b = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int Hkv = a.n_kv, Hq = Hkv * G, S = a.out.S;
+    pdl_trigger();
     int T, he;
     read_lengths(a.seq_len, a.hist_end, b, a.sink, a.max_pages * a.page_size, a.status, T, he);
     const SplitRange r = history_split(a.sink, he, (int)gridDim.x, s);   // C sub-splits per slot
@@ -240,6 +241,9 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2)) int2_mma_kernel(Mm
     }
 
     // ----------------------------------------------------------- consumers --
+    // The copies above read only the pool, the page table and the lengths; q_rot and the
+    // partials belong to the previous kernels in the stream.
+    pdl_wait();
     const int h = warp % Hkv, sub = warp / Hkv, nsub = kCW / Hkv;
     const int gid = lane >> 2, t = lane & 3;
 
@@ -663,13 +667,14 @@ cudaError_t launch_mma(const oscar_layout_t &L, MmaArgs a, int batch, cudaStream
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = a.csize;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
+    add_overlap_attr(cfg, attr);
     return cudaLaunchKernelEx(&cfg, kern, a);
 }
 

@@ -15,6 +15,7 @@
 // (thread j = channel j).
 
 #include "oscar_internal.cuh"
+#include "ptx.cuh"
 
 namespace oscar {
 namespace {
@@ -197,10 +198,12 @@ __global__ void __launch_bounds__(32 * G) rotate_q_kernel(const uint16_t *q, con
     const int tid = threadIdx.x, g = tid >> 5, j = tid & 31;
     const size_t row0 = ((size_t)b * n_kv + h) * G;        // first query row of this kv head
     const float *R = RK + (size_t)h * kHeadDim * kHeadDim + quarter * 32;
+    pdl_trigger();
     for (int e = tid; e < kHeadDim * 8; e += 32 * G) {       // 128 rows x 8 float4
         const int i = e >> 3, c4 = e & 7;
         reinterpret_cast<float4 *>(&Rs[i][0])[c4] = __ldg(reinterpret_cast<const float4 *>(R + i * kHeadDim) + c4);
     }
+    pdl_wait();                                             // q and q_rot belong to the previous kernel
     for (int e = tid; e < G * kHeadDim; e += 32 * G) qs[e / kHeadDim][e % kHeadDim] = bf16_to_f32(q[row0 * kHeadDim + e]);
     __syncthreads();
     float acc = 0.0f;
@@ -266,15 +269,20 @@ cudaError_t launch_quantize_rotated(const oscar_layout_t &L, const float *x, int
 cudaError_t launch_rotate_q(const oscar_layout_t &L, const uint16_t *q, const float *RK, int batch,
                             float *q_rot, cudaStream_t st) {
     if (batch <= 0) return cudaSuccess;
-    const dim3 grid(batch * L.n_kv_heads * 4);
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attrs[1];
+    cfg.gridDim = dim3(batch * L.n_kv_heads * 4);
+    cfg.blockDim = dim3(32 * L.gqa);
+    cfg.stream = st;
+    cfg.attrs = attrs;
+    add_overlap_attr(cfg, attrs);
     switch (L.gqa) {
-        case 1: rotate_q_kernel<1><<<grid, 32, 0, st>>>(q, RK, L.n_kv_heads, q_rot); break;
-        case 2: rotate_q_kernel<2><<<grid, 64, 0, st>>>(q, RK, L.n_kv_heads, q_rot); break;
-        case 4: rotate_q_kernel<4><<<grid, 128, 0, st>>>(q, RK, L.n_kv_heads, q_rot); break;
-        case 8: rotate_q_kernel<8><<<grid, 256, 0, st>>>(q, RK, L.n_kv_heads, q_rot); break;
+        case 1: return cudaLaunchKernelEx(&cfg, rotate_q_kernel<1>, q, RK, L.n_kv_heads, q_rot);
+        case 2: return cudaLaunchKernelEx(&cfg, rotate_q_kernel<2>, q, RK, L.n_kv_heads, q_rot);
+        case 4: return cudaLaunchKernelEx(&cfg, rotate_q_kernel<4>, q, RK, L.n_kv_heads, q_rot);
+        case 8: return cudaLaunchKernelEx(&cfg, rotate_q_kernel<8>, q, RK, L.n_kv_heads, q_rot);
         default: return cudaErrorInvalidValue;
     }
-    return cudaGetLastError();
 }
 
 }  // namespace oscar

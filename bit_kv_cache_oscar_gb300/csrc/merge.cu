@@ -17,6 +17,7 @@
 // independent, so they are computed in parallel and the sums are plain FMA chains.
 
 #include "oscar_internal.cuh"
+#include "ptx.cuh"
 
 namespace oscar {
 namespace {
@@ -43,20 +44,37 @@ __device__ __forceinline__ float exp2_taylor(float x) {
 }
 
 constexpr int kPad = kHeadDim + 1;   // R_V rows padded: thread j reads row j conflict-free
+constexpr int kQuarter = kHeadDim / 4;
 
-// grid = (Hq, batch); 128 threads, thread j owns output channel j of one query head.
-// Dynamic smem: [R_V 128 x 129 if RV] [A 128] [w S+1] [l S+1] [red 8].
+// grid = (Hq, batch, 4 with R_V / 1 without); 128 threads.  Every CTA merges the history
+// slots of one query head for all 128 channels (thread j owns channel j); with R_V, CTA z
+// then rotates back output channels [32 z, 32 z + 32) (thread j < 32 owns channel 32 z + j)
+// from the 32 rows of R_V that it staged before waiting for the partials' producer.
+// Dynamic smem: [R_V 32 x 129 if RV] [A 128] [w S+1] [l S+1] [red 8].
 __global__ void __launch_bounds__(128) merge_kernel(PartialsView p, const float *RV, int n_q_heads, int gqa,
                                                     uint16_t *out, float *out_f32, float *lse) {
     extern __shared__ __align__(16) float smem[];
-    const int hq = blockIdx.x, b = blockIdx.y, j = threadIdx.x;
+    const int hq = blockIdx.x, b = blockIdx.y, z = blockIdx.z, j = threadIdx.x;
     const int S = p.S;
     float *Rs = smem;
-    float *As = smem + (RV ? kHeadDim * kPad : 0);
+    float *As = smem + (RV ? kQuarter * kPad : 0);
     float *ws = As + kHeadDim;
     float *ls = ws + (S + 1);
     float *red = ls + (S + 1);
     const size_t row0 = ((size_t)b * n_q_heads + hq) * (S + 1);
+
+    pdl_trigger();
+    if (RV) {
+        // rows 32 z .. 32 z + 31 of this head's R_V (32 rows x 32 float4)
+        const float4 *R = reinterpret_cast<const float4 *>(RV + ((size_t)(hq / gqa) * kHeadDim + z * kQuarter) * kHeadDim);
+#pragma unroll
+        for (int e = j; e < kQuarter * kHeadDim / 4; e += 128) {
+            const float4 v = __ldg(R + e);
+            float *dst = Rs + (e >> 5) * kPad + (e & 31) * 4;
+            dst[0] = v.x; dst[1] = v.y; dst[2] = v.z; dst[3] = v.w;
+        }
+    }
+    pdl_wait();                                  // the partials come from the previous kernels
 
     float mloc = -INFINITY;
     for (int i = j; i <= S; i += 128) {
@@ -68,15 +86,6 @@ __global__ void __launch_bounds__(128) merge_kernel(PartialsView p, const float 
 #pragma unroll
     for (int o = 16; o; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
     if ((j & 31) == 0) red[j >> 5] = mloc;
-    if (RV) {
-        const float4 *R = reinterpret_cast<const float4 *>(RV + (size_t)(hq / gqa) * kHeadDim * kHeadDim);
-#pragma unroll 8
-        for (int e = j; e < kHeadDim * kHeadDim / 4; e += 128) {
-            const float4 v = __ldg(R + e);
-            float *dst = Rs + (e >> 5) * kPad + (e & 31) * 4;
-            dst[0] = v.x; dst[1] = v.y; dst[2] = v.z; dst[3] = v.w;
-        }
-    }
     __syncthreads();
     const float M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
     for (int i = j; i <= S; i += 128) ws[i] = ls[i] > 0.0f ? exp2_taylor(__fsub_rn(ws[i], M)) : 0.0f;
@@ -93,9 +102,12 @@ __global__ void __launch_bounds__(128) merge_kernel(PartialsView p, const float 
         A = on ? __fmaf_rn(x, w, A) : A;
     }
     float Ar = A;
+    int c = j;                               // output channel of this thread
     if (RV) {
         As[j] = A;
         __syncthreads();
+        if (j >= kQuarter) return;
+        c = z * kQuarter + j;
         float r = 0.0f;
 #pragma unroll 8
         for (int i = 0; i < kHeadDim; ++i) r = __fmaf_rn(As[i], Rs[j * kPad + i], r);
@@ -104,13 +116,13 @@ __global__ void __launch_bounds__(128) merge_kernel(PartialsView p, const float 
     if (ls[S] > 0.0f) {
         const float w = ws[S];
         L = __fmaf_rn(ls[S], w, L);
-        Ar = __fmaf_rn(acc[(size_t)S * kHeadDim], w, Ar);
+        Ar = __fmaf_rn(p.acc[(row0 + S) * kHeadDim + c], w, Ar);
     }
     const float o = L > 0.0f ? __fdiv_rn(Ar, L) : 0.0f;
     const size_t orow = (size_t)b * n_q_heads + hq;
-    if (out) out[orow * kHeadDim + j] = f32_to_bf16_rn(o);
-    if (out_f32) out_f32[orow * kHeadDim + j] = o;
-    if (lse && j == 0) lse[orow] = L > 0.0f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
+    if (out) out[orow * kHeadDim + c] = f32_to_bf16_rn(o);
+    if (out_f32) out_f32[orow * kHeadDim + c] = o;
+    if (lse && z == 0 && j == 0) lse[orow] = L > 0.0f ? (M + log2f(L)) * 0.6931471805599453f : -INFINITY;
 }
 
 }  // namespace
@@ -119,7 +131,7 @@ cudaError_t launch_merge(const oscar_layout_t &L, PartialsView p, const float *R
                          float *out_f32, float *lse, cudaStream_t st) {
     if (batch <= 0) return cudaSuccess;
     const int hq = L.n_kv_heads * L.gqa;
-    const size_t smem = sizeof(float) * ((RV ? kHeadDim * kPad : 0) + kHeadDim + 2 * (p.S + 1) + 8);
+    const size_t smem = sizeof(float) * ((RV ? kQuarter * kPad : 0) + kHeadDim + 2 * (p.S + 1) + 8);
     static thread_local int configured[64] = {0};
     int dev = 0;
     cudaGetDevice(&dev);
@@ -128,8 +140,15 @@ cudaError_t launch_merge(const oscar_layout_t &L, PartialsView p, const float *R
         if (e != cudaSuccess) return e;
         configured[dev] = (int)smem;
     }
-    merge_kernel<<<dim3(hq, batch), 128, smem, st>>>(p, RV, hq, L.gqa, out, out_f32, lse);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attrs[1];
+    cfg.gridDim = dim3(hq, batch, RV ? 4 : 1);
+    cfg.blockDim = dim3(128);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cfg.attrs = attrs;
+    add_overlap_attr(cfg, attrs);
+    return cudaLaunchKernelEx(&cfg, merge_kernel, p, RV, hq, L.gqa, out, out_f32, lse);
 }
 
 }  // namespace oscar

@@ -75,6 +75,18 @@ __device__ __forceinline__ void read_lengths(const int32_t *seq_len, const int32
 // Record the one-line reason returned by oscar_last_error_string() and return `code`.
 oscar_status_t set_last_error(oscar_status_t code, const char *msg);
 
+// Process-wide launch-overlap switch (programmatic dependent launch); see oscar.h.
+bool launch_overlap();
+
+// Launch configuration with the programmatic-serialization attribute when overlap is on.
+// `attrs` must have room for the attribute and outlive the launch call.
+inline void add_overlap_attr(cudaLaunchConfig_t &cfg, cudaLaunchAttribute *attrs) {
+    if (!launch_overlap()) return;
+    cudaLaunchAttribute &at = attrs[cfg.numAttrs++];
+    at.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at.val.programmaticStreamSerializationAllowed = 1;
+}
+
 // ---------------------------------------------------------------- launches --
 
 struct Int2PoolView {

@@ -302,6 +302,29 @@ OSCAR_API oscar_status_t oscar_decode_attention_noalloc(
     int32_t max_pages_per_req, const int32_t *seq_len, const int32_t *hist_end, int32_t batch, float sm_scale,
     int32_t n_splits, const float *R_V, uint16_t *out, float *out_f32, float *lse, void *stream);
 
+/*
+ * Launch overlap between consecutive decode kernels (programmatic dependent
+ * launch), process-wide, off by default; applies to calls made after it returns.
+ * No method page describes it: it is a launch policy of this library.
+ *
+ * When on, oscar_rotate_q, oscar_decode_attention_history (tensor-core path),
+ * oscar_decode_attention and oscar_merge launch their kernels so that each may
+ * start while the kernel before it in the same stream is still running.  Before
+ * it waits for that kernel, a kernel only reads what a decode step treats as
+ * fixed: R_K / R_V, the INT2 and BF16 pools, the page tables, seq_len and
+ * hist_end.  Everything else (q, q_rot, the partials, the outputs) is read or
+ * written after the wait.  The caller therefore guarantees that the kernel
+ * preceding one of these calls in the stream does not write R_K, R_V, a pool,
+ * a page table, seq_len or hist_end; oscar_demote, for example, must be followed
+ * by an event or another kernel before the decode kernels that read its pages,
+ * or overlap must be off.  With overlap off every launch waits for the previous
+ * kernel to complete, as CUDA streams do by default.
+ *
+ * Returns OSCAR_OK; oscar_get_launch_overlap() reads the current setting (0/1).
+ */
+OSCAR_API oscar_status_t oscar_set_launch_overlap(int32_t enabled);
+OSCAR_API int32_t oscar_get_launch_overlap(void);
+
 /* Read and clear the device status word of the current device (synchronizes `stream`). */
 OSCAR_API oscar_status_t oscar_get_device_status(int32_t *status_bits, void *stream);
 

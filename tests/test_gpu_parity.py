@@ -228,6 +228,53 @@ def test_halves_on_two_streams_equal_the_combined_call():
     assert torch.equal(part.m, ref.m) and torch.equal(part.l, ref.l) and torch.equal(part.acc, ref.acc)
 
 
+def _layers_back_to_back(case, qs, n_splits, sync=True):
+    """rotate_q -> decode_attention -> merge for several queries in one stream, sharing q_rot and
+    the partials buffer between them (so a launch that overlapped too far would change bits)."""
+    L, dev = case.layout, case.dev
+    B = len(case.seq)
+    q_rot = torch.empty((B, L.n_q_heads, D), dtype=torch.float32, device="cuda")
+    part = ob.Partials.empty(L, B, n_splits)
+    outs = []
+    for q in qs:
+        o32 = torch.empty((B, L.n_q_heads, D), dtype=torch.float32, device="cuda")
+        ob.oscar_rotate_q(L, q, dev["RK"], q_rot)
+        ob.oscar_decode_attention(L, q, q_rot, dev["bf16"], dev["bf16_table"], dev["int2"], dev["int2_table"],
+                                  dev["seq_len"], dev["hist_end"], case.sm_scale, part)
+        ob.oscar_merge(L, part, dev["RV"], None, o32, None)
+        outs.append(o32)
+    if sync:
+        torch.cuda.synchronize()
+    return outs
+
+
+def test_launch_overlap_gives_identical_bits():
+    """Programmatic dependent launch between the decode kernels changes no output bit, eagerly
+    and inside a CUDA graph."""
+    case = sc.make_case(n_kv=8, gqa=4, page_size=64, seq=(5000, 2100))
+    sc.upload(case)
+    gen = torch.Generator(device="cpu").manual_seed(7)
+    qs = [torch.randn(case.dev["q"].shape, generator=gen).to(torch.bfloat16).cuda() for _ in range(5)]
+    assert not ob.oscar_get_launch_overlap()
+    ref = _layers_back_to_back(case, qs, 20)
+    try:
+        ob.oscar_set_launch_overlap(True)
+        assert ob.oscar_get_launch_overlap()
+        got = _layers_back_to_back(case, qs, 20)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            holder = [None]
+            holder[0] = _layers_back_to_back(case, qs, 20, sync=False)
+        g.replay()
+        torch.cuda.synchronize()
+        got_graph = holder[0]
+    finally:
+        ob.oscar_set_launch_overlap(False)
+    for r, a, b in zip(ref, got, got_graph):
+        assert torch.equal(r, a) and torch.equal(r, b)
+    assert ob.oscar_get_device_status() == 0
+
+
 def test_bf16_full_cache_parity():
     """The all-BF16 comparison kernel: oracle with no history region (sink = h_end = 0)."""
     case = sc.make_case(n_kv=2, gqa=4, page_size=16, seq=(1024, 555))
