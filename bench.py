@@ -250,8 +250,8 @@ class Model:
 
     # One decode step over all layers (the path).  Per layer the BF16 sink/recent half runs on
     # a second stream next to q rotation + the INT2 history half; the merge joins them.
-    # Optional events bracket each INT2 history launch.
-    def step(self, events=None, side=None, win=None):
+    # Optional events bracket each decode-attention launch.
+    def step(self, events=None, side=None):
         import torch
         from bit_kv_cache_oscar_gb300 import binding as ob
         L, w = self.L, self.w
@@ -263,23 +263,14 @@ class Model:
                     ob.oscar_demote(L, st["bf16"], self.bf16_table, st["int2"], self.int2_table, self.dem_req,
                                     self.dem_pos, st["RK"], st["RV"], 0.96, 0.92, stream=side)
         for l, st in enumerate(self.layers):
-            if win is not None:
-                win.wait_stream(cur)
-                with torch.cuda.stream(win):
-                    ob.oscar_decode_attention_window(L, self.q_all[l], st["bf16"], self.bf16_table, self.seq_len,
-                                                     self.hist_dev, self.sm_scale, self.part, stream=win)
-            else:
-                ob.oscar_decode_attention_window(L, self.q_all[l], st["bf16"], self.bf16_table, self.seq_len,
-                                                 self.hist_dev, self.sm_scale, self.part)
             ob.oscar_rotate_q(L, self.q_all[l], st["RK"], self.q_rot)
             if events is not None:
                 events[l][0].record()
-            ob.oscar_decode_attention_history(L, self.q_rot, st["int2"], self.int2_table, self.seq_len,
-                                              self.hist_dev, self.sm_scale, self.part)
+            # history splits and the BF16 window in one launch
+            ob.oscar_decode_attention(L, self.q_all[l], self.q_rot, st["bf16"], self.bf16_table, st["int2"],
+                                      self.int2_table, self.seq_len, self.hist_dev, self.sm_scale, self.part)
             if events is not None:
                 events[l][1].record()
-            if win is not None:
-                cur.wait_stream(win)
             ob.oscar_merge(L, self.part, st["RV"], self.out_all[l])
         if self.demote and side is not None:
             cur.wait_stream(side)
@@ -292,8 +283,8 @@ class Model:
             ob.oscar_merge(self.L, self.part_full, None, self.out_full[l])
 
     def launches_per_step(self) -> int:
-        # rotate_q, INT2 history, BF16 window, merge per layer (+ the demotion)
-        return self.w.layers * (4 + (1 if self.demote else 0))
+        # rotate_q, decode attention (INT2 history + BF16 window), merge per layer (+ the demotion)
+        return self.w.layers * (3 + (1 if self.demote else 0))
 
 
 def capture(fn, steps: int = 1):
@@ -442,10 +433,9 @@ def main():
     ob.oscar_set_launch_overlap(not args.no_overlap)
     bts = bytes_per_step(w, model.seq, model.hist_end)
     side = torch.cuda.Stream()
-    win = torch.cuda.Stream()
 
     # headline: one-step graph replayed K times
-    g = capture(lambda: model.step(side=side, win=win))
+    g = capture(lambda: model.step(side=side))
     with ClockSampler(local) as clk:
         t = time_graph(g, args.steps, args.warmup, dist)
     ms_step = 1e3 * t / args.steps
@@ -454,11 +444,11 @@ def main():
     # roofline: per-launch durations of the decode-attention call, events captured in a K-step graph
     evs = [[(torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
             for _ in range(w.layers)] for _ in range(args.steps)]
-    gp = capture(lambda: model.step(events=evs[0], side=side, win=win))
+    gp = capture(lambda: model.step(events=evs[0], side=side))
     gk = torch.cuda.CUDAGraph()
     with torch.cuda.graph(gk):
         for k in range(args.steps):
-            model.step(events=evs[k], side=side, win=win)
+            model.step(events=evs[k], side=side)
     for _ in range(args.warmup):
         gp.replay()
     torch.cuda.synchronize()
@@ -467,9 +457,10 @@ def main():
     durs = [evs[k][l][0].elapsed_time(evs[k][l][1]) / 1e3 for k in range(args.steps) for l in range(w.layers)]
     dur = statistics.mean(durs)
     peaks = measured_peaks()
-    unit_bytes = bts["int2_per_layer"] + w.batch * w.n_q_heads * w.head_dim * 4   # history + q_rot
+    # one decode-attention launch: INT2 history + BF16 window + q (bf16) + q_rot (fp32)
+    unit_bytes = bts["int2_per_layer"] + bts["bf16_per_layer"] + w.batch * w.n_q_heads * w.head_dim * (2 + 4)
     achieved = unit_bytes / dur / 1e9
-    traffic = stored_traffic("int2_history", w.name)
+    traffic = stored_traffic("decode_attention", w.name)
 
     # e2e: q from pinned host memory -> step -> out to pinned host memory, every step
     q_host = [torch.empty_like(model.q_all, device="cpu").pin_memory() for _ in range(2)]
@@ -524,7 +515,7 @@ def main():
             "bytes_per_step": bts["per_step"],
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                         "kernel": "oscar_decode_attention_history (INT2 history split-K, one layer)",
+                         "kernel": "oscar_decode_attention (INT2 history split-K + BF16 window, one layer, one launch)",
                          "bytes_per_launch": unit_bytes, "launch_us": dur * 1e6,
                          "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs copy bandwidth)"},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": model.launches_per_step() * args.steps,

@@ -137,9 +137,10 @@ int32_t oscar_suggest_splits(const oscar_layout_t *L, int32_t batch, int32_t max
     int active = 0;
     if (oscar::int2_mma_supported(*L)) {
         // one split = a cluster of C CTAs (all kv heads each): as many splits as clusters fit at once
+        // (one more cluster per request takes the BF16 window)
         const int c = oscar::int2_mma_cluster_size(*L, &active);
         if (active <= 0) active = (2 * sm_count) / c;
-        want = active / batch;
+        want = active / batch - 1;
     } else {
         // one CTA per (split, kv head): about two resident CTAs per SM
         want = (2L * sm_count + (long)batch * L->n_kv_heads - 1) / ((long)batch * L->n_kv_heads);
@@ -214,6 +215,12 @@ oscar_status_t oscar_decode_attention(const oscar_layout_t *layout, const uint16
     if (batch > 65535) return fail(OSCAR_ERR_INVALID_ARG, "batch %d > 65535", batch);
     int32_t *st = status_ptr();
     cudaStream_t s = (cudaStream_t)stream;
+    if (oscar::int2_mma_supported(*layout))   // history splits and window in one launch
+        return cuda_status(oscar::launch_decode_mma(*layout, q_rot, int2_view(int2_pool), int2_page_table, q,
+                                                    bf16_view(bf16_pool), bf16_page_table, max_pages_per_req,
+                                                    seq_len, hist_end, batch, sm_scale, part_view(partials), st,
+                                                    true, true, s),
+                           "decode attention launch");
     cudaError_t e = oscar::launch_int2_attention(*layout, q_rot, int2_view(int2_pool), int2_page_table,
                                                  max_pages_per_req, seq_len, hist_end, batch, sm_scale,
                                                  part_view(partials), st, s);

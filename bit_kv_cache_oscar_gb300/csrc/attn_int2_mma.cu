@@ -110,16 +110,20 @@ struct MmaArgs {
     int stages, stage_bytes, off_v, off_s, arr_bytes, ws_bytes, stage_off;
     int csize;        // CTAs per cluster; each cluster writes one partial slot
     int res_off;      // byte offset (from the first stage) of the per-CTA result area
+    int hist_ctas;    // CTAs [0, hist_ctas) of grid.x take the history; the rest the BF16 window
+    int win_off;      // byte offset (from the first stage) of the window CTAs' warp results
+    const uint16_t *q;          // raw bf16 queries (window CTAs)
+    Bf16PoolView bpool;         // BF16 sink/recent pool and its page table (window CTAs)
+    const int32_t *bpt;
 };
 
 // Cluster reduction: every CTA of a cluster holds (m, l, acc) for each query head of its
 // sub-split in shared memory; CTA `rank` combines query heads rank, rank + C, ... over the
-// C CTAs in rank order and writes partial slot blockIdx.x / C.  Every thread calls this once.
-__device__ __forceinline__ void cluster_combine(const MmaArgs &a, const float *res, int Hq, int b) {
+// C CTAs in rank order and writes partial slot `slot`.  Every thread calls this once.
+__device__ __forceinline__ void cluster_combine(const MmaArgs &a, const float *res, int Hq, int b, int slot) {
     const int C = a.csize;
     cluster_sync_all();
     const int rank = (int)cluster_ctarank();
-    const int slot = blockIdx.x / C;
     const size_t S1 = (size_t)a.out.S + 1;
     const int mine = (Hq - rank + C - 1) / C;
     const uint32_t rm = saddr(res), rl = rm + Hq * 4, ra = rm + 2 * Hq * 4;
@@ -146,6 +150,132 @@ __device__ __forceinline__ void cluster_combine(const MmaArgs &a, const float *r
     cluster_sync_all();                 // no CTA leaves while its shared memory is being read
 }
 
+// ---- BF16 sink/recent window, on CUDA cores, in the CTAs after the history ones.
+// Window positions of request b, in order: [0, n0) then [lo1, T), n0 = min(sink, T),
+// lo1 = max(h_end, n0).  Window CTA wr of wc takes positions [wr*n/wc, (wr+1)*n/wc); warp w
+// takes kv head w % Hkv and every (8/Hkv)-th position of that range; lane l owns channels
+// 4l..4l+3.  Each token is folded into a per-warp online softmax (base 2), the warps of a kv
+// head are combined in a fixed order, and the CTA's result goes to `res` (cluster) or
+// straight to partial slot S.  Every thread of the CTA calls this.
+template <int G>
+__device__ void window_cta(const MmaArgs &a, float *wsm, float *res, int T, int he, int b, int wr, int wc) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int Hkv = a.n_kv, Hq = Hkv * G, nsub = kCW / Hkv, S = a.out.S;
+    const int n0 = min(a.sink, T), lo1 = max(he, n0);
+    const int n = n0 + (T - lo1);
+    const int i_lo = (int)((long long)wr * n / wc), i_hi = (int)((long long)(wr + 1) * n / wc);
+    float m[G], l[G], acc[G][4];
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+        m[hh] = -INFINITY;
+        l[hh] = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[hh][c] = 0.f;
+    }
+    if (warp < kCW) {
+        const int h = warp % Hkv, sub = warp / Hkv;
+        float q[G][4];
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) {
+            const uint2 v = reinterpret_cast<const uint2 *>(a.q + ((size_t)b * Hq + h * G + hh) * kHeadDim)[lane];
+            q[hh][0] = __uint_as_float(v.x << 16); q[hh][1] = __uint_as_float(v.x & 0xffff0000u);
+            q[hh][2] = __uint_as_float(v.y << 16); q[hh][3] = __uint_as_float(v.y & 0xffff0000u);
+        }
+        constexpr int U = 4;                     // tokens whose rows are loaded together
+        for (int i0 = i_lo + sub; i0 < i_hi; i0 += U * nsub) {
+            uint2 kk[U], vv[U];
+            bool ok[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int i = i0 + u * nsub;
+                ok[u] = false;
+                kk[u] = vv[u] = make_uint2(0u, 0u);
+                if (i < i_hi) {
+                    const int p = i < n0 ? i : lo1 + (i - n0);
+                    const int page = a.bpt[(size_t)b * a.max_pages + p / a.page_size];
+                    if (page >= 0 && page < a.bpool.n_pages) {
+                        const size_t row = ((size_t)page * a.page_size + p % a.page_size) * Hkv + h;
+                        kk[u] = __ldg(reinterpret_cast<const uint2 *>(a.bpool.k + row * kHeadDim) + lane);
+                        vv[u] = __ldg(reinterpret_cast<const uint2 *>(a.bpool.v + row * kHeadDim) + lane);
+                        ok[u] = true;
+                    } else if (lane == 0) {
+                        flag_status(a.status, OSCAR_DEV_BAD_BF16_PAGE);
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (!ok[u]) continue;
+                const float k4[4] = {__uint_as_float(kk[u].x << 16), __uint_as_float(kk[u].x & 0xffff0000u),
+                                     __uint_as_float(kk[u].y << 16), __uint_as_float(kk[u].y & 0xffff0000u)};
+                const float v4[4] = {__uint_as_float(vv[u].x << 16), __uint_as_float(vv[u].x & 0xffff0000u),
+                                     __uint_as_float(vv[u].y << 16), __uint_as_float(vv[u].y & 0xffff0000u)};
+                float d[G];
+#pragma unroll
+                for (int hh = 0; hh < G; ++hh)
+                    d[hh] = fmaf(q[hh][3], k4[3], fmaf(q[hh][2], k4[2], fmaf(q[hh][1], k4[1], q[hh][0] * k4[0])));
+#pragma unroll
+                for (int o = 16; o; o >>= 1)
+#pragma unroll
+                    for (int hh = 0; hh < G; ++hh) d[hh] += __shfl_xor_sync(0xffffffffu, d[hh], o);
+#pragma unroll
+                for (int hh = 0; hh < G; ++hh) {
+                    const float t = d[hh] * a.scale2;
+                    const float mn = fmaxf(m[hh], t);
+                    const float al = exp2f(m[hh] - mn), pr = exp2f(t - mn);
+                    l[hh] = fmaf(l[hh], al, pr);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) acc[hh][c] = fmaf(acc[hh][c], al, pr * v4[c]);
+                    m[hh] = mn;
+                }
+            }
+        }
+        // warp results: wsm = [warp][G] m, [warp][G] l, [warp][G][128] acc
+        float *wm = wsm, *wl = wsm + kCW * G, *wa = wsm + 2 * kCW * G;
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh) {
+            if (lane == 0) {
+                wm[warp * G + hh] = m[hh];
+                wl[warp * G + hh] = l[hh];
+            }
+            *reinterpret_cast<float4 *>(wa + (warp * G + hh) * kHeadDim + 4 * lane) =
+                make_float4(acc[hh][0], acc[hh][1], acc[hh][2], acc[hh][3]);
+        }
+    }
+    pdl_trigger();
+    __syncthreads();
+    const bool to_res = a.csize > 1;
+    const float *wm = wsm, *wl = wsm + kCW * G, *wa = wsm + 2 * kCW * G;
+    for (int e = threadIdx.x; e < Hq * kHeadDim; e += blockDim.x) {
+        const int hq = e / kHeadDim, d = e % kHeadDim, h = hq / G, hh = hq % G;
+        float M = -INFINITY;
+        for (int w = h; w < kCW; w += Hkv) M = fmaxf(M, wm[w * G + hh]);
+        float L = 0.f, A = 0.f;
+        if (M != -INFINITY) {
+            for (int w = h; w < kCW; w += Hkv) {
+                const float f = exp2f(wm[w * G + hh] - M);
+                L = fmaf(wl[w * G + hh], f, L);
+                A = fmaf(wa[(w * G + hh) * kHeadDim + d], f, A);
+            }
+        }
+        if (to_res) {
+            res[2 * Hq + hq * kHeadDim + d] = A;
+            if (d == 0) {
+                res[hq] = M;
+                res[Hq + hq] = L;
+            }
+        } else {
+            const size_t row = ((size_t)b * Hq + hq) * (S + 1) + S;
+            a.out.acc[row * kHeadDim + d] = A;
+            if (d == 0) {
+                a.out.m[row] = M;
+                a.out.l[row] = L;
+            }
+        }
+    }
+    if (to_res) cluster_combine(a, res, Hq, b, S);
+}
+
 // token position within a 16-token tile -> PV k-column (the K permutation shared by A and B)
 __device__ __forceinline__ int kpos(int tok) { return (tok & 8) + 2 * (tok & 3) + ((tok >> 2) & 1); }
 
@@ -161,10 +291,15 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2)) int2_mma_kernel(Mm
     const int s = blockIdx.x, b = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int Hkv = a.n_kv, Hq = Hkv * G, S = a.out.S;
-    pdl_trigger();
     int T, he;
     read_lengths(a.seq_len, a.hist_end, b, a.sink, a.max_pages * a.page_size, a.status, T, he);
-    const SplitRange r = history_split(a.sink, he, (int)gridDim.x, s);   // C sub-splits per slot
+    if (s >= a.hist_ctas) {                    // a BF16 window CTA (uniform over the cluster)
+        pdl_wait();                            // q and the partials belong to the previous kernels
+        window_cta<G>(a, reinterpret_cast<float *>(stage0 + a.win_off), reinterpret_cast<float *>(stage0 + a.res_off),
+                      T, he, b, s - a.hist_ctas, (int)gridDim.x - a.hist_ctas);
+        return;
+    }
+    const SplitRange r = history_split(a.sink, he, a.hist_ctas, s);   // C sub-splits per slot
     const int n_iters = (r.tile_hi - r.tile_lo + kTilesPerStage - 1) / kTilesPerStage;
 
     if (threadIdx.x == 0) {
@@ -236,7 +371,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2)) int2_mma_kernel(Mm
             if (lane == 0) mbar_arrive(saddr(&bars[st]));
         }
         asm volatile("cp.async.wait_all;" ::: "memory");
-        if (a.csize > 1) cluster_combine(a, reinterpret_cast<const float *>(stage0 + a.res_off), Hq, b);
+        if (a.csize > 1) cluster_combine(a, reinterpret_cast<const float *>(stage0 + a.res_off), Hq, b, blockIdx.x / a.csize);
         return;
     }
 
@@ -483,6 +618,9 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2)) int2_mma_kernel(Mm
         if (lane == 0) mbar_arrive(saddr(&bars[4 + st]));
     }
 
+    // The next kernel in the stream may launch once every CTA's consumers are past their loop
+    // (only they trigger: the copy warp finishes its loop stages ahead of them).
+    pdl_trigger();
     // ---- finish: reduce the per-thread sums over the 8 lanes of a column, scale the outputs
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -532,7 +670,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2)) int2_mma_kernel(Mm
                 }
             }
         }
-        if (to_res) cluster_combine(a, res, Hq, b);
+        if (to_res) cluster_combine(a, res, Hq, b, blockIdx.x / a.csize);
         return;
     }
 
@@ -581,7 +719,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2)) int2_mma_kernel(Mm
             }
         }
     }
-    if (to_res) cluster_combine(a, res, Hq, b);
+    if (to_res) cluster_combine(a, res, Hq, b, blockIdx.x / a.csize);
 }
 
 // Largest cluster size C in {8, 4, 2} whose co-resident clusters still occupy at least 90% of
@@ -646,7 +784,8 @@ int mma_smem_plan(const oscar_layout_t &L, MmaArgs &a) {
     a.stages = stages;
     const int combine = (kCW / Hkv > 1) ? kCW * NT * 4 * (2 + kHeadDim) * 4 : 0;
     a.res_off = combine;
-    const int tail = combine + Hq * (2 + kHeadDim) * 4;
+    a.win_off = a.res_off + Hq * (2 + kHeadDim) * 4;
+    const int tail = a.win_off + kCW * G * (2 + kHeadDim) * 4;
     return a.stage_off + (stages * a.stage_bytes > tail ? stages * a.stage_bytes : tail);
 }
 
@@ -658,12 +797,13 @@ int mma_cluster_size(const oscar_layout_t &L, int *active) {
 }
 
 template <int G, int NGRP>
-cudaError_t launch_mma(const oscar_layout_t &L, MmaArgs a, int batch, cudaStream_t st) {
+cudaError_t launch_mma(const oscar_layout_t &L, MmaArgs a, int batch, bool history, bool window, cudaStream_t st) {
     const int smem = mma_smem_plan<G, NGRP>(L, a);
     auto kern = int2_mma_kernel<G, NGRP>;
     a.csize = int2_cluster_size(reinterpret_cast<const void *>(kern), smem, kThreads);
+    a.hist_ctas = history ? a.out.S * a.csize : 0;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.out.S * a.csize, batch);
+    cfg.gridDim = dim3(a.hist_ctas + (window ? a.csize : 0), batch);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
@@ -702,12 +842,15 @@ bool int2_mma_supported(const oscar_layout_t &L) {
     return (H == 1 || H == 2 || H == 4 || H == 8) && L.head_dim == kHeadDim;
 }
 
-cudaError_t launch_int2_attention_mma(const oscar_layout_t &L, const float *q_rot, Int2PoolView pool,
-                                      const int32_t *pt, int max_pages, const int32_t *seq_len,
-                                      const int32_t *hist_end, int batch, float sm_scale, PartialsView out,
-                                      int32_t *status, cudaStream_t st) {
-    if (batch <= 0) return cudaSuccess;
+cudaError_t launch_decode_mma(const oscar_layout_t &L, const float *q_rot, Int2PoolView pool, const int32_t *pt,
+                              const uint16_t *q, Bf16PoolView bpool, const int32_t *bpt, int max_pages,
+                              const int32_t *seq_len, const int32_t *hist_end, int batch, float sm_scale,
+                              PartialsView out, int32_t *status, bool history, bool window, cudaStream_t st) {
+    if (batch <= 0 || (!history && !window)) return cudaSuccess;
     MmaArgs a{};
+    a.q = q;
+    a.bpool = bpool;
+    a.bpt = bpt;
     a.q_rot = q_rot;
     a.pool = pool;
     a.pt = pt;
@@ -722,7 +865,7 @@ cudaError_t launch_int2_attention_mma(const oscar_layout_t &L, const float *q_ro
     a.status = status;
     const int ngrp = kHeadDim / L.group;
 #define OSCAR_MMA_CASE(GG, NN) \
-    if (L.gqa == GG && ngrp == NN) return launch_mma<GG, NN>(L, a, batch, st);
+    if (L.gqa == GG && ngrp == NN) return launch_mma<GG, NN>(L, a, batch, history, window, st);
     OSCAR_MMA_CASE(1, 1) OSCAR_MMA_CASE(2, 1) OSCAR_MMA_CASE(4, 1) OSCAR_MMA_CASE(8, 1)
     OSCAR_MMA_CASE(1, 2) OSCAR_MMA_CASE(2, 2) OSCAR_MMA_CASE(4, 2) OSCAR_MMA_CASE(8, 2)
     OSCAR_MMA_CASE(1, 4) OSCAR_MMA_CASE(2, 4) OSCAR_MMA_CASE(4, 4) OSCAR_MMA_CASE(8, 4)

@@ -198,7 +198,6 @@ __global__ void __launch_bounds__(32 * G) rotate_q_kernel(const uint16_t *q, con
     const int tid = threadIdx.x, g = tid >> 5, j = tid & 31;
     const size_t row0 = ((size_t)b * n_kv + h) * G;        // first query row of this kv head
     const float *R = RK + (size_t)h * kHeadDim * kHeadDim + quarter * 32;
-    pdl_trigger();
     for (int e = tid; e < kHeadDim * 8; e += 32 * G) {       // 128 rows x 8 float4
         const int i = e >> 3, c4 = e & 7;
         reinterpret_cast<float4 *>(&Rs[i][0])[c4] = __ldg(reinterpret_cast<const float4 *>(R + i * kHeadDim) + c4);
@@ -209,6 +208,10 @@ __global__ void __launch_bounds__(32 * G) rotate_q_kernel(const uint16_t *q, con
     float acc = 0.0f;
 #pragma unroll 16
     for (int i = 0; i < kHeadDim; ++i) acc = __fmaf_rn(qs[g][i], Rs[i][j], acc);
+    // The attention kernel that follows may launch only now: launched earlier, its CTAs take
+    // SM slots piecemeal while this and the previous kernels still hold some, and its clusters
+    // end up placed worse than on an idle GPU.
+    pdl_trigger();
     q_rot[(row0 + g) * kHeadDim + quarter * 32 + j] = acc;
 }
 

@@ -76,6 +76,16 @@ __global__ void __launch_bounds__(128) merge_kernel(PartialsView p, const float 
     }
     pdl_wait();                                  // the partials come from the previous kernels
 
+    // Issue the loads of this thread's accumulator column (history slots < kPre and the BF16
+    // slot) before anything that depends on them, so that they are all in flight at once.
+    constexpr int kPre = 48;
+    const float *acc = p.acc + row0 * kHeadDim + j;
+    float xs[kPre];
+#pragma unroll
+    for (int i = 0; i < kPre; ++i) xs[i] = i < S ? acc[(size_t)i * kHeadDim] : 0.0f;
+    const int c = RV ? z * kQuarter + (j & (kQuarter - 1)) : j;   // output channel (threads j < 32 with R_V)
+    const float xS = p.acc[(row0 + S) * kHeadDim + c];
+
     float mloc = -INFINITY;
     for (int i = j; i <= S; i += 128) {
         const float li = p.l[row0 + i], mi = p.m[row0 + i];
@@ -91,10 +101,19 @@ __global__ void __launch_bounds__(128) merge_kernel(PartialsView p, const float 
     for (int i = j; i <= S; i += 128) ws[i] = ls[i] > 0.0f ? exp2_taylor(__fsub_rn(ws[i], M)) : 0.0f;
     __syncthreads();
 
+    // empty slots are skipped by select: L = fma(l_i, w_i, L), A = fma(acc_i, w_i, A), i ascending
     float L = 0.0f, A = 0.0f;
-    const float *acc = p.acc + row0 * kHeadDim + j;
+#pragma unroll
+    for (int i = 0; i < kPre; ++i) {
+        if (i < S) {
+            const float li = ls[i], w = ws[i];
+            const bool on = li > 0.0f;
+            L = on ? __fmaf_rn(li, w, L) : L;
+            A = on ? __fmaf_rn(xs[i], w, A) : A;
+        }
+    }
 #pragma unroll 8
-    for (int i = 0; i < S; ++i) {            // empty slots are skipped by select, so loads issue early
+    for (int i = kPre; i < S; ++i) {
         const float li = ls[i], w = ws[i];
         const float x = acc[(size_t)i * kHeadDim];
         const bool on = li > 0.0f;
@@ -102,12 +121,10 @@ __global__ void __launch_bounds__(128) merge_kernel(PartialsView p, const float 
         A = on ? __fmaf_rn(x, w, A) : A;
     }
     float Ar = A;
-    int c = j;                               // output channel of this thread
     if (RV) {
         As[j] = A;
         __syncthreads();
         if (j >= kQuarter) return;
-        c = z * kQuarter + j;
         float r = 0.0f;
 #pragma unroll 8
         for (int i = 0; i < kHeadDim; ++i) r = __fmaf_rn(As[i], Rs[j * kPad + i], r);
@@ -116,7 +133,7 @@ __global__ void __launch_bounds__(128) merge_kernel(PartialsView p, const float 
     if (ls[S] > 0.0f) {
         const float w = ws[S];
         L = __fmaf_rn(ls[S], w, L);
-        Ar = __fmaf_rn(p.acc[(row0 + S) * kHeadDim + c], w, Ar);
+        Ar = __fmaf_rn(xS, w, Ar);
     }
     const float o = L > 0.0f ? __fdiv_rn(Ar, L) : 0.0f;
     const size_t orow = (size_t)b * n_q_heads + hq;

@@ -127,10 +127,12 @@ bool int2_mma_supported(const oscar_layout_t &L);
 // CTAs per cluster the tensor-core INT2 kernel will use for this layout (8 if no device is
 // visible); *active (optional) gets how many such clusters are resident at once (0 if unknown).
 int int2_mma_cluster_size(const oscar_layout_t &L, int *active = nullptr);
-cudaError_t launch_int2_attention_mma(const oscar_layout_t &L, const float *q_rot, Int2PoolView pool,
-                                      const int32_t *pt, int max_pages, const int32_t *seq_len,
-                                      const int32_t *hist_end, int batch, float sm_scale, PartialsView out,
-                                      int32_t *status, cudaStream_t st);
+// The tensor-core INT2 history splits (history) and/or the BF16 sink/recent window
+// (window) in one launch; the window CTAs write partial slot S.
+cudaError_t launch_decode_mma(const oscar_layout_t &L, const float *q_rot, Int2PoolView pool, const int32_t *pt,
+                              const uint16_t *q, Bf16PoolView bpool, const int32_t *bpt, int max_pages,
+                              const int32_t *seq_len, const int32_t *hist_end, int batch, float sm_scale,
+                              PartialsView out, int32_t *status, bool history, bool window, cudaStream_t st);
 
 // Tensor-core BF16 kernel (mode 0 any n_kv_heads; mode 1 n_kv_heads in {1, 2, 4, 8}).
 bool bf16_mma_supported(const oscar_layout_t &L, int mode);

@@ -144,9 +144,10 @@ OSCAR_API size_t oscar_partials_acc_floats(const oscar_layout_t *layout, int32_t
  * A split count that fills the GPU for `batch` requests whose longest history
  * spans max_hist_tokens tokens, in one wave: each split is computed by a
  * cluster of up to 8 CTAs that combine their results before writing the
- * split's partial, and the count is the number of such clusters the current
- * device keeps resident at once divided by `batch` (sm_count is used when no
- * device is visible); at least one 16-token history tile per split, clamped
+ * split's partial, one more cluster per request computes the BF16 window, and
+ * the count is the number of such clusters the current device keeps resident
+ * at once divided by `batch`, minus that window cluster (sm_count is used when
+ * no device is visible); at least one 16-token history tile per split, clamped
  * to [1, 1024].
  */
 OSCAR_API int32_t oscar_suggest_splits(const oscar_layout_t *layout, int32_t batch, int32_t max_hist_tokens,
@@ -214,7 +215,9 @@ OSCAR_API oscar_status_t oscar_rotate_q(const oscar_layout_t *layout, const uint
  * 16-token tiles (tile i = positions 16i..16i+15): with first = sink/16 and
  * n = ceil(h/16) - first, split s covers tiles [first + floor(s·n/S),
  * first + floor((s+1)·n/S)) clipped to [sink, h); the BF16 partial covers
- * [0, sink) ∪ [h, T).
+ * [0, sink) ∪ [h, T).  When the tensor-core kernels support the layout (1, 2,
+ * 4 or 8 kv heads) both parts are computed by one launch, whose last cluster
+ * per request takes the BF16 window.
  */
 OSCAR_API oscar_status_t oscar_decode_attention(const oscar_layout_t *layout,
                                       const uint16_t *q, const float *q_rot,
@@ -229,7 +232,8 @@ OSCAR_API oscar_status_t oscar_decode_attention(const oscar_layout_t *layout,
  * streams so that they overlap (they write disjoint slots of `partials`):
  * _history writes the history slots 0..S-1 from the INT2 pool and q_rot;
  * _window writes the BF16 slot S (sink + recent) from the BF16 pool and q.
- * Arguments as for oscar_decode_attention.
+ * Arguments as for oscar_decode_attention.  Each half writes the same bits as
+ * the combined call.
  */
 OSCAR_API oscar_status_t oscar_decode_attention_history(const oscar_layout_t *layout, const float *q_rot,
                                                         const oscar_int2_pool_t *int2_pool,
