@@ -41,7 +41,7 @@ D = 128
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["oscar", "reference"], default="oscar")
     ap.add_argument("--workload", default="qwen3_8b_100k", choices=sorted(syn.WORKLOADS))
@@ -113,7 +113,7 @@ def source_hash() -> str:
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 200 ms while the timed region runs."""
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms while the timed region runs."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -126,7 +126,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -441,20 +441,21 @@ def main():
     ms_step = 1e3 * t / args.steps
     value = job_throughput(world, w.batch, t, args.steps)
 
-    # roofline: per-launch durations of the decode-attention call, events captured in a K-step graph
+    # roofline: per-launch durations of the decode-attention call, events captured in a KR-step graph
+    KR = min(args.steps, 20)
     evs = [[(torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
-            for _ in range(w.layers)] for _ in range(args.steps)]
+            for _ in range(w.layers)] for _ in range(KR)]
     gp = capture(lambda: model.step(events=evs[0], side=side))
     gk = torch.cuda.CUDAGraph()
     with torch.cuda.graph(gk):
-        for k in range(args.steps):
+        for k in range(KR):
             model.step(events=evs[k], side=side)
     for _ in range(args.warmup):
         gp.replay()
     torch.cuda.synchronize()
     gk.replay()
     torch.cuda.synchronize()
-    durs = [evs[k][l][0].elapsed_time(evs[k][l][1]) / 1e3 for k in range(args.steps) for l in range(w.layers)]
+    durs = [evs[k][l][0].elapsed_time(evs[k][l][1]) / 1e3 for k in range(KR) for l in range(w.layers)]
     dur = statistics.mean(durs)
     peaks = measured_peaks()
     # one decode-attention launch: INT2 history + BF16 window + q (bf16) + q_rot (fp32)
