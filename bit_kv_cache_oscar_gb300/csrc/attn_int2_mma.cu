@@ -276,8 +276,23 @@ __device__ void window_cta(const MmaArgs &a, float *wsm, float *res, int T, int 
     if (to_res) cluster_combine(a, res, Hq, b, S);
 }
 
-// token position within a 16-token tile -> PV k-column (the K permutation shared by A and B)
-__device__ __forceinline__ int kpos(int tok) { return (tok & 8) + 2 * (tok & 3) + ((tok >> 2) & 1); }
+constexpr float kLazy = 8.0f;   // log2 headroom before the running maximum is raised
+constexpr int kWsWords = 20;    // words per P-operand column: 2 tiles x 8 + 4 (bank spread)
+
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// (v0, v1) -> f16x2 of the round-to-nearest values (hi) and f16x2 of their residuals (lo)
+__device__ __forceinline__ void split2(float v0, float v1, uint32_t &hi, uint32_t &lo) {
+    const __half2 h = __floats2half2_rn(v0, v1);
+    const float2 hf = __half22float2(h);
+    const __half2 l = __floats2half2_rn(v0 - hf.x, v1 - hf.y);
+    hi = *reinterpret_cast<const uint32_t *>(&h);
+    lo = *reinterpret_cast<const uint32_t *>(&l);
+}
 
 template <int G, int NGRP>
 __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2)) int2_mma_kernel(MmaArgs a) {
@@ -425,13 +440,13 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2)) int2_mma_kernel(Mm
     const float csc = a.scale2 * kTwo24;
     const int rs = Hkv * NGRP;                  // scale/zero elements per token row in a stage
     const int arr_el = a.arr_bytes / 2;
-    __half *Ws = reinterpret_cast<__half *>(smem + 128 + warp * a.ws_bytes);
+    uint32_t *Ws = reinterpret_cast<uint32_t *>(smem + 128 + warp * a.ws_bytes);   // [NGRP][NCOL][kWsWords]
 
-    float m_run[NT], l_run[NT], zs[NT][NGRP];
+    float m_run[NT], m_true[NT], l_run[NT], zs[NT][NGRP];
     float oacc[NT][8][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-        m_run[nt] = -INFINITY;
+        m_run[nt] = m_true[nt] = -INFINITY;
         l_run[nt] = 0.f;
 #pragma unroll
         for (int jg = 0; jg < NGRP; ++jg) zs[nt][jg] = 0.f;
@@ -498,20 +513,26 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2)) int2_mma_kernel(Mm
                 }
             }
 
-            // ---- logits of 4 tokens per thread, online softmax over the 32 tokens, P*scale -> Ws
+            // ---- logits of 4 tokens per thread, online softmax over the 32 tokens, P*scale -> Ws.
+            // Tiles start inside [r.lo, r.hi) (r.lo is a tile boundary), so a token is valid when its
+            // tile holds data and it lies below r.hi.  The running maximum is raised only when the
+            // pass's maximum exceeds it by more than kLazy (so P <= 2^kLazy and most passes skip the
+            // rescale); the true maximum is tracked alongside and restored at the end.
             float alpha[NT];
+            int lim[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+                lim[u] = uok[u] ? r.hi - (r.tile_lo + it * kTilesPerStage + jt[u]) * kTileTokens : 0;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 float tv[2][2];
-                bool vok[2][2];
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
                     const uint16_t *sk = reinterpret_cast<const uint16_t *>(sb + a.off_s) +
                                          jt[u] * kTileTokens * rs + h * NGRP;
-                    const int pos0 = (r.tile_lo + it * kTilesPerStage + jt[u]) * kTileTokens;
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        const int tok = gid + 8 * e, p = pos0 + tok;
+                        const int tok = gid + 8 * e;
                         float tt = 0.f;
 #pragma unroll
                         for (int jg = 0; jg < NGRP; ++jg) {
@@ -519,22 +540,25 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2)) int2_mma_kernel(Mm
                             const float dot = sacc[u][nt][jg][2 * e] + sacc[u][nt][jg][2 * e + 1];
                             tt += fmaf(sc * csc, dot, zc * qz[nt][jg]);
                         }
-                        vok[u][e] = uok[u] && p >= r.lo && p < r.hi;
-                        tv[u][e] = vok[u][e] ? tt : -INFINITY;
+                        tv[u][e] = tok < lim[u] ? tt : -INFINITY;
                     }
                 }
                 float mx = fmaxf(fmaxf(tv[0][0], tv[0][1]), fmaxf(tv[1][0], tv[1][1]));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-                const float mn = fmaxf(m_run[nt], mx);
-                float pv[2][2] = {{0.f, 0.f}, {0.f, 0.f}}, al = 1.f;
+                m_true[nt] = fmaxf(m_true[nt], mx);
+                float mn = m_run[nt], al = 1.f;
+                if (mx > mn + kLazy) {                 // also the first finite maximum (mn = -inf)
+                    al = ex2_approx(mn - mx);
+                    mn = mx;
+                }
+                float pv[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
                 if (mn != -INFINITY) {
-                    al = exp2f(m_run[nt] - mn);
 #pragma unroll
                     for (int u = 0; u < 2; ++u)
 #pragma unroll
-                        for (int e = 0; e < 2; ++e) pv[u][e] = exp2f(tv[u][e] - mn);
+                        for (int e = 0; e < 2; ++e) pv[u][e] = ex2_approx(tv[u][e] - mn);
                 }
                 alpha[nt] = al;
                 m_run[nt] = mn;
@@ -542,23 +566,28 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2)) int2_mma_kernel(Mm
 #pragma unroll
                 for (int jg = 0; jg < NGRP; ++jg) {
                     float zadd = 0.f;
-                    __half *Wg = Ws + jg * NCOL * 32;
+                    uint32_t *Wg = Ws + jg * NCOL * kWsWords;
                     const int c_hi = nt * 8 + 2 * t;
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
                         const uint16_t *sk = reinterpret_cast<const uint16_t *>(sb + a.off_s) +
                                              jt[u] * kTileTokens * rs + h * NGRP;
+                        float w[2];
 #pragma unroll
                         for (int e = 0; e < 2; ++e) {
                             const int tok = gid + 8 * e;
                             const float svv = bf16_to_f32(sk[2 * arr_el + tok * rs + jg]);
                             const float zvv = bf16_to_f32(sk[3 * arr_el + tok * rs + jg]);
-                            const float w = vok[u][e] ? pv[u][e] * svv : 0.f;
-                            zadd += vok[u][e] ? pv[u][e] * zvv : 0.f;
-                            const int kc = u * 16 + kpos(tok);
-                            Wg[c_hi * 32 + kc] = split_part(w, 0);
-                            Wg[(c_hi + 1) * 32 + kc] = split_part(w, 1);
+                            // rows past the valid range hold arbitrary bits (NaN included): select, never multiply
+                            const bool ok = tok < lim[u];
+                            w[e] = ok ? pv[u][e] * svv : 0.f;
+                            zadd = ok ? fmaf(pv[u][e], zvv, zadd) : zadd;
                         }
+                        // tokens gid, gid + 8 are PV k-columns 2 gid, 2 gid + 1 of tile u: one word
+                        uint32_t hi, lo;
+                        split2(w[0], w[1], hi, lo);
+                        Wg[c_hi * kWsWords + u * 8 + gid] = hi;
+                        Wg[(c_hi + 1) * kWsWords + u * 8 + gid] = lo;
                     }
                     zs[nt][jg] = fmaf(zs[nt][jg], al, zadd);
                 }
@@ -581,9 +610,10 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2)) int2_mma_kernel(Mm
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const uint8_t *Vc = sb + a.off_v + h * 2048 + jt[u] * kTileTokens * 32;
+                // k-columns 2t, 2t+1 <- tokens t, t+8; 2t+8, 2t+9 <- tokens t+4, t+12
                 const uint32_t X = *reinterpret_cast<const uint32_t *>(Vc + t * 32 + 4 * gid);
-                const uint32_t Y = *reinterpret_cast<const uint32_t *>(Vc + (t + 4) * 32 + 4 * gid);
-                const uint32_t X2 = *reinterpret_cast<const uint32_t *>(Vc + (t + 8) * 32 + 4 * gid);
+                const uint32_t Y = *reinterpret_cast<const uint32_t *>(Vc + (t + 8) * 32 + 4 * gid);
+                const uint32_t X2 = *reinterpret_cast<const uint32_t *>(Vc + (t + 4) * 32 + 4 * gid);
                 const uint32_t Y2 = *reinterpret_cast<const uint32_t *>(Vc + (t + 12) * 32 + 4 * gid);
                 const uint32_t P1 = __byte_perm(X, Y, 0x5410), P2 = __byte_perm(X, Y, 0x6521);
                 const uint32_t P3 = __byte_perm(X, Y, 0x7632), P4 = __byte_perm(X, Y, 0x7733);
@@ -594,9 +624,9 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2)) int2_mma_kernel(Mm
                 for (int jg = 0; jg < NGRP; ++jg)
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) {
-                        const __half *col = Ws + jg * NCOL * 32 + (nt * 8 + gid) * 32 + u * 16;
-                        bw[jg][nt][0] = *reinterpret_cast<const uint32_t *>(col + 2 * t);
-                        bw[jg][nt][1] = *reinterpret_cast<const uint32_t *>(col + 2 * t + 8);
+                        const uint32_t *col = Ws + jg * NCOL * kWsWords + (nt * 8 + gid) * kWsWords + u * 8;
+                        bw[jg][nt][0] = col[t];
+                        bw[jg][nt][1] = col[t + 4];
                     }
 #pragma unroll
                 for (int mt = 0; mt < 8; ++mt) {
@@ -632,6 +662,14 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2)) int2_mma_kernel(Mm
         }
     }
     const int gv = gid * NGRP / 8;
+    // back to the split's true maximum: l, the zero-point sum and the accumulators scale by 2^(m_run - m_true)
+    float fix[NT];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        fix[nt] = m_true[nt] == -INFINITY ? 1.f : ex2_approx(m_run[nt] - m_true[nt]);
+        l_run[nt] *= fix[nt];
+        m_run[nt] = m_true[nt];
+    }
     float outv[NT][16];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
@@ -641,8 +679,8 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2)) int2_mma_kernel(Mm
             if (gv == jg) z = zs[nt][jg];
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
-            outv[nt][2 * mt] = fmaf(oacc[nt][mt][0] + oacc[nt][mt][1], kTwo24 / pv_factor(2 * mt), z);
-            outv[nt][2 * mt + 1] = fmaf(oacc[nt][mt][2] + oacc[nt][mt][3], kTwo24 / pv_factor(2 * mt + 1), z);
+            outv[nt][2 * mt] = fmaf(oacc[nt][mt][0] + oacc[nt][mt][1], kTwo24 / pv_factor(2 * mt), z) * fix[nt];
+            outv[nt][2 * mt + 1] = fmaf(oacc[nt][mt][2] + oacc[nt][mt][3], kTwo24 / pv_factor(2 * mt + 1), z) * fix[nt];
         }
     }
 
@@ -776,7 +814,7 @@ int mma_smem_plan(const oscar_layout_t &L, MmaArgs &a) {
     a.arr_bytes = kStageTok * Hkv * NGRP * 2;
     a.off_s = 2 * a.off_v;
     a.stage_bytes = (a.off_s + 4 * a.arr_bytes + 127) & ~127;
-    a.ws_bytes = NGRP * 8 * NT * 32 * 2;
+    a.ws_bytes = NGRP * 8 * NT * kWsWords * 4;
     a.stage_off = 128 + ((kCW * a.ws_bytes + 127) & ~127);
     const int budget = (G == 8 ? 200 : 110) * 1024;    // two CTAs per SM below G = 8
     int stages = kMaxStages;
