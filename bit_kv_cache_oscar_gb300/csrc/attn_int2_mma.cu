@@ -26,7 +26,9 @@
 //    per-warp shared buffer; each warp takes two 16-token tiles per pass.
 // Every wait is bounded: a wait that gives up sets OSCAR_DEV_WAIT_TIMEOUT.
 
+#include <cuda.h>
 #include <cuda_fp16.h>
+#include <cstring>
 
 #include "oscar_internal.cuh"
 #include "ptx.cuh"
@@ -294,11 +296,17 @@ __device__ __forceinline__ void split2(float v0, float v1, uint32_t &hi, uint32_
     lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 
-template <int G, int NGRP>
-__global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2)) int2_mma_kernel(MmaArgs a) {
+// TMA: 8 kv heads.  The copy warp moves each tile's codes with two 2-D tensor-map boxes per
+// array (16 rows x 128 bytes = 4 heads, 128-byte swizzle) and its scale/zero rows with 1-D bulk
+// copies; otherwise (1, 2 or 4 kv heads) it scatters 16-byte cp.async chunks head-major.
+template <int G, int NGRP, bool TMA>
+__global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
+    int2_mma_kernel(MmaArgs a, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
     constexpr int NT = (G == 8) ? 2 : 1;      // n-tiles of 8 columns: 4 heads x {hi, lo} each
     constexpr int NCOL = 8 * NT;
-    extern __shared__ __align__(128) uint8_t smem[];
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    // swizzled boxes land on 1024-byte boundaries: the carve-up starts at an aligned address
+    uint8_t *smem = smem_raw + ((1024u - (saddr(smem_raw) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);   // full[0..3], empty[4..7]
     int *masks = reinterpret_cast<int *>(smem + 64);        // per stage: bit j = tile j holds data
     uint8_t *stage0 = smem + a.stage_off;
@@ -319,7 +327,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2)) int2_mma_kernel(Mm
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < a.stages; ++i) {
-            mbar_init(saddr(&bars[i]), 33);      // 32 copy-completion arrivals + the mask arrival
+            mbar_init(saddr(&bars[i]), TMA ? 1 : 33);   // TMA: the expect-tx arrival; else 32 cp.async + mask
             mbar_init(saddr(&bars[4 + i]), kCW);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -329,17 +337,15 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2)) int2_mma_kernel(Mm
     // ------------------------------------------------------------ producer --
     if (warp == kCW) {
         const int lgH = Hkv == 1 ? 0 : Hkv == 2 ? 1 : Hkv == 4 ? 2 : 3;
-        // lanes 0..3 hold the page ids of the stage's 4 tiles, loaded one stage ahead
-        auto page_of = [&](int it) -> int {
-            const int tile = r.tile_lo + it * kTilesPerStage + lane;
-            return (lane < kTilesPerStage && tile < r.tile_hi)
-                       ? a.pt[(size_t)b * a.max_pages + tile * kTileTokens / a.page_size] : -1;
-        };
-        int pg_next = page_of(0);
+        // Page ids of 32 consecutive logical pages, lane i holding page pg_base + i: one load
+        // serves 32 pages (128 tiles at 64-token pages), so the copies never wait on the table.
+        const int tpp = a.page_size / kTileTokens;           // tiles per page
+        const int tile_bytes = 2 * kTileTokens * 8 * 32 + 4 * kTileTokens * 8 * NGRP * 2;   // TMA path (8 heads)
+        const int32_t *prow = a.pt + (size_t)b * a.max_pages;
+        int pg_base = r.tile_lo / tpp;
+        int pg_reg = (pg_base + lane < a.max_pages) ? prow[pg_base + lane] : -1;
         bool ok = true;
         for (int it = 0; it < n_iters && ok; ++it) {
-            const int pg_mine = pg_next;
-            pg_next = page_of(it + 1);
             const int st = it % a.stages;
             if (it >= a.stages && !mbar_wait(saddr(&bars[4 + st]), ((it / a.stages) - 1) & 1)) {
                 if (lane == 0) flag_status(a.status, OSCAR_DEV_WAIT_TIMEOUT);
@@ -348,11 +354,57 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2)) int2_mma_kernel(Mm
             }
             uint8_t *sb = stage0 + st * a.stage_bytes;
             int mask = 0;
+            if constexpr (TMA) {
+                // lane = 8 j + op: op 0..3 the code boxes (K lo/hi heads, V lo/hi), 4..7 scale/zero rows
+                const int jl = lane >> 3, op = lane & 7;
+                int row0 = 0;
+                for (int j = 0; j < kTilesPerStage; ++j) {
+                    const int tile = r.tile_lo + it * kTilesPerStage + j;
+                    if (tile >= r.tile_hi) break;
+                    const int lp = tile / tpp;
+                    if (lp - pg_base >= 32) {
+                        pg_base = lp;
+                        pg_reg = (pg_base + lane < a.max_pages) ? prow[pg_base + lane] : -1;
+                    }
+                    const int page = __shfl_sync(0xffffffffu, pg_reg, lp - pg_base);
+                    if (page < 0 || page >= a.pool.n_pages) {
+                        if (lane == 0) flag_status(a.status, OSCAR_DEV_BAD_INT2_PAGE);
+                        continue;
+                    }
+                    mask |= 1 << j;
+                    if (j == jl) row0 = page * a.page_size + (tile * kTileTokens) % a.page_size;
+                }
+                const uint32_t full = saddr(&bars[st]);
+                if (lane == 0) {
+                    masks[st] = mask;
+                    mbar_arrive_expect_tx(full, __popc(mask) * tile_bytes);
+                }
+                __syncwarp();
+                if ((mask >> jl) & 1) {
+                    const uint32_t d = saddr(sb) + jl * 4096;
+                    if (op < 4) {
+                        tma_load_2d(d + (op >> 1) * a.off_v + (op & 1) * 2048, (op >> 1) ? &tmv : &tmk, (op & 1) * 128,
+                                    row0, full);
+                    } else {
+                        const int arr = op - 4, nsb = kTileTokens * 8 * NGRP * 2;   // bytes of one tile's rows
+                        const uint16_t *src = arr == 0 ? a.pool.scale_k : arr == 1 ? a.pool.zero_k
+                                            : arr == 2 ? a.pool.scale_v : a.pool.zero_v;
+                        tma_load_1d(saddr(sb + a.off_s) + arr * a.arr_bytes + jl * nsb, src + (size_t)row0 * 8 * NGRP,
+                                    nsb, full);
+                    }
+                }
+                continue;
+            }
             for (int j = 0; j < kTilesPerStage; ++j) {
                 const int tile = r.tile_lo + it * kTilesPerStage + j;
                 if (tile >= r.tile_hi) break;
                 const int pos0 = tile * kTileTokens;
-                const int page = __shfl_sync(0xffffffffu, pg_mine, j);
+                const int lp = tile / tpp;
+                if (lp - pg_base >= 32) {                      // warp-uniform refill of the page window
+                    pg_base = lp;
+                    pg_reg = (pg_base + lane < a.max_pages) ? prow[pg_base + lane] : -1;
+                }
+                const int page = __shfl_sync(0xffffffffu, pg_reg, lp - pg_base);
                 if (page < 0 || page >= a.pool.n_pages) {
                     if (lane == 0) flag_status(a.status, OSCAR_DEV_BAD_INT2_PAGE);
                     continue;
@@ -437,6 +489,28 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2)) int2_mma_kernel(Mm
                 if (hh == nt * 4 + t) qz[nt][jg] = x * a.scale2;
         }
     }
+    // Byte offsets of this thread's code words inside a tile (rows gid / gid+8 for K; rows t,
+    // t+8, t+4, t+12 for V), and the tile base of head h.  TMA tiles are [2 halves][16 rows][128 B]
+    // with 16-byte chunk c of row r stored at chunk c ^ (r & 7); cp.async tiles are [head][row][32 B].
+    int kofs0, kofs1, vofs[4];
+    {
+        const int vrow[4] = {t, t + 8, t + 4, t + 12};
+        if constexpr (TMA) {
+            const int hh = h & 3, ck = 2 * hh + (t >> 1), cv = 2 * hh + (gid >> 2);
+            kofs0 = gid * 128 + ((ck ^ gid) << 4) + (t & 1) * 8;
+            kofs1 = kofs0 + 8 * 128;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) vofs[i] = vrow[i] * 128 + ((cv ^ (vrow[i] & 7)) << 4) + (gid & 3) * 4;
+        } else {
+            kofs0 = gid * 32 + 8 * t;
+            kofs1 = kofs0 + 8 * 32;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) vofs[i] = vrow[i] * 32 + 4 * gid;
+        }
+    }
+    auto tile_base = [&](const uint8_t *arr, int j) -> const uint8_t * {
+        return TMA ? arr + j * 4096 + (h >> 2) * 2048 : arr + h * 2048 + j * (kTileTokens * 32);
+    };
     const float csc = a.scale2 * kTwo24;
     const int rs = Hkv * NGRP;                  // scale/zero elements per token row in a stage
     const int arr_el = a.arr_bytes / 2;
@@ -486,9 +560,9 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2)) int2_mma_kernel(Mm
             uint2 kw0[2], kw1[2];
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-                const uint8_t *Kc = sb + h * 2048 + jt[u] * kTileTokens * 32;
-                kw0[u] = *reinterpret_cast<const uint2 *>(Kc + gid * 32 + 8 * t);
-                kw1[u] = *reinterpret_cast<const uint2 *>(Kc + (gid + 8) * 32 + 8 * t);
+                const uint8_t *Kc = tile_base(sb, jt[u]);
+                kw0[u] = *reinterpret_cast<const uint2 *>(Kc + kofs0);
+                kw1[u] = *reinterpret_cast<const uint2 *>(Kc + kofs1);
             }
 #pragma unroll
             for (int kap = 0; kap < 2; ++kap) {
@@ -609,12 +683,12 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2)) int2_mma_kernel(Mm
             const int gv = gid * NGRP / 8;
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-                const uint8_t *Vc = sb + a.off_v + h * 2048 + jt[u] * kTileTokens * 32;
+                const uint8_t *Vc = tile_base(sb + a.off_v, jt[u]);
                 // k-columns 2t, 2t+1 <- tokens t, t+8; 2t+8, 2t+9 <- tokens t+4, t+12
-                const uint32_t X = *reinterpret_cast<const uint32_t *>(Vc + t * 32 + 4 * gid);
-                const uint32_t Y = *reinterpret_cast<const uint32_t *>(Vc + (t + 8) * 32 + 4 * gid);
-                const uint32_t X2 = *reinterpret_cast<const uint32_t *>(Vc + (t + 4) * 32 + 4 * gid);
-                const uint32_t Y2 = *reinterpret_cast<const uint32_t *>(Vc + (t + 12) * 32 + 4 * gid);
+                const uint32_t X = *reinterpret_cast<const uint32_t *>(Vc + vofs[0]);
+                const uint32_t Y = *reinterpret_cast<const uint32_t *>(Vc + vofs[1]);
+                const uint32_t X2 = *reinterpret_cast<const uint32_t *>(Vc + vofs[2]);
+                const uint32_t Y2 = *reinterpret_cast<const uint32_t *>(Vc + vofs[3]);
                 const uint32_t P1 = __byte_perm(X, Y, 0x5410), P2 = __byte_perm(X, Y, 0x6521);
                 const uint32_t P3 = __byte_perm(X, Y, 0x7632), P4 = __byte_perm(X, Y, 0x7733);
                 const uint32_t Q1 = __byte_perm(X2, Y2, 0x5410), Q2 = __byte_perm(X2, Y2, 0x6521);
@@ -815,7 +889,7 @@ int mma_smem_plan(const oscar_layout_t &L, MmaArgs &a) {
     a.off_s = 2 * a.off_v;
     a.stage_bytes = (a.off_s + 4 * a.arr_bytes + 127) & ~127;
     a.ws_bytes = NGRP * 8 * NT * kWsWords * 4;
-    a.stage_off = 128 + ((kCW * a.ws_bytes + 127) & ~127);
+    a.stage_off = (128 + kCW * a.ws_bytes + 1023) & ~1023;   // stages start 1024-byte aligned
     const int budget = (G == 8 ? 200 : 110) * 1024;    // two CTAs per SM below G = 8
     int stages = kMaxStages;
     while (stages > 2 && a.stage_off + stages * a.stage_bytes > budget) --stages;
@@ -824,20 +898,65 @@ int mma_smem_plan(const oscar_layout_t &L, MmaArgs &a) {
     a.res_off = combine;
     a.win_off = a.res_off + Hq * (2 + kHeadDim) * 4;
     const int tail = a.win_off + kCW * G * (2 + kHeadDim) * 4;
-    return a.stage_off + (stages * a.stage_bytes > tail ? stages * a.stage_bytes : tail);
+    // + 1024: the kernel rounds the dynamic shared memory base up to a 1024-byte boundary
+    return 1024 + a.stage_off + (stages * a.stage_bytes > tail ? stages * a.stage_bytes : tail);
 }
 
 template <int G, int NGRP>
 int mma_cluster_size(const oscar_layout_t &L, int *active) {
     MmaArgs a{};
     const int smem = mma_smem_plan<G, NGRP>(L, a);
-    return int2_cluster_size(reinterpret_cast<const void *>(int2_mma_kernel<G, NGRP>), smem, kThreads, active);
+    const void *kern = L.n_kv_heads == 8 ? reinterpret_cast<const void *>(int2_mma_kernel<G, NGRP, true>)
+                                         : reinterpret_cast<const void *>(int2_mma_kernel<G, NGRP, false>);
+    return int2_cluster_size(kern, smem, kThreads, active);
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+// cuTensorMapEncodeTiled from the driver, looked up once through the runtime.
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        EncodeTiledFn f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            f = reinterpret_cast<EncodeTiledFn>(p);
+        cudaGetLastError();
+        return f;
+    }();
+    return fn;
+}
+
+// An INT2 codes array of 8 kv heads, [rows = n_pages * page_size][256 bytes], as a 2-D uint8 tensor
+// map whose box is 16 rows x 128 bytes (4 heads) with 128-byte swizzle.
+bool codes_tensor_map(CUtensorMap *tm, const uint8_t *base, long long rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || !base) return false;
+    const cuuint64_t dims[2] = {256, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {256};
+    const cuuint32_t box[2] = {128, (cuuint32_t)kTileTokens};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int G, int NGRP>
 cudaError_t launch_mma(const oscar_layout_t &L, MmaArgs a, int batch, bool history, bool window, cudaStream_t st) {
     const int smem = mma_smem_plan<G, NGRP>(L, a);
-    auto kern = int2_mma_kernel<G, NGRP>;
+    const bool tma = L.n_kv_heads == 8;
+    auto kern = tma ? int2_mma_kernel<G, NGRP, true> : int2_mma_kernel<G, NGRP, false>;
+    CUtensorMap tmk, tmv;
+    memset(&tmk, 0, sizeof(tmk));
+    memset(&tmv, 0, sizeof(tmv));
+    if (tma && history) {
+        const long long rows = (long long)a.pool.n_pages * L.page_size;
+        if (!codes_tensor_map(&tmk, a.pool.codes_k, rows) || !codes_tensor_map(&tmv, a.pool.codes_v, rows))
+            return cudaErrorInvalidValue;
+    }
     a.csize = int2_cluster_size(reinterpret_cast<const void *>(kern), smem, kThreads);
     a.hist_ctas = history ? a.out.S * a.csize : 0;
     cudaLaunchConfig_t cfg = {};
@@ -853,7 +972,7 @@ cudaError_t launch_mma(const oscar_layout_t &L, MmaArgs a, int batch, bool histo
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     add_overlap_attr(cfg, attr);
-    return cudaLaunchKernelEx(&cfg, kern, a);
+    return cudaLaunchKernelEx(&cfg, kern, a, tmk, tmv);
 }
 
 }  // namespace

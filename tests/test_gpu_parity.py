@@ -172,6 +172,7 @@ def test_merge_bit_exact(S, empty):
             assert np.array_equal(ob16[b, hq], rb)
 
 
+@pytest.mark.parametrize("n_kv", [2, 8])          # 8 kv heads: the tensor-map copy path
 @pytest.mark.parametrize("seq,hist,gqa,ps,group,S", [
     ((1024, 700, 333), None, 4, 16, 128, 4),          # ragged batch, short request with little history
     ((40,), None, 4, 16, 128, 2),                      # shorter than the sink: no history at all
@@ -180,8 +181,8 @@ def test_merge_bit_exact(S, empty):
     ((1500,), None, 1, 32, 64, 6),                     # G=1, group 64
     ((1100,), (843,), 2, 16, 128, 5),                  # history end mid-page, one demoted row still BF16
 ])
-def test_decode_edge_cases(seq, hist, gqa, ps, group, S):
-    case = sc.make_case(n_kv=2, gqa=gqa, page_size=ps, group=group, seq=seq, hist_end=hist)
+def test_decode_edge_cases(seq, hist, gqa, ps, group, S, n_kv):
+    case = sc.make_case(n_kv=n_kv, gqa=gqa, page_size=ps, group=group, seq=seq, hist_end=hist)
     sc.upload(case)
     out, out32, lse, _ = sc.run_decode(case, S)
     _check_outputs(case, out, out32, lse)
