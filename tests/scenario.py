@@ -55,22 +55,24 @@ class Case:
 
 
 def make_case(n_kv=2, gqa=4, page_size=16, group=128, seq=(1024,), seed=0, layer=0, hist_end=None,
-              sink=64, recent=256, device="cuda") -> Case:
+              sink=64, recent=256, device="cuda", gen_device="cpu", shared_prefix=0) -> Case:
+    """gen_device="cuda" draws K/V on the GPU (long contexts); both sides still get the same
+    tensors (the oracle reads the sampled heads back)."""
     layout = ob.Layout(n_kv, gqa, page_size, group, sink, recent)
     prof, RK, RV = oracle_rotations(seed, layer, n_kv, gqa)
     w = syn.Workload("case", 1, n_kv * gqa, n_kv, len(seq), max(seq), page_size, group=group,
-                     sink=sink, recent=recent, seed=seed)
+                     sink=sink, recent=recent, seed=seed, shared_prefix=shared_prefix)
     pages = syn.page_layout(w, list(seq), hist_end=hist_end)
     K, V = [], []
     for b, T in enumerate(seq):
-        k, v = syn.kv_rows(seed, layer, b, 0, T, prof)
+        k, v = syn.kv_rows(seed, layer, b, 0, T, prof, device=gen_device, shared_prefix=shared_prefix)
         K.append(k)
         V.append(v)
     q = syn.queries(seed, layer, len(seq), gqa, prof)
     return Case(layout, list(seq), pages.hist_end.copy(), K, V, q, RK, RV, pages, 1.0 / math.sqrt(D))
 
 
-def upload(case: Case, device="cuda", demote_history=True):
+def upload(case: Case, device="cuda", demote_history=True, keep_rotated=True):
     """Allocate pools and fill them: BF16 rows where the page layout keeps BF16 pages, and the
     history demoted through oscar_demote from a staging pool holding every row."""
     L, P = case.layout, case.pages
@@ -94,12 +96,11 @@ def upload(case: Case, device="cuda", demote_history=True):
     st_table = -np.ones((B, P.int2_table.shape[1]), np.int32)
     base = 0
     for b, T in enumerate(case.seq):
-        for lp in range(n_log[b]):
-            p0, p1 = lp * ps, min(T, (lp + 1) * ps)
-            stage.k[base + lp, :p1 - p0] = case.K[b][p0:p1].to(device)
-            stage.v[base + lp, :p1 - p0] = case.V[b][p0:p1].to(device)
-            st_table[b, lp] = base + lp
-        base += n_log[b]
+        n = n_log[b]                       # logical pages of request b sit at base .. base+n-1
+        stage.k[base:base + n].reshape(n * ps, L.n_kv_heads, D)[:T] = case.K[b].to(device)
+        stage.v[base:base + n].reshape(n * ps, L.n_kv_heads, D)[:T] = case.V[b].to(device)
+        st_table[b, :n] = np.arange(base, base + n, dtype=np.int32)
+        base += n
     dev.update(
         bf16=bf, int2=i2, stage=stage,
         bf16_table=torch.from_numpy(P.bf16_table).to(device),
@@ -118,10 +119,11 @@ def upload(case: Case, device="cuda", demote_history=True):
         dev["demote_req"] = torch.tensor(req, dtype=torch.int32, device=device)
         dev["demote_pos"] = torch.tensor(pos, dtype=torch.int32, device=device)
         if req:
-            dev["rotated"] = torch.empty((len(req), 2, L.n_kv_heads, D), dtype=torch.float32, device=device)
+            if keep_rotated:
+                dev["rotated"] = torch.empty((len(req), 2, L.n_kv_heads, D), dtype=torch.float32, device=device)
             ob.oscar_demote(L, stage, dev["stage_table"], i2, dev["int2_table"], dev["demote_req"],
                             dev["demote_pos"], dev["RK"], dev["RV"], oracle.C_K, oracle.C_V,
-                            rotated_out=dev["rotated"])
+                            rotated_out=dev.get("rotated"))
     return dev
 
 

@@ -1,0 +1,100 @@
+"""Parity at the workloads' full sizes, on sampled (request, query head) outputs.
+
+Each case runs the decode step exactly as bench.py does (oscar_rotate_q ->
+oscar_decode_attention -> oscar_merge on one stream, launch overlap on, the
+library's split suggestion for the batch), then compares sampled heads with the
+oracle's fp64 attention over its own demotion of those heads' history.  Samples
+always include the shortest and the longest request.  K/V are drawn on the GPU
+(the oracle reads back the sampled heads), so the same tensors feed both sides.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oscar_synthetic as syn
+from bit_kv_cache_oscar_gb300 import binding as ob
+from tests import scenario as sc
+
+pytestmark = pytest.mark.gpu
+
+D = 128
+
+
+def _run_like_bench(case):
+    L, dev = case.layout, case.dev
+    B = len(case.seq)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    S = ob.oscar_suggest_splits(L, B, int(max(case.hist_end)) - L.sink, sms)
+    q_rot = torch.empty((B, L.n_q_heads, D), dtype=torch.float32, device="cuda")
+    part = ob.Partials.empty(L, B, S)
+    out32 = torch.empty((B, L.n_q_heads, D), dtype=torch.float32, device="cuda")
+    out = torch.empty((B, L.n_q_heads, D), dtype=torch.bfloat16, device="cuda")
+    try:
+        ob.oscar_set_launch_overlap(True)
+        ob.oscar_rotate_q(L, dev["q"], dev["RK"], q_rot)
+        ob.oscar_decode_attention(L, dev["q"], q_rot, dev["bf16"], dev["bf16_table"], dev["int2"],
+                                  dev["int2_table"], dev["seq_len"], dev["hist_end"], case.sm_scale, part)
+        ob.oscar_merge(L, part, dev["RV"], out, out32, None)
+        torch.cuda.synchronize()
+    finally:
+        ob.oscar_set_launch_overlap(False)
+    assert ob.oscar_get_device_status() == 0
+    return out, out32
+
+
+def _check(case, out, out32, pairs):
+    ref = sc.oracle_outputs(case, pairs)
+    o32 = out32.cpu().numpy()
+    ob16 = out.float().cpu().numpy()
+    for (b, hq), (o_ref, _) in ref.items():
+        ok, r, m = sc.tolerance_ok(o32[b, hq][None], o_ref[None])
+        assert ok, (b, hq, r, m)
+        # the bf16 output is the fp32 one rounded to nearest even
+        assert np.array_equal(ob16[b, hq], torch.from_numpy(o32[b, hq]).bfloat16().float().numpy())
+
+
+def _pairs(seq, gqa, kv_heads, per_head=2):
+    """Shortest and longest request x the given kv heads x per_head of their query heads."""
+    reqs = sorted({int(np.argmin(seq)), int(np.argmax(seq))})
+    pairs = []
+    for b in reqs:
+        for h in kv_heads:
+            for j in range(per_head):
+                pairs.append((b, h * gqa + (j * (gqa - 1)) // max(per_head - 1, 1)))
+    return pairs
+
+
+def test_fullsize_qwen3_8b_100k():
+    """The benchmark's workload: 32 q / 8 kv heads, one request of 100,000 tokens, page 64."""
+    w = syn.WORKLOADS["qwen3_8b_100k"]
+    case = sc.make_case(n_kv=w.n_kv_heads, gqa=w.n_q_heads // w.n_kv_heads, page_size=w.page_size,
+                        group=w.group, seq=(w.context,), gen_device="cuda")
+    sc.upload(case, keep_rotated=False)
+    out, out32 = _run_like_bench(case)
+    pairs = [(0, hq) for hq in (0, 3, 9, 14, 17, 22, 28, 31)]     # kv heads 0, 2, 4, 7
+    _check(case, out, out32, pairs)
+
+
+@pytest.mark.parametrize("name", ["qwen3_32b_131k_g128", "qwen3_32b_131k_g32"])
+def test_fullsize_qwen3_32b_131k(name):
+    """64 q / 8 kv heads (GQA 8), 4 requests of 131,072 tokens, groups of 128 and of 32."""
+    w = syn.WORKLOADS[name]
+    seq = tuple([w.context] * w.batch)
+    case = sc.make_case(n_kv=w.n_kv_heads, gqa=w.n_q_heads // w.n_kv_heads, page_size=w.page_size,
+                        group=w.group, seq=seq, gen_device="cuda")
+    sc.upload(case, keep_rotated=False)
+    out, out32 = _run_like_bench(case)
+    pairs = [(0, 8), (0, 15), (0, 48), (0, 55), (3, 8), (3, 15), (3, 48), (3, 55)]
+    _check(case, out, out32, pairs)
+
+
+def test_fullsize_ragged_shared_prefix():
+    """The ragged-batch shape (contexts drawn from 65,536..100,000, a 16,384-token prefix shared
+    through the page tables) at 4 requests instead of 32."""
+    w = syn.WORKLOADS["qwen3_8b_b32_ragged"]
+    seq = tuple(int(t) for t in syn.context_lengths(w)[:4])
+    case = sc.make_case(n_kv=w.n_kv_heads, gqa=w.n_q_heads // w.n_kv_heads, page_size=w.page_size,
+                        group=w.group, seq=seq, gen_device="cuda", shared_prefix=w.shared_prefix)
+    sc.upload(case, keep_rotated=False)
+    out, out32 = _run_like_bench(case)
+    _check(case, out, out32, _pairs(seq, case.layout.gqa, (1, 6)))
