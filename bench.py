@@ -2,8 +2,8 @@
 """Decode-attention benchmark of the OSCAR INT2 KV-cache path on GB300.
 
 One step = the attention of one decode token for every layer of the model:
-per layer, q -> q·R_K (oscar_rotate_q), INT2 history + BF16 sink/recent
-partials (oscar_decode_attention), online-softmax merge with R_V^T
+per layer, q·R_K + INT2 history + BF16 sink/recent partials in one launch
+(oscar_decode_attention_fused), then the online-softmax merge with R_V^T
 (oscar_merge); for workloads that demote every step, the demotion of the
 token leaving the recent window runs on a side stream in the same step.
 Steps are captured in a CUDA graph and timed with CUDA events.
@@ -263,12 +263,11 @@ class Model:
                     ob.oscar_demote(L, st["bf16"], self.bf16_table, st["int2"], self.int2_table, self.dem_req,
                                     self.dem_pos, st["RK"], st["RV"], 0.96, 0.92, stream=side)
         for l, st in enumerate(self.layers):
-            ob.oscar_rotate_q(L, self.q_all[l], st["RK"], self.q_rot)
             if events is not None:
                 events[l][0].record()
-            # history splits and the BF16 window in one launch
-            ob.oscar_decode_attention(L, self.q_all[l], self.q_rot, st["bf16"], self.bf16_table, st["int2"],
-                                      self.int2_table, self.seq_len, self.hist_dev, self.sm_scale, self.part)
+            # query rotation, history splits and the BF16 window in one launch
+            ob.oscar_decode_attention_fused(L, self.q_all[l], st["RK"], st["bf16"], self.bf16_table, st["int2"],
+                                            self.int2_table, self.seq_len, self.hist_dev, self.sm_scale, self.part)
             if events is not None:
                 events[l][1].record()
             ob.oscar_merge(L, self.part, st["RV"], self.out_all[l])
@@ -283,8 +282,8 @@ class Model:
             ob.oscar_merge(self.L, self.part_full, None, self.out_full[l])
 
     def launches_per_step(self) -> int:
-        # rotate_q, decode attention (INT2 history + BF16 window), merge per layer (+ the demotion)
-        return self.w.layers * (3 + (1 if self.demote else 0))
+        # decode attention (rotation + INT2 history + BF16 window), merge per layer (+ the demotion)
+        return self.w.layers * (2 + (1 if self.demote else 0))
 
 
 def capture(fn, steps: int = 1):
@@ -458,8 +457,9 @@ def main():
     durs = [evs[k][l][0].elapsed_time(evs[k][l][1]) / 1e3 for k in range(KR) for l in range(w.layers)]
     dur = statistics.mean(durs)
     peaks = measured_peaks()
-    # one decode-attention launch: INT2 history + BF16 window + q (bf16) + q_rot (fp32)
-    unit_bytes = bts["int2_per_layer"] + bts["bf16_per_layer"] + w.batch * w.n_q_heads * w.head_dim * (2 + 4)
+    # one decode-attention launch: INT2 history + BF16 window + q (bf16) + R_K (fp32, one per kv head)
+    unit_bytes = (bts["int2_per_layer"] + bts["bf16_per_layer"] + w.batch * w.n_q_heads * w.head_dim * 2
+                  + w.n_kv_heads * w.head_dim * w.head_dim * 4)
     achieved = unit_bytes / dur / 1e9
     traffic = stored_traffic("decode_attention", w.name)
 
@@ -516,7 +516,7 @@ def main():
             "bytes_per_step": bts["per_step"],
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                         "kernel": "oscar_decode_attention (INT2 history split-K + BF16 window, one layer, one launch)",
+                         "kernel": "oscar_decode_attention_fused (q.R_K + INT2 history split-K + BF16 window, one layer, one launch)",
                          "bytes_per_launch": unit_bytes, "launch_us": dur * 1e6,
                          "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs copy bandwidth)"},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": model.launches_per_step() * args.steps,

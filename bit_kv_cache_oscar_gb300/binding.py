@@ -49,7 +49,7 @@ EXPORTS = [
     "oscar_quantize_rotated", "oscar_rotate_q", "oscar_decode_attention", "oscar_merge",
     "oscar_bf16_decode_attention", "oscar_get_device_status", "oscar_last_error_string", "oscar_version",
     "oscar_decode_attention_noalloc", "oscar_decode_attention_history", "oscar_decode_attention_window",
-    "oscar_set_launch_overlap", "oscar_get_launch_overlap",
+    "oscar_set_launch_overlap", "oscar_get_launch_overlap", "oscar_decode_attention_fused",
 ]
 
 
@@ -99,6 +99,9 @@ def lib():
     L.oscar_last_error_string.restype = ctypes.c_char_p
     L.oscar_version.argtypes = []
     L.oscar_version.restype = ctypes.c_char_p
+    L.oscar_decode_attention_fused.argtypes = [P(LayoutC), vp, vp, P(Bf16PoolC), vp, P(Int2PoolC), vp, i32, vp,
+                                               vp, i32, ctypes.c_float, P(PartialsC), vp]
+    L.oscar_decode_attention_fused.restype = st
     L.oscar_set_launch_overlap.argtypes = [i32]
     L.oscar_set_launch_overlap.restype = st
     L.oscar_get_launch_overlap.argtypes = []
@@ -252,6 +255,17 @@ def oscar_decode_attention(layout: Layout, q: torch.Tensor, q_rot: torch.Tensor,
                            stream=None):
     _check("oscar_decode_attention", lib().oscar_decode_attention(
         ctypes.byref(layout.c()), _ptr(q), _ptr(q_rot), ctypes.byref(bf16_pool.c()), _ptr(bf16_page_table),
+        ctypes.byref(int2_pool.c()), _ptr(int2_page_table), int(int2_page_table.shape[-1]), _ptr(seq_len),
+        _ptr(hist_end), int(q.shape[0]), float(sm_scale), ctypes.byref(partials.c()), _stream(stream)))
+
+
+def oscar_decode_attention_fused(layout: Layout, q: torch.Tensor, R_K: torch.Tensor, bf16_pool: Bf16Pool,
+                                 bf16_page_table: torch.Tensor, int2_pool: Int2Pool, int2_page_table: torch.Tensor,
+                                 seq_len: torch.Tensor, hist_end: torch.Tensor, sm_scale: float, partials: Partials,
+                                 stream=None):
+    """oscar_decode_attention with q . R_K computed inside the launch (same partials bits)."""
+    _check("oscar_decode_attention_fused", lib().oscar_decode_attention_fused(
+        ctypes.byref(layout.c()), _ptr(q), _ptr(R_K), ctypes.byref(bf16_pool.c()), _ptr(bf16_page_table),
         ctypes.byref(int2_pool.c()), _ptr(int2_page_table), int(int2_page_table.shape[-1]), _ptr(seq_len),
         _ptr(hist_end), int(q.shape[0]), float(sm_scale), ctypes.byref(partials.c()), _stream(stream)))
 

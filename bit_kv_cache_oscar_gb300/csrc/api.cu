@@ -216,7 +216,7 @@ oscar_status_t oscar_decode_attention(const oscar_layout_t *layout, const uint16
     int32_t *st = status_ptr();
     cudaStream_t s = (cudaStream_t)stream;
     if (oscar::int2_mma_supported(*layout))   // history splits and window in one launch
-        return cuda_status(oscar::launch_decode_mma(*layout, q_rot, int2_view(int2_pool), int2_page_table, q,
+        return cuda_status(oscar::launch_decode_mma(*layout, q_rot, nullptr, int2_view(int2_pool), int2_page_table, q,
                                                     bf16_view(bf16_pool), bf16_page_table, max_pages_per_req,
                                                     seq_len, hist_end, batch, sm_scale, part_view(partials), st,
                                                     true, true, s),
@@ -228,6 +228,32 @@ oscar_status_t oscar_decode_attention(const oscar_layout_t *layout, const uint16
     e = oscar::launch_bf16_attention(*layout, q, bf16_view(bf16_pool), bf16_page_table, max_pages_per_req,
                                      seq_len, hist_end, batch, sm_scale, part_view(partials), 0, st, s);
     return cuda_status(e, "BF16 sink/recent attention launch");
+}
+
+oscar_status_t oscar_decode_attention_fused(const oscar_layout_t *layout, const uint16_t *q, const float *R_K,
+                                            const oscar_bf16_pool_t *bf16_pool, const int32_t *bf16_page_table,
+                                            const oscar_int2_pool_t *int2_pool, const int32_t *int2_page_table,
+                                            int32_t max_pages_per_req, const int32_t *seq_len,
+                                            const int32_t *hist_end, int32_t batch, float sm_scale,
+                                            const oscar_partials_t *partials, void *stream) {
+    TRY(check_layout(layout));
+    TRY(check_bf16_pool(bf16_pool));
+    TRY(check_int2_pool(int2_pool));
+    TRY(check_partials(partials));
+    if (batch < 0 || batch > 65535) return fail(OSCAR_ERR_INVALID_ARG, "batch %d outside 0..65535", batch);
+    if (batch == 0) return OSCAR_OK;
+    if (!q || !R_K || !bf16_page_table || !int2_page_table || !seq_len || !hist_end)
+        return fail(OSCAR_ERR_INVALID_ARG, "NULL argument");
+    if (!aligned16(q) || !aligned16(R_K)) return fail(OSCAR_ERR_INVALID_ARG, "q/R_K not 16-byte aligned");
+    if (max_pages_per_req < 1) return fail(OSCAR_ERR_INVALID_ARG, "max_pages_per_req %d < 1", max_pages_per_req);
+    if (!oscar::int2_mma_supported(*layout))
+        return fail(OSCAR_ERR_UNSUPPORTED, "fused rotation needs 1, 2, 4 or 8 kv heads; use oscar_rotate_q + "
+                                           "oscar_decode_attention");
+    return cuda_status(oscar::launch_decode_mma(*layout, nullptr, R_K, int2_view(int2_pool), int2_page_table, q,
+                                                bf16_view(bf16_pool), bf16_page_table, max_pages_per_req, seq_len,
+                                                hist_end, batch, sm_scale, part_view(partials), status_ptr(), true,
+                                                true, (cudaStream_t)stream),
+                       "fused decode attention launch");
 }
 
 oscar_status_t oscar_decode_attention_history(const oscar_layout_t *layout, const float *q_rot,

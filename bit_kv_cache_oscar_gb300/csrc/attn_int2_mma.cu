@@ -114,10 +114,17 @@ struct MmaArgs {
     int res_off;      // byte offset (from the first stage) of the per-CTA result area
     int hist_ctas;    // CTAs [0, hist_ctas) of grid.x take the history; the rest the BF16 window
     int win_off;      // byte offset (from the first stage) of the window CTAs' warp results
-    const uint16_t *q;          // raw bf16 queries (window CTAs)
+    const float *RK;            // non-null: history CTAs rotate q themselves (q_rot unused)
+    int rot_off;                // byte offset (from the aligned base) of the rotated-query rows [Hq][128]
+    int rk_chunk;               // bytes of R_K staged per step in the stage area (16, 32 or 64 KB)
+    const uint16_t *q;          // raw bf16 queries (window CTAs, and the rotation when RK is set)
     Bf16PoolView bpool;         // BF16 sink/recent pool and its page table (window CTAs)
     const int32_t *bpt;
 };
+
+// Per-CTA result area: m [Hq], l [Hq], then acc [Hq][128] from float res_acc(Hq) on, a multiple
+// of 4 floats so that the accumulator rows take 16-byte vector stores for any Hq.
+__host__ __device__ constexpr int res_acc(int Hq) { return (2 * Hq + 3) & ~3; }
 
 // Cluster reduction: every CTA of a cluster holds (m, l, acc) for each query head of its
 // sub-split in shared memory; CTA `rank` combines query heads rank, rank + C, ... over the
@@ -128,7 +135,7 @@ __device__ __forceinline__ void cluster_combine(const MmaArgs &a, const float *r
     const int rank = (int)cluster_ctarank();
     const size_t S1 = (size_t)a.out.S + 1;
     const int mine = (Hq - rank + C - 1) / C;
-    const uint32_t rm = saddr(res), rl = rm + Hq * 4, ra = rm + 2 * Hq * 4;
+    const uint32_t rm = saddr(res), rl = rm + Hq * 4, ra = rm + res_acc(Hq) * 4;
     for (int e = threadIdx.x; e < mine * kHeadDim; e += blockDim.x) {
         const int hq = rank + (e / kHeadDim) * C, d = e % kHeadDim;
         float M = -INFINITY;
@@ -261,7 +268,7 @@ __device__ void window_cta(const MmaArgs &a, float *wsm, float *res, int T, int 
             }
         }
         if (to_res) {
-            res[2 * Hq + hq * kHeadDim + d] = A;
+            res[res_acc(Hq) + hq * kHeadDim + d] = A;
             if (d == 0) {
                 res[hq] = M;
                 res[Hq + hq] = L;
@@ -330,12 +337,42 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
             mbar_init(saddr(&bars[i]), TMA ? 1 : 33);   // TMA: the expect-tx arrival; else 32 cp.async + mask
             mbar_init(saddr(&bars[4 + i]), kCW);
         }
+        if (a.RK) {
+            mbar_init(saddr(smem + 96), 1);        // R_K chunk landed (expect-tx)
+            mbar_init(saddr(smem + 104), kCW);     // R_K chunk consumed by every consumer warp
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
 
     // ------------------------------------------------------------ producer --
     if (warp == kCW) {
+        if (a.RK) {
+            // Stage R_K of the kv heads this CTA rotates (rank, rank + C, ...) in the stage area,
+            // a chunk at a time, before any KV copy lands there.  R_K is fixed: no wait needed.
+            const int C = a.csize, rank = C > 1 ? (int)cluster_ctarank() : 0;
+            const uint32_t rk_full = saddr(smem + 96), rk_free = saddr(smem + 104);
+            const int nch = kHeadDim * kHeadDim * 4 / a.rk_chunk;
+            int n = 0;
+            bool ok_rk = true;
+            for (int hk = rank; hk < Hkv && ok_rk; hk += C)
+                for (int c = 0; c < nch; ++c, ++n) {
+                    if (n > 0 && !mbar_wait(rk_free, (n - 1) & 1)) {
+                        if (lane == 0) flag_status(a.status, OSCAR_DEV_WAIT_TIMEOUT);
+                        ok_rk = false;
+                        break;
+                    }
+                    if (lane == 0) {
+                        mbar_arrive_expect_tx(rk_full, a.rk_chunk);
+                        tma_load_1d(saddr(stage0), reinterpret_cast<const uint8_t *>(a.RK + (size_t)hk * kHeadDim * kHeadDim) +
+                                                       (size_t)c * a.rk_chunk, a.rk_chunk, rk_full);
+                    }
+                    __syncwarp();
+                }
+            if (ok_rk && n > 0 && !mbar_wait(rk_free, (n - 1) & 1) && lane == 0)
+                flag_status(a.status, OSCAR_DEV_WAIT_TIMEOUT);
+            if (C > 1) cluster_sync_all();         // phase 0: the cluster's rotated queries are in place
+        }
         const int lgH = Hkv == 1 ? 0 : Hkv == 2 ? 1 : Hkv == 4 ? 2 : 3;
         // Page ids of 32 consecutive logical pages, lane i holding page pg_base + i: one load
         // serves 32 pages (128 tiles at 64-token pages), so the copies never wait on the table.
@@ -448,6 +485,61 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
     pdl_wait();
     const int h = warp % Hkv, sub = warp / Hkv, nsub = kCW / Hkv;
     const int gid = lane >> 2, t = lane & 3;
+    const int C = a.csize, rank = C > 1 ? (int)cluster_ctarank() : 0;
+    float *qrot_s = reinterpret_cast<float *>(smem + a.rot_off);     // [Hq][128] rotated queries of the request
+    if (a.RK) {
+        // q_rot = q . R_K for kv heads rank, rank + C, ...: thread (g0, j) runs the fp32 chain
+        // acc = fma(q[g][i], R_K[i][j], acc), i ascending, for heads g0, g0 + 2, ... (the same
+        // operations, in the same order, as oscar_rotate_q).
+        const uint32_t rk_full = saddr(smem + 96), rk_free = saddr(smem + 104);
+        float *qs = reinterpret_cast<float *>(smem + 128);           // [G][128] (P-buffer area, free until the loop)
+        const int ctid = threadIdx.x, j = ctid & (kHeadDim - 1), g0 = ctid >> 7;
+        const int rpc = a.rk_chunk / (kHeadDim * 4), nch = kHeadDim / rpc;
+        constexpr int NG = (G + 1) / 2;
+        int n = 0;
+        for (int hk = rank; hk < Hkv; hk += C) {
+            consumer_sync();
+            for (int e = ctid; e < G * kHeadDim; e += kCW * 32)
+                qs[e] = bf16_to_f32(a.q[((size_t)b * Hq + hk * G) * kHeadDim + e]);
+            consumer_sync();
+            float racc[NG];
+#pragma unroll
+            for (int k = 0; k < NG; ++k) racc[k] = 0.f;
+            for (int c = 0; c < nch; ++c, ++n) {
+                if (!mbar_wait(rk_full, n & 1) && lane == 0) flag_status(a.status, OSCAR_DEV_WAIT_TIMEOUT);
+                const float *R = reinterpret_cast<const float *>(stage0);
+#pragma unroll 8
+                for (int i = 0; i < rpc; ++i) {
+                    const float rv = R[i * kHeadDim + j];
+#pragma unroll
+                    for (int k = 0; k < NG; ++k) {
+                        const int g = g0 + 2 * k;
+                        if (g < G) racc[k] = __fmaf_rn(qs[g * kHeadDim + c * rpc + i], rv, racc[k]);
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(rk_free);
+            }
+            // every CTA of the cluster gets the rows: stores to the peers need no round trip
+#pragma unroll
+            for (int k = 0; k < NG; ++k) {
+                const int g = g0 + 2 * k;
+                if (g < G) {
+                    float *dst = qrot_s + (hk * G + g) * kHeadDim + j;
+                    if (C == 1) {
+                        *dst = racc[k];
+                    } else {
+                        for (int q = 0; q < C; ++q) st_dsmem_f32(saddr(dst), (uint32_t)q, racc[k]);
+                    }
+                }
+            }
+        }
+        if (C > 1) cluster_sync_all(); else consumer_sync();
+    }
+    // rotated query element (hq, d): the previous kernel's q_rot, or this CTA's copy of the rows
+    auto qrot = [&](int hq, int d) -> float {
+        return a.RK ? qrot_s[hq * kHeadDim + d] : a.q_rot[((size_t)b * Hq + hq) * kHeadDim + d];
+    };
 
     // B operand of QK: q_rot split into f16 hi/lo, divided by the code factor of its k-row.
     uint32_t bq[NT][8][2];
@@ -456,7 +548,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
     for (int nt = 0; nt < NT; ++nt) {
         const int hh = nt * 4 + (gid >> 1), part = gid & 1;
         const bool valid = hh < G;
-        const float *qr = a.q_rot + ((size_t)b * Hq + h * G + (valid ? hh : 0)) * kHeadDim;
+        const int hq = h * G + (valid ? hh : 0);
 #pragma unroll
         for (int kap = 0; kap < 2; ++kap)
 #pragma unroll
@@ -465,8 +557,8 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
                 for (int e = 0; e < 2; ++e) {
                     const int rr = 2 * sg + e, W = 2 * t + kap;
                     const float inv = 1.0f / qk_factor(rr);
-                    const float v0 = valid ? qr[16 * W + rr] * inv : 0.f;
-                    const float v1 = valid ? qr[16 * W + 8 + rr] * inv : 0.f;
+                    const float v0 = valid ? qrot(hq, 16 * W + rr) * inv : 0.f;
+                    const float v1 = valid ? qrot(hq, 16 * W + 8 + rr) * inv : 0.f;
                     bq[nt][kap * 4 + sg][e] = pack2(split_part(v0, part), split_part(v1, part));
                 }
     }
@@ -476,8 +568,8 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
 #pragma unroll
         for (int jg = 0; jg < NGRP; ++jg) qz[nt][jg] = 0.f;
     for (int hh = 0; hh < G; ++hh) {
-        const float4 v = reinterpret_cast<const float4 *>(a.q_rot + ((size_t)b * Hq + h * G + hh) * kHeadDim)[lane];
-        const float sum4 = (v.x + v.y) + (v.z + v.w);
+        const int hq = h * G + hh;
+        const float sum4 = (qrot(hq, 4 * lane) + qrot(hq, 4 * lane + 1)) + (qrot(hq, 4 * lane + 2) + qrot(hq, 4 * lane + 3));
         const int lg = (4 * lane) * NGRP / kHeadDim;
 #pragma unroll
         for (int jg = 0; jg < NGRP; ++jg) {
@@ -770,7 +862,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
             if (hh < G) {
                 const int hq = h * G + hh;
                 const size_t row = ((size_t)b * Hq + hq) * S1 + s;
-                float4 *dst = reinterpret_cast<float4 *>(to_res ? res + 2 * Hq + hq * kHeadDim + 16 * gid
+                float4 *dst = reinterpret_cast<float4 *>(to_res ? res + res_acc(Hq) + hq * kHeadDim + 16 * gid
                                                                 : a.out.acc + row * kHeadDim + 16 * gid);
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4)
@@ -823,7 +915,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
             }
             const int hq = h * G + hh;
             const size_t row = ((size_t)b * Hq + hq) * S1 + s;
-            *reinterpret_cast<float4 *>(to_res ? res + 2 * Hq + hq * kHeadDim + c4 : a.out.acc + row * kHeadDim + c4) =
+            *reinterpret_cast<float4 *>(to_res ? res + res_acc(Hq) + hq * kHeadDim + c4 : a.out.acc + row * kHeadDim + c4) =
                 make_float4(A0, A1, A2, A3);
             if (c4 == 0) {
                 (to_res ? res + hq : a.out.m + row)[0] = M;
@@ -891,15 +983,19 @@ int mma_smem_plan(const oscar_layout_t &L, MmaArgs &a) {
     a.ws_bytes = NGRP * 8 * NT * kWsWords * 4;
     a.stage_off = (128 + kCW * a.ws_bytes + 1023) & ~1023;   // stages start 1024-byte aligned
     const int budget = (G == 8 ? 200 : 110) * 1024;    // two CTAs per SM below G = 8
+    const int rot_bytes = Hq * kHeadDim * 4;            // rotated queries (fused rotation)
     int stages = kMaxStages;
-    while (stages > 2 && a.stage_off + stages * a.stage_bytes > budget) --stages;
+    while (stages > 2 && a.stage_off + stages * a.stage_bytes + rot_bytes > budget) --stages;
     a.stages = stages;
     const int combine = (kCW / Hkv > 1) ? kCW * NT * 4 * (2 + kHeadDim) * 4 : 0;
     a.res_off = combine;
-    a.win_off = a.res_off + Hq * (2 + kHeadDim) * 4;
+    a.win_off = a.res_off + (res_acc(Hq) + Hq * kHeadDim) * 4;
     const int tail = a.win_off + kCW * G * (2 + kHeadDim) * 4;
+    const int area = stages * a.stage_bytes;             // R_K is staged here a chunk at a time
+    a.rk_chunk = area >= 65536 ? 65536 : area >= 32768 ? 32768 : 16384;
+    a.rot_off = a.stage_off + (area > tail ? area : tail);
     // + 1024: the kernel rounds the dynamic shared memory base up to a 1024-byte boundary
-    return 1024 + a.stage_off + (stages * a.stage_bytes > tail ? stages * a.stage_bytes : tail);
+    return 1024 + a.rot_off + rot_bytes;
 }
 
 template <int G, int NGRP>
@@ -947,6 +1043,12 @@ bool codes_tensor_map(CUtensorMap *tm, const uint8_t *base, long long rows) {
 template <int G, int NGRP>
 cudaError_t launch_mma(const oscar_layout_t &L, MmaArgs a, int batch, bool history, bool window, cudaStream_t st) {
     const int smem = mma_smem_plan<G, NGRP>(L, a);
+    // the carve-up's invariants: vector and bulk-copy targets 16-byte aligned, tensor-map boxes
+    // 1024-byte aligned, R_K chunks inside the stage area
+    if (((a.stage_off | a.stage_bytes | a.off_v | a.off_s | a.arr_bytes | a.res_off | a.win_off | a.rot_off) & 15) ||
+        (a.stage_off & 1023) || (a.stage_bytes & 1023 && L.n_kv_heads == 8) ||
+        (a.RK && a.stages * a.stage_bytes < a.rk_chunk))
+        return cudaErrorInvalidValue;
     const bool tma = L.n_kv_heads == 8;
     auto kern = tma ? int2_mma_kernel<G, NGRP, true> : int2_mma_kernel<G, NGRP, false>;
     CUtensorMap tmk, tmv;
@@ -999,12 +1101,14 @@ bool int2_mma_supported(const oscar_layout_t &L) {
     return (H == 1 || H == 2 || H == 4 || H == 8) && L.head_dim == kHeadDim;
 }
 
-cudaError_t launch_decode_mma(const oscar_layout_t &L, const float *q_rot, Int2PoolView pool, const int32_t *pt,
-                              const uint16_t *q, Bf16PoolView bpool, const int32_t *bpt, int max_pages,
-                              const int32_t *seq_len, const int32_t *hist_end, int batch, float sm_scale,
-                              PartialsView out, int32_t *status, bool history, bool window, cudaStream_t st) {
+cudaError_t launch_decode_mma(const oscar_layout_t &L, const float *q_rot, const float *RK, Int2PoolView pool,
+                              const int32_t *pt, const uint16_t *q, Bf16PoolView bpool, const int32_t *bpt,
+                              int max_pages, const int32_t *seq_len, const int32_t *hist_end, int batch,
+                              float sm_scale, PartialsView out, int32_t *status, bool history, bool window,
+                              cudaStream_t st) {
     if (batch <= 0 || (!history && !window)) return cudaSuccess;
     MmaArgs a{};
+    a.RK = RK;
     a.q = q;
     a.bpool = bpool;
     a.bpt = bpt;

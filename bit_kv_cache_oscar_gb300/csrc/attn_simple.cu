@@ -252,8 +252,8 @@ cudaError_t launch_int2_attention(const oscar_layout_t &L, const float *q_rot, I
                                   int32_t *status, cudaStream_t st) {
     if (batch <= 0) return cudaSuccess;
     if (int2_mma_supported(L))
-        return launch_decode_mma(L, q_rot, pool, pt, nullptr, Bf16PoolView{nullptr, nullptr, 0}, nullptr, max_pages,
-                                 seq_len, hist_end, batch, sm_scale, out, status, true, false, st);
+        return launch_decode_mma(L, q_rot, nullptr, pool, pt, nullptr, Bf16PoolView{nullptr, nullptr, 0}, nullptr,
+                                 max_pages, seq_len, hist_end, batch, sm_scale, out, status, true, false, st);
     Int2Args a{q_rot, pool, pt, max_pages, L.page_size, L.n_kv_heads, L.group, L.sink, seq_len, hist_end,
                sm_scale * kLog2e, out, status};
     return launch_g<Int2Launcher>(L.gqa, dim3(out.S, L.n_kv_heads, batch), a, st);
@@ -265,8 +265,8 @@ cudaError_t launch_bf16_attention(const oscar_layout_t &L, const uint16_t *q, Bf
                                   int mode, int32_t *status, cudaStream_t st) {
     if (batch <= 0) return cudaSuccess;
     if (mode == 0 && int2_mma_supported(L))   // the window CTAs of the tensor-core INT2 kernel
-        return launch_decode_mma(L, nullptr, Int2PoolView{}, nullptr, q, pool, pt, max_pages, seq_len, hist_end,
-                                 batch, sm_scale, out, status, false, true, st);
+        return launch_decode_mma(L, nullptr, nullptr, Int2PoolView{}, nullptr, q, pool, pt, max_pages, seq_len,
+                                 hist_end, batch, sm_scale, out, status, false, true, st);
     if (bf16_mma_supported(L, mode))
         return launch_bf16_attention_mma(L, q, pool, pt, max_pages, seq_len, hist_end, batch, sm_scale, out, mode,
                                          status, st);

@@ -63,7 +63,6 @@ __global__ void __launch_bounds__(128) merge_kernel(PartialsView p, const float 
     float *red = ls + (S + 1);
     const size_t row0 = ((size_t)b * n_q_heads + hq) * (S + 1);
 
-    pdl_trigger();
     if (RV) {
         // rows 32 z .. 32 z + 31 of this head's R_V (32 rows x 32 float4)
         const float4 *R = reinterpret_cast<const float4 *>(RV + ((size_t)(hq / gqa) * kHeadDim + z * kQuarter) * kHeadDim);
@@ -135,6 +134,9 @@ __global__ void __launch_bounds__(128) merge_kernel(PartialsView p, const float 
         L = __fmaf_rn(ls[S], w, L);
         Ar = __fmaf_rn(xS, w, Ar);
     }
+    // The next kernel may launch only now: launched earlier, its CTAs take SM slots while this
+    // grid still holds some, and the next attention kernel's clusters end up placed worse.
+    pdl_trigger();
     const float o = L > 0.0f ? __fdiv_rn(Ar, L) : 0.0f;
     const size_t orow = (size_t)b * n_q_heads + hq;
     if (out) out[orow * kHeadDim + c] = f32_to_bf16_rn(o);

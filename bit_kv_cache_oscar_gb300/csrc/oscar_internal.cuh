@@ -128,11 +128,13 @@ bool int2_mma_supported(const oscar_layout_t &L);
 // visible); *active (optional) gets how many such clusters are resident at once (0 if unknown).
 int int2_mma_cluster_size(const oscar_layout_t &L, int *active = nullptr);
 // The tensor-core INT2 history splits (history) and/or the BF16 sink/recent window
-// (window) in one launch; the window CTAs write partial slot S.
-cudaError_t launch_decode_mma(const oscar_layout_t &L, const float *q_rot, Int2PoolView pool, const int32_t *pt,
-                              const uint16_t *q, Bf16PoolView bpool, const int32_t *bpt, int max_pages,
-                              const int32_t *seq_len, const int32_t *hist_end, int batch, float sm_scale,
-                              PartialsView out, int32_t *status, bool history, bool window, cudaStream_t st);
+// (window) in one launch; the window CTAs write partial slot S.  With RK non-null the history
+// CTAs compute q_rot = q . R_K themselves (q_rot is not read).
+cudaError_t launch_decode_mma(const oscar_layout_t &L, const float *q_rot, const float *RK, Int2PoolView pool,
+                              const int32_t *pt, const uint16_t *q, Bf16PoolView bpool, const int32_t *bpt,
+                              int max_pages, const int32_t *seq_len, const int32_t *hist_end, int batch,
+                              float sm_scale, PartialsView out, int32_t *status, bool history, bool window,
+                              cudaStream_t st);
 
 // Tensor-core BF16 kernel (mode 0 any n_kv_heads; mode 1 n_kv_heads in {1, 2, 4, 8}).
 bool bf16_mma_supported(const oscar_layout_t &L, int mode);

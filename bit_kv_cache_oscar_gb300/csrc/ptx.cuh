@@ -124,4 +124,12 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t local_saddr, uint32_t ran
     return v;
 }
 
+// Store a float to the shared memory of CTA `rank` of this cluster, at the offset that
+// local_saddr has in this CTA's shared memory (visible to it after a cluster barrier).
+__device__ __forceinline__ void st_dsmem_f32(uint32_t local_saddr, uint32_t rank, float v) {
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(local_saddr), "r"(rank));
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(ra), "f"(v) : "memory");
+}
+
 }  // namespace oscar

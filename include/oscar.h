@@ -228,6 +228,27 @@ OSCAR_API oscar_status_t oscar_decode_attention(const oscar_layout_t *layout,
                                       float sm_scale, const oscar_partials_t *partials, void *stream);
 
 /*
+ * oscar_decode_attention with the query rotation folded in: takes the unrotated q
+ * and R_K (fp32 [n_kv_heads][head_dim][head_dim], as for oscar_rotate_q) instead
+ * of q_rot.  Each cluster of history CTAs rotates the queries of its request, one
+ * kv head per CTA, from R_K staged in shared memory, and shares the rows across
+ * the cluster; the arithmetic is oscar_rotate_q's (one fused multiply-add per
+ * term, ascending input channel), so the partials are bit for bit those of
+ * oscar_rotate_q followed by oscar_decode_attention.  Requires a layout the
+ * tensor-core kernels take (n_kv_heads 1, 2, 4 or 8); otherwise returns
+ * OSCAR_ERR_UNSUPPORTED and the caller uses the two calls.  No method page
+ * describes this fusion; it removes one launch per layer.
+ */
+OSCAR_API oscar_status_t oscar_decode_attention_fused(const oscar_layout_t *layout, const uint16_t *q,
+                                                      const float *R_K, const oscar_bf16_pool_t *bf16_pool,
+                                                      const int32_t *bf16_page_table,
+                                                      const oscar_int2_pool_t *int2_pool,
+                                                      const int32_t *int2_page_table, int32_t max_pages_per_req,
+                                                      const int32_t *seq_len, const int32_t *hist_end,
+                                                      int32_t batch, float sm_scale,
+                                                      const oscar_partials_t *partials, void *stream);
+
+/*
  * The two halves of oscar_decode_attention, for callers that run them on two
  * streams so that they overlap (they write disjoint slots of `partials`):
  * _history writes the history slots 0..S-1 from the INT2 pool and q_rot;
@@ -312,7 +333,8 @@ OSCAR_API oscar_status_t oscar_decode_attention_noalloc(
  * No method page describes it: it is a launch policy of this library.
  *
  * When on, oscar_rotate_q, oscar_decode_attention_history (tensor-core path),
- * oscar_decode_attention and oscar_merge launch their kernels so that each may
+ * oscar_decode_attention, oscar_decode_attention_fused and oscar_merge launch
+ * their kernels so that each may
  * start while the kernel before it in the same stream is still running.  Before
  * it waits for that kernel, a kernel only reads what a decode step treats as
  * fixed: R_K / R_V, the INT2 and BF16 pools, the page tables, seq_len and

@@ -1,8 +1,8 @@
 """Parity at the workloads' full sizes, on sampled (request, query head) outputs.
 
-Each case runs the decode step exactly as bench.py does (oscar_rotate_q ->
-oscar_decode_attention -> oscar_merge on one stream, launch overlap on, the
-library's split suggestion for the batch), then compares sampled heads with the
+Each case runs the decode step exactly as bench.py does (oscar_decode_attention_fused
+-> oscar_merge on one stream, launch overlap on, the library's split suggestion for
+the batch), then compares sampled heads with the
 oracle's fp64 attention over its own demotion of those heads' history.  Samples
 always include the shortest and the longest request.  K/V are drawn on the GPU
 (the oracle reads back the sampled heads), so the same tensors feed both sides.
@@ -25,15 +25,13 @@ def _run_like_bench(case):
     B = len(case.seq)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     S = ob.oscar_suggest_splits(L, B, int(max(case.hist_end)) - L.sink, sms)
-    q_rot = torch.empty((B, L.n_q_heads, D), dtype=torch.float32, device="cuda")
     part = ob.Partials.empty(L, B, S)
     out32 = torch.empty((B, L.n_q_heads, D), dtype=torch.float32, device="cuda")
     out = torch.empty((B, L.n_q_heads, D), dtype=torch.bfloat16, device="cuda")
     try:
         ob.oscar_set_launch_overlap(True)
-        ob.oscar_rotate_q(L, dev["q"], dev["RK"], q_rot)
-        ob.oscar_decode_attention(L, dev["q"], q_rot, dev["bf16"], dev["bf16_table"], dev["int2"],
-                                  dev["int2_table"], dev["seq_len"], dev["hist_end"], case.sm_scale, part)
+        ob.oscar_decode_attention_fused(L, dev["q"], dev["RK"], dev["bf16"], dev["bf16_table"], dev["int2"],
+                                        dev["int2_table"], dev["seq_len"], dev["hist_end"], case.sm_scale, part)
         ob.oscar_merge(L, part, dev["RV"], out, out32, None)
         torch.cuda.synchronize()
     finally:

@@ -276,6 +276,42 @@ def test_launch_overlap_gives_identical_bits():
     assert ob.oscar_get_device_status() == 0
 
 
+@pytest.mark.parametrize("n_kv,gqa,ps,group,seq,S", [
+    (8, 4, 64, 128, (3000, 1700), 6),     # the benchmark's shape, clusters of 8: one kv head per CTA
+    (8, 8, 64, 32, (2500,), 5),            # GQA 8, group 32
+    (4, 2, 32, 64, (1800, 900), 4),
+    (2, 4, 16, 128, (1200,), 3),            # more CTAs per cluster than kv heads
+    (1, 8, 16, 128, (900,), 2),             # R_K staged in 16 KB chunks
+    (1, 1, 16, 32, (700,), 2),
+])
+def test_fused_rotation_matches_rotate_then_decode(n_kv, gqa, ps, group, seq, S):
+    """oscar_decode_attention_fused writes the partials of oscar_rotate_q + oscar_decode_attention,
+    bit for bit."""
+    case = sc.make_case(n_kv=n_kv, gqa=gqa, page_size=ps, group=group, seq=seq)
+    sc.upload(case)
+    L, dev = case.layout, case.dev
+    _, _, _, ref = sc.run_decode(case, S)
+    part = ob.Partials.empty(L, len(seq), S)
+    part.m.fill_(float("nan"))
+    part.l.fill_(float("nan"))
+    part.acc.fill_(float("nan"))
+    ob.oscar_decode_attention_fused(L, dev["q"], dev["RK"], dev["bf16"], dev["bf16_table"], dev["int2"],
+                                    dev["int2_table"], dev["seq_len"], dev["hist_end"], case.sm_scale, part)
+    torch.cuda.synchronize()
+    assert torch.equal(part.m, ref.m) and torch.equal(part.l, ref.l) and torch.equal(part.acc, ref.acc)
+    assert ob.oscar_get_device_status() == 0
+
+
+def test_fused_rotation_rejects_other_head_counts():
+    case = sc.make_case(n_kv=3, gqa=2, page_size=16, seq=(400,))
+    sc.upload(case)
+    L, dev = case.layout, case.dev
+    part = ob.Partials.empty(L, 1, 2)
+    with pytest.raises(ob.OscarError, match="kv heads"):
+        ob.oscar_decode_attention_fused(L, dev["q"], dev["RK"], dev["bf16"], dev["bf16_table"], dev["int2"],
+                                        dev["int2_table"], dev["seq_len"], dev["hist_end"], case.sm_scale, part)
+
+
 def test_bf16_full_cache_parity():
     """The all-BF16 comparison kernel: oracle with no history region (sink = h_end = 0)."""
     case = sc.make_case(n_kv=2, gqa=4, page_size=16, seq=(1024, 555))
