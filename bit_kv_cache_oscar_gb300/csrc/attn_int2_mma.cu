@@ -286,6 +286,10 @@ __device__ void window_cta(const MmaArgs &a, float *wsm, float *res, int T, int 
 }
 
 constexpr float kLazy = 8.0f;   // log2 headroom before the running maximum is raised
+// rotated-query rows in shared memory: element d of a row at d + d / 32 (row stride 132), so
+// that the operand reads of a warp (4 heads x 4 column groups) fall in distinct banks
+constexpr int kQS = kHeadDim + kHeadDim / 32;
+__device__ __forceinline__ int qs_col(int d) { return d + (d >> 5); }
 constexpr int kWsWords = 20;    // words per P-operand column: 2 tiles x 8 + 4 (bank spread)
 
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -320,7 +324,11 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
 
     const int s = blockIdx.x, b = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int Hkv = a.n_kv, Hq = Hkv * G, S = a.out.S;
+    // With 8 kv heads (the tensor-map path) the stage layout is compile-time: addresses fold.
+    const int Hkv = TMA ? 8 : a.n_kv, Hq = Hkv * G, S = a.out.S;
+    const int off_v = TMA ? 8 * 2048 : a.off_v, off_s = TMA ? 2 * 8 * 2048 : a.off_s;
+    const int arr_bytes = TMA ? kStageTok * 8 * NGRP * 2 : a.arr_bytes;
+    const int stage_bytes = TMA ? ((2 * 8 * 2048 + 4 * kStageTok * 8 * NGRP * 2 + 127) & ~127) : a.stage_bytes;
     int T, he;
     read_lengths(a.seq_len, a.hist_end, b, a.sink, a.max_pages * a.page_size, a.status, T, he);
     if (s >= a.hist_ctas) {                    // a BF16 window CTA (uniform over the cluster)
@@ -389,7 +397,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
                 ok = false;
                 break;
             }
-            uint8_t *sb = stage0 + st * a.stage_bytes;
+            uint8_t *sb = stage0 + st * stage_bytes;
             int mask = 0;
             if constexpr (TMA) {
                 // lane = 8 j + op: op 0..3 the code boxes (K lo/hi heads, V lo/hi), 4..7 scale/zero rows
@@ -420,13 +428,13 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
                 if ((mask >> jl) & 1) {
                     const uint32_t d = saddr(sb) + jl * 4096;
                     if (op < 4) {
-                        tma_load_2d(d + (op >> 1) * a.off_v + (op & 1) * 2048, (op >> 1) ? &tmv : &tmk, (op & 1) * 128,
+                        tma_load_2d(d + (op >> 1) * off_v + (op & 1) * 2048, (op >> 1) ? &tmv : &tmk, (op & 1) * 128,
                                     row0, full);
                     } else {
                         const int arr = op - 4, nsb = kTileTokens * 8 * NGRP * 2;   // bytes of one tile's rows
                         const uint16_t *src = arr == 0 ? a.pool.scale_k : arr == 1 ? a.pool.zero_k
                                             : arr == 2 ? a.pool.scale_v : a.pool.zero_v;
-                        tma_load_1d(saddr(sb + a.off_s) + arr * a.arr_bytes + jl * nsb, src + (size_t)row0 * 8 * NGRP,
+                        tma_load_1d(saddr(sb + off_s) + arr * arr_bytes + jl * nsb, src + (size_t)row0 * 8 * NGRP,
                                     nsb, full);
                     }
                 }
@@ -456,17 +464,17 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
                     const int slot = c >> (lgH + 1), head = (c >> 1) & (Hkv - 1), half = c & 1;
                     const uint32_t dst = tile_dst + head * 2048 + slot * 32 + half * 16;
                     cp_async16(dst, srck + c * 16);
-                    cp_async16(dst + a.off_v, srcv + c * 16);
+                    cp_async16(dst + off_v, srcv + c * 16);
                 }
                 const int nsc = (2 * NGRP) << lgH;      // 16-byte chunks of one scale/zero array
                 const size_t soff = row0 * Hkv * NGRP;
-                const uint32_t sdst = saddr(sb + a.off_s) + j * nsc * 16;
+                const uint32_t sdst = saddr(sb + off_s) + j * nsc * 16;
                 for (int c = lane; c < nsc; c += 32) {
                     cp_async16(sdst + c * 16, reinterpret_cast<const uint8_t *>(a.pool.scale_k + soff) + c * 16);
-                    cp_async16(sdst + a.arr_bytes + c * 16, reinterpret_cast<const uint8_t *>(a.pool.zero_k + soff) + c * 16);
-                    cp_async16(sdst + 2 * a.arr_bytes + c * 16,
+                    cp_async16(sdst + arr_bytes + c * 16, reinterpret_cast<const uint8_t *>(a.pool.zero_k + soff) + c * 16);
+                    cp_async16(sdst + 2 * arr_bytes + c * 16,
                                reinterpret_cast<const uint8_t *>(a.pool.scale_v + soff) + c * 16);
-                    cp_async16(sdst + 3 * a.arr_bytes + c * 16,
+                    cp_async16(sdst + 3 * arr_bytes + c * 16,
                                reinterpret_cast<const uint8_t *>(a.pool.zero_v + soff) + c * 16);
                 }
             }
@@ -486,7 +494,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
     const int h = warp % Hkv, sub = warp / Hkv, nsub = kCW / Hkv;
     const int gid = lane >> 2, t = lane & 3;
     const int C = a.csize, rank = C > 1 ? (int)cluster_ctarank() : 0;
-    float *qrot_s = reinterpret_cast<float *>(smem + a.rot_off);     // [Hq][128] rotated queries of the request
+    float *qrot_s = reinterpret_cast<float *>(smem + a.rot_off);     // [Hq][kQS] rotated queries of the request
     if (a.RK) {
         // q_rot = q . R_K for kv heads rank, rank + C, ...: thread (g0, j) runs the fp32 chain
         // acc = fma(q[g][i], R_K[i][j], acc), i ascending, for heads g0, g0 + 2, ... (the same
@@ -525,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
             for (int k = 0; k < NG; ++k) {
                 const int g = g0 + 2 * k;
                 if (g < G) {
-                    float *dst = qrot_s + (hk * G + g) * kHeadDim + j;
+                    float *dst = qrot_s + (hk * G + g) * kQS + qs_col(j);
                     if (C == 1) {
                         *dst = racc[k];
                     } else {
@@ -538,7 +546,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
     }
     // rotated query element (hq, d): the previous kernel's q_rot, or this CTA's copy of the rows
     auto qrot = [&](int hq, int d) -> float {
-        return a.RK ? qrot_s[hq * kHeadDim + d] : a.q_rot[((size_t)b * Hq + hq) * kHeadDim + d];
+        return a.RK ? qrot_s[hq * kQS + qs_col(d)] : a.q_rot[((size_t)b * Hq + hq) * kHeadDim + d];
     };
 
     // B operand of QK: q_rot split into f16 hi/lo, divided by the code factor of its k-row.
@@ -605,7 +613,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
     };
     const float csc = a.scale2 * kTwo24;
     const int rs = Hkv * NGRP;                  // scale/zero elements per token row in a stage
-    const int arr_el = a.arr_bytes / 2;
+    const int arr_el = arr_bytes / 2;
     uint32_t *Ws = reinterpret_cast<uint32_t *>(smem + 128 + warp * a.ws_bytes);   // [NGRP][NCOL][kWsWords]
 
     float m_run[NT], m_true[NT], l_run[NT], zs[NT][NGRP];
@@ -622,13 +630,13 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
             for (int c = 0; c < 4; ++c) oacc[nt][mt][c] = 0.f;
     }
 
-    for (int it = 0; it < n_iters; ++it) {
-        const int st = it % a.stages;
-        if (!mbar_wait(saddr(&bars[st]), (it / a.stages) & 1)) {
+    int st = 0, ph = 0;                          // stage and its phase parity, stepped (no division)
+    for (int it = 0; it < n_iters; ++it, st = (st + 1 == a.stages) ? 0 : st + 1, ph ^= (st == 0)) {
+        if (!mbar_wait(saddr(&bars[st]), ph)) {
             if (lane == 0) flag_status(a.status, OSCAR_DEV_WAIT_TIMEOUT);
             break;
         }
-        const uint8_t *sb = stage0 + st * a.stage_bytes;
+        const uint8_t *sb = stage0 + st * stage_bytes;
         const int mask = masks[st];
         // this warp's tiles of the stage: sub, sub + nsub, ...; taken two at a time (32 tokens)
         for (int ja = sub; ja < kTilesPerStage; ja += 2 * nsub) {
@@ -694,7 +702,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
                 float tv[2][2];
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
-                    const uint16_t *sk = reinterpret_cast<const uint16_t *>(sb + a.off_s) +
+                    const uint16_t *sk = reinterpret_cast<const uint16_t *>(sb + off_s) +
                                          jt[u] * kTileTokens * rs + h * NGRP;
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
@@ -736,7 +744,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
                     const int c_hi = nt * 8 + 2 * t;
 #pragma unroll
                     for (int u = 0; u < 2; ++u) {
-                        const uint16_t *sk = reinterpret_cast<const uint16_t *>(sb + a.off_s) +
+                        const uint16_t *sk = reinterpret_cast<const uint16_t *>(sb + off_s) +
                                              jt[u] * kTileTokens * rs + h * NGRP;
                         float w[2];
 #pragma unroll
@@ -775,7 +783,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
             const int gv = gid * NGRP / 8;
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
-                const uint8_t *Vc = tile_base(sb + a.off_v, jt[u]);
+                const uint8_t *Vc = tile_base(sb + off_v, jt[u]);
                 // k-columns 2t, 2t+1 <- tokens t, t+8; 2t+8, 2t+9 <- tokens t+4, t+12
                 const uint32_t X = *reinterpret_cast<const uint32_t *>(Vc + vofs[0]);
                 const uint32_t Y = *reinterpret_cast<const uint32_t *>(Vc + vofs[1]);
@@ -983,7 +991,7 @@ int mma_smem_plan(const oscar_layout_t &L, MmaArgs &a) {
     a.ws_bytes = NGRP * 8 * NT * kWsWords * 4;
     a.stage_off = (128 + kCW * a.ws_bytes + 1023) & ~1023;   // stages start 1024-byte aligned
     const int budget = (G == 8 ? 200 : 110) * 1024;    // two CTAs per SM below G = 8
-    const int rot_bytes = Hq * kHeadDim * 4;            // rotated queries (fused rotation)
+    const int rot_bytes = Hq * kQS * 4;                 // rotated queries (fused rotation)
     int stages = kMaxStages;
     while (stages > 2 && a.stage_off + stages * a.stage_bytes + rot_bytes > budget) --stages;
     a.stages = stages;
@@ -1050,6 +1058,10 @@ cudaError_t launch_mma(const oscar_layout_t &L, MmaArgs a, int batch, bool histo
         (a.RK && a.stages * a.stage_bytes < a.rk_chunk))
         return cudaErrorInvalidValue;
     const bool tma = L.n_kv_heads == 8;
+    // the tensor-map kernel folds these for 8 kv heads
+    if (tma && (a.off_v != 8 * 2048 || a.off_s != 2 * 8 * 2048 || a.arr_bytes != kStageTok * 8 * NGRP * 2 ||
+                a.stage_bytes != ((2 * 8 * 2048 + 4 * kStageTok * 8 * NGRP * 2 + 127) & ~127)))
+        return cudaErrorInvalidValue;
     auto kern = tma ? int2_mma_kernel<G, NGRP, true> : int2_mma_kernel<G, NGRP, false>;
     CUtensorMap tmk, tmv;
     memset(&tmk, 0, sizeof(tmk));
