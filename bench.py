@@ -147,6 +147,16 @@ class ClockSampler:
                 self.proc.kill()
             self.t.join(timeout=2)
 
+    @staticmethod
+    def max_sm_mhz(index: int):
+        """The GPU's maximum SM clock (MHz) from nvidia-smi, or None."""
+        try:
+            out = subprocess.run(["nvidia-smi", f"--id={index}", "--query-gpu=clocks.max.sm",
+                                  "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=20)
+            return float(out.stdout.strip().splitlines()[0])
+        except (OSError, ValueError, IndexError, subprocess.TimeoutExpired):
+            return None
+
     def summary(self) -> dict:
         sm, mx, reasons = [], 0.0, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
@@ -251,12 +261,13 @@ class Model:
     # One decode step over all layers (the path).  Per layer the BF16 sink/recent half runs on
     # a second stream next to q rotation + the INT2 history half; the merge joins them.
     # Optional events bracket each decode-attention launch.
-    def step(self, events=None, side=None):
+    def step(self, events=None, side=None, demote=None):
         import torch
         from bit_kv_cache_oscar_gb300 import binding as ob
         L, w = self.L, self.w
         cur = torch.cuda.current_stream()
-        if self.demote and side is not None:
+        demote = self.demote if demote is None else demote
+        if demote and side is not None:
             side.wait_stream(cur)
             with torch.cuda.stream(side):
                 for st in self.layers:
@@ -271,8 +282,15 @@ class Model:
             if events is not None:
                 events[l][1].record()
             ob.oscar_merge(L, self.part, st["RV"], self.out_all[l])
-        if self.demote and side is not None:
+        if demote and side is not None:
             cur.wait_stream(side)
+
+    def demote_step(self):
+        """The per-step demotion alone: one token per request, layer and kv head (K and V)."""
+        from bit_kv_cache_oscar_gb300 import binding as ob
+        for st in self.layers:
+            ob.oscar_demote(self.L, st["bf16"], self.bf16_table, st["int2"], self.int2_table, self.dem_req,
+                            self.dem_pos, st["RK"], st["RV"], 0.96, 0.92)
 
     def step_bf16(self):
         from bit_kv_cache_oscar_gb300 import binding as ob
@@ -402,6 +420,44 @@ def run_reference(args, w, rank):
     print(json.dumps(line), flush=True)
 
 
+def bulk_demotion(model, w, args, dist) -> dict:
+    """oscar_demote over one layer's whole history of request 0 ([sink, hist_end), every kv head,
+    K and V) from a BF16 staging pool into a scratch INT2 pool: rows/s and the fp32 FMA roofline
+    (each row-head is two 128x128 fp32 FMA chains; peak = SMs x 128 FP32 lanes x 2 x clock)."""
+    import torch
+    from bit_kv_cache_oscar_gb300 import binding as ob
+    L, dev, ps = model.L, model.dev, w.page_size
+    T = int(model.seq[0])
+    he = int(model.hist_end[0])
+    n_log = (T + ps - 1) // ps
+    prof = syn.channel_profile(w.seed, 0, w.n_kv_heads)
+    k, v = syn.kv_rows(w.seed, 0, 0, 0, T, prof, device=dev)
+    stage = ob.Bf16Pool.empty(L, n_log, dev)
+    stage.k.view(-1, w.n_kv_heads, D)[:T] = k
+    stage.v.view(-1, w.n_kv_heads, D)[:T] = v
+    del k, v
+    table = torch.arange(n_log, dtype=torch.int32, device=dev).view(1, n_log)
+    i2 = ob.Int2Pool.empty(L, n_log, dev)
+    pos = torch.arange(w.sink, he, dtype=torch.int32, device=dev)
+    req = torch.zeros_like(pos)
+    st = model.layers[0]
+    fn = lambda: ob.oscar_demote(L, stage, table, i2, table, req, pos, st["RK"], st["RV"], 0.96, 0.92)
+    g = capture(fn)
+    reps = max(3, min(args.steps, 20))
+    tb = time_graph(g, reps, args.warmup, dist) / reps
+    n_rh = int(pos.numel()) * w.n_kv_heads
+    flops = n_rh * 2 * 2 * D * D
+    props = torch.cuda.get_device_properties(dev)
+    clk_mhz = ClockSampler.max_sm_mhz(dev.index or 0) or 2070.0
+    peak = props.multi_processor_count * 128 * 2 * clk_mhz * 1e6 / 1e12
+    achieved = flops / tb / 1e12
+    del stage, i2
+    return {"rows": int(pos.numel()), "row_heads": n_rh, "ms": tb * 1e3, "row_heads_per_s": n_rh / tb,
+            "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak,
+                         "peak_source": "derived: SMs x 128 fp32 lanes x 2 flops x max SM clock (no tensor cores)"}}
+
+
 # ------------------------------------------------------------------- main ----
 
 def main():
@@ -487,6 +543,17 @@ def main():
     e2e = {"value": job_throughput(world, w.batch, te, args.steps), "unit": "tokens/s",
            "h2d_bytes_per_step": model.q_all.numel() * 2, "d2h_bytes_per_step": model.out_all.numel() * 2}
 
+    # demotion (rows a1-a3): the per-step demotion (one token per request, layer and kv head, on
+    # the side stream in the workloads that demote every step) timed alone and as the step's
+    # overhead; and a bulk demotion of one layer's whole history (the pool fill of a prefix hit)
+    gd = capture(model.demote_step)
+    td = time_graph(gd, args.steps, args.warmup, dist) / args.steps
+    gs = capture(lambda: model.step(side=side, demote=True))
+    ts = time_graph(gs, args.steps, args.warmup, dist) / args.steps
+    demotion = {"per_step_us": td * 1e6, "rows_per_step": w.layers * w.batch * w.n_kv_heads * 2,
+                "step_ms_with_demotion": ts * 1e3, "step_overhead": ts / (t / args.steps)}
+    demotion["bulk"] = bulk_demotion(model, w, args, dist)
+
     bf16 = None
     if model.bf16_full is not None:
         gb = capture(model.step_bf16)
@@ -520,7 +587,7 @@ def main():
                          "bytes_per_launch": unit_bytes, "launch_us": dur * 1e6,
                          "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs copy bandwidth)"},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": model.launches_per_step() * args.steps,
-            "clocks": clk.summary(), "bf16_cache": bf16,
+            "clocks": clk.summary(), "bf16_cache": bf16, "demotion": demotion,
         }
         print(json.dumps(line), flush=True)
     if dist:
