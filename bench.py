@@ -5,7 +5,7 @@ One step = the attention of one decode token for every layer of the model:
 per layer, q·R_K + INT2 history + BF16 sink/recent partials in one launch
 (oscar_decode_attention_fused), then the online-softmax merge with R_V^T
 (oscar_merge); for workloads that demote every step, the demotion of the
-token leaving the recent window runs on a side stream in the same step.
+token leaving the recent window runs inside the same decode launch.
 Steps are captured in a CUDA graph and timed with CUDA events.
 
 Prints one JSON line (rank 0).  Default workload: Qwen3-8B shape at 100,000
@@ -60,7 +60,7 @@ def parse_args():
 def workload_text(w: syn.Workload) -> str:
     ctx = f"contexts U{{{w.ragged[0]}..{w.ragged[1]}}}" if w.ragged else f"context {w.context}"
     extra = f", {w.shared_prefix}-token shared prefix" if w.shared_prefix else ""
-    dem = ", one demotion per request/layer/kv head per step (side stream)" if w.demote_per_step else ""
+    dem = ", one demotion per request/layer/kv head per step (inside the decode launch)" if w.demote_per_step else ""
     return (f"{w.name}: {w.layers} layers, {w.n_q_heads} q / {w.n_kv_heads} kv heads, head_dim {w.head_dim}, "
             f"batch {w.batch}, {ctx} ({w.sink} BF16 sink + INT2 history + {w.recent} BF16 recent){extra}, "
             f"page {w.page_size}, group {w.group}{dem}")
@@ -261,29 +261,23 @@ class Model:
     # One decode step over all layers (the path).  Per layer the BF16 sink/recent half runs on
     # a second stream next to q rotation + the INT2 history half; the merge joins them.
     # Optional events bracket each decode-attention launch.
-    def step(self, events=None, side=None, demote=None):
+    def step(self, events=None, demote=None):
         import torch
         from bit_kv_cache_oscar_gb300 import binding as ob
         L, w = self.L, self.w
         cur = torch.cuda.current_stream()
         demote = self.demote if demote is None else demote
-        if demote and side is not None:
-            side.wait_stream(cur)
-            with torch.cuda.stream(side):
-                for st in self.layers:
-                    ob.oscar_demote(L, st["bf16"], self.bf16_table, st["int2"], self.int2_table, self.dem_req,
-                                    self.dem_pos, st["RK"], st["RV"], 0.96, 0.92, stream=side)
         for l, st in enumerate(self.layers):
             if events is not None:
                 events[l][0].record()
-            # query rotation, history splits and the BF16 window in one launch
+            # query rotation, history splits, the BF16 window (and the per-step demotion) in one launch
             ob.oscar_decode_attention_fused(L, self.q_all[l], st["RK"], st["bf16"], self.bf16_table, st["int2"],
-                                            self.int2_table, self.seq_len, self.hist_dev, self.sm_scale, self.part)
+                                            self.int2_table, self.seq_len, self.hist_dev, self.sm_scale, self.part,
+                                            demote_pos=self.dem_pos if demote else None, R_V=st["RV"],
+                                            c_K=0.96, c_V=0.92)
             if events is not None:
                 events[l][1].record()
             ob.oscar_merge(L, self.part, st["RV"], self.out_all[l])
-        if demote and side is not None:
-            cur.wait_stream(side)
 
     def demote_step(self):
         """The per-step demotion alone: one token per request, layer and kv head (K and V)."""
@@ -487,10 +481,9 @@ def main():
     # read from INT2), so consecutive kernels may overlap.
     ob.oscar_set_launch_overlap(not args.no_overlap)
     bts = bytes_per_step(w, model.seq, model.hist_end)
-    side = torch.cuda.Stream()
 
     # headline: one-step graph replayed K times
-    g = capture(lambda: model.step(side=side))
+    g = capture(lambda: model.step())
     with ClockSampler(local) as clk:
         t = time_graph(g, args.steps, args.warmup, dist)
     ms_step = 1e3 * t / args.steps
@@ -500,11 +493,11 @@ def main():
     KR = min(args.steps, 20)
     evs = [[(torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
             for _ in range(w.layers)] for _ in range(KR)]
-    gp = capture(lambda: model.step(events=evs[0], side=side))
+    gp = capture(lambda: model.step(events=evs[0]))
     gk = torch.cuda.CUDAGraph()
     with torch.cuda.graph(gk):
         for k in range(KR):
-            model.step(events=evs[k], side=side)
+            model.step(events=evs[k])
     for _ in range(args.warmup):
         gp.replay()
     torch.cuda.synchronize()
@@ -543,12 +536,13 @@ def main():
     e2e = {"value": job_throughput(world, w.batch, te, args.steps), "unit": "tokens/s",
            "h2d_bytes_per_step": model.q_all.numel() * 2, "d2h_bytes_per_step": model.out_all.numel() * 2}
 
-    # demotion (rows a1-a3): the per-step demotion (one token per request, layer and kv head, on
-    # the side stream in the workloads that demote every step) timed alone and as the step's
-    # overhead; and a bulk demotion of one layer's whole history (the pool fill of a prefix hit)
+    # demotion (rows a1-a3): the per-step demotion (one token per request, layer and kv head,
+    # folded into the decode launch in the workloads that demote every step) timed alone through
+    # oscar_demote and as the step's overhead; and a bulk demotion of one layer's whole history
+    # (the pool fill of a prefix hit)
     gd = capture(model.demote_step)
     td = time_graph(gd, args.steps, args.warmup, dist) / args.steps
-    gs = capture(lambda: model.step(side=side, demote=True))
+    gs = capture(lambda: model.step(demote=True))
     ts = time_graph(gs, args.steps, args.warmup, dist) / args.steps
     demotion = {"per_step_us": td * 1e6, "rows_per_step": w.layers * w.batch * w.n_kv_heads * 2,
                 "step_ms_with_demotion": ts * 1e3, "step_overhead": ts / (t / args.steps)}

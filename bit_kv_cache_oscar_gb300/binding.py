@@ -100,7 +100,8 @@ def lib():
     L.oscar_version.argtypes = []
     L.oscar_version.restype = ctypes.c_char_p
     L.oscar_decode_attention_fused.argtypes = [P(LayoutC), vp, vp, P(Bf16PoolC), vp, P(Int2PoolC), vp, i32, vp,
-                                               vp, i32, ctypes.c_float, P(PartialsC), vp]
+                                               vp, i32, ctypes.c_float, P(PartialsC), vp, vp, ctypes.c_float,
+                                               ctypes.c_float, vp]
     L.oscar_decode_attention_fused.restype = st
     L.oscar_set_launch_overlap.argtypes = [i32]
     L.oscar_set_launch_overlap.restype = st
@@ -262,12 +263,16 @@ def oscar_decode_attention(layout: Layout, q: torch.Tensor, q_rot: torch.Tensor,
 def oscar_decode_attention_fused(layout: Layout, q: torch.Tensor, R_K: torch.Tensor, bf16_pool: Bf16Pool,
                                  bf16_page_table: torch.Tensor, int2_pool: Int2Pool, int2_page_table: torch.Tensor,
                                  seq_len: torch.Tensor, hist_end: torch.Tensor, sm_scale: float, partials: Partials,
-                                 stream=None):
-    """oscar_decode_attention with q . R_K computed inside the launch (same partials bits)."""
+                                 demote_pos: Optional[torch.Tensor] = None, R_V: Optional[torch.Tensor] = None,
+                                 c_K: float = 0.0, c_V: float = 0.0, stream=None):
+    """oscar_decode_attention with q . R_K computed inside the launch (same partials bits); with
+    demote_pos ([batch] int32, -1 = none) also the per-step demotion of those positions."""
     _check("oscar_decode_attention_fused", lib().oscar_decode_attention_fused(
         ctypes.byref(layout.c()), _ptr(q), _ptr(R_K), ctypes.byref(bf16_pool.c()), _ptr(bf16_page_table),
         ctypes.byref(int2_pool.c()), _ptr(int2_page_table), int(int2_page_table.shape[-1]), _ptr(seq_len),
-        _ptr(hist_end), int(q.shape[0]), float(sm_scale), ctypes.byref(partials.c()), _stream(stream)))
+        _ptr(hist_end), int(q.shape[0]), float(sm_scale), ctypes.byref(partials.c()),
+        _ptr(demote_pos) if demote_pos is not None else None, _ptr(R_V) if R_V is not None else None,
+        float(c_K), float(c_V), _stream(stream)))
 
 
 def oscar_decode_attention_history(layout: Layout, q_rot: torch.Tensor, int2_pool: Int2Pool,

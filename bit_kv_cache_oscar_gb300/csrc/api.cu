@@ -119,6 +119,35 @@ std::atomic<int> g_overlap{0};
 
 bool oscar::launch_overlap() { return g_overlap.load(std::memory_order_relaxed) != 0; }
 
+namespace {
+struct SmemLimit {
+    const void *kern;
+    int dev, bytes;
+};
+std::mutex g_smem_mu;
+SmemLimit g_smem[256];
+int g_n_smem = 0;
+}  // namespace
+
+cudaError_t oscar::ensure_dyn_smem(const void *kern, int smem) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    std::lock_guard<std::mutex> lk(g_smem_mu);
+    int k = 0;
+    while (k < g_n_smem && !(g_smem[k].kern == kern && g_smem[k].dev == dev)) ++k;
+    if (k < g_n_smem && g_smem[k].bytes >= smem) return cudaSuccess;
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    if (k == g_n_smem) {
+        if (g_n_smem == 256) return cudaSuccess;        // untracked: set again next time
+        g_smem[g_n_smem++] = {kern, dev, smem};
+    } else {
+        g_smem[k].bytes = smem;
+    }
+    return cudaSuccess;
+}
+
 extern "C" {
 
 size_t oscar_partials_ml_floats(const oscar_layout_t *L, int32_t batch, int32_t n_splits) {
@@ -235,7 +264,8 @@ oscar_status_t oscar_decode_attention_fused(const oscar_layout_t *layout, const 
                                             const oscar_int2_pool_t *int2_pool, const int32_t *int2_page_table,
                                             int32_t max_pages_per_req, const int32_t *seq_len,
                                             const int32_t *hist_end, int32_t batch, float sm_scale,
-                                            const oscar_partials_t *partials, void *stream) {
+                                            const oscar_partials_t *partials, const int32_t *demote_pos,
+                                            const float *R_V, float c_K, float c_V, void *stream) {
     TRY(check_layout(layout));
     TRY(check_bf16_pool(bf16_pool));
     TRY(check_int2_pool(int2_pool));
@@ -249,10 +279,20 @@ oscar_status_t oscar_decode_attention_fused(const oscar_layout_t *layout, const 
     if (!oscar::int2_mma_supported(*layout))
         return fail(OSCAR_ERR_UNSUPPORTED, "fused rotation needs 1, 2, 4 or 8 kv heads; use oscar_rotate_q + "
                                            "oscar_decode_attention");
-    return cuda_status(oscar::launch_decode_mma(*layout, nullptr, R_K, int2_view(int2_pool), int2_page_table, q,
-                                                bf16_view(bf16_pool), bf16_page_table, max_pages_per_req, seq_len,
-                                                hist_end, batch, sm_scale, part_view(partials), status_ptr(), true,
-                                                true, (cudaStream_t)stream),
+    oscar::FusedDemotion dem{};
+    if (demote_pos) {
+        if (!R_V || !aligned16(R_V)) return fail(OSCAR_ERR_INVALID_ARG, "demotion needs a 16-byte aligned R_V");
+        dem.dem_pos = demote_pos;
+        dem.RV = R_V;
+        dem.cK = c_K;
+        dem.cV = c_V;
+        dem.dst = {int2_pool->codes_k, int2_pool->codes_v, int2_pool->scale_k, int2_pool->zero_k,
+                   int2_pool->scale_v, int2_pool->zero_v, int2_pool->n_pages};
+    }
+    return cuda_status(oscar::launch_decode_mma_demote(*layout, R_K, int2_view(int2_pool), int2_page_table, q,
+                                                       bf16_view(bf16_pool), bf16_page_table, max_pages_per_req,
+                                                       seq_len, hist_end, batch, sm_scale, part_view(partials),
+                                                       status_ptr(), dem, (cudaStream_t)stream),
                        "fused decode attention launch");
 }
 

@@ -363,14 +363,7 @@ cudaError_t launch_bf(BfArgs a, dim3 grid, cudaStream_t st) {
     a.stage_off = 128 + ((kCW * a.ws_bytes + 127) & ~127);
     const int combine = kCW * NT * 4 * (2 + kHeadDim) * 4;
     const int smem = a.stage_off + (kStages * kStageBytes > combine ? kStages * kStageBytes : combine);
-    static thread_local int configured[64] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 64 && configured[dev] < smem) {
-        cudaError_t e = cudaFuncSetAttribute(bf16_mma_kernel<G>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-        if (e != cudaSuccess) return e;
-        configured[dev] = smem;
-    }
+    if (cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void *>(bf16_mma_kernel<G>), smem)) return e;
     bf16_mma_kernel<G><<<grid, kThreads, smem, st>>>(a);
     return cudaGetLastError();
 }

@@ -32,6 +32,7 @@
 
 #include "oscar_internal.cuh"
 #include "ptx.cuh"
+#include "quant.cuh"
 
 namespace oscar {
 namespace {
@@ -112,12 +113,15 @@ struct MmaArgs {
     int stages, stage_bytes, off_v, off_s, arr_bytes, ws_bytes, stage_off;
     int csize;        // CTAs per cluster; each cluster writes one partial slot
     int res_off;      // byte offset (from the first stage) of the per-CTA result area
-    int hist_ctas;    // CTAs [0, hist_ctas) of grid.x take the history; the rest the BF16 window
+    int hist_ctas;    // CTAs of grid.x that take the history (after the window CTAs)
+    int win_ctas;     // CTAs [0, win_ctas) of grid.x take the BF16 window (0 or one cluster)
     int win_off;      // byte offset (from the first stage) of the window CTAs' warp results
     const float *RK;            // non-null: history CTAs rotate q themselves (q_rot unused)
     int rot_off;                // byte offset (from the aligned base) of the rotated-query rows [Hq][128]
     int rk_chunk;               // bytes of R_K staged per step in the stage area (16, 32 or 64 KB)
     const uint16_t *q;          // raw bf16 queries (window CTAs, and the rotation when RK is set)
+    FusedDemotion dem;          // per-step demotion done by the window CTAs (dem.dem_pos NULL: none)
+    int group;
     Bf16PoolView bpool;         // BF16 sink/recent pool and its page table (window CTAs)
     const int32_t *bpt;
 };
@@ -159,6 +163,88 @@ __device__ __forceinline__ void cluster_combine(const MmaArgs &a, const float *r
     cluster_sync_all();                 // no CTA leaves while its shared memory is being read
 }
 
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Fold U tokens (K/V rows kk, vv: lane l holds channels 4l..4l+3; ok[u] = token present) into
+// the online softmax (base 2) of the warp's G query heads.  The U*G per-lane partial dot
+// products are summed across the warp by a reduce-scatter (each step halves the values a lane
+// keeps), so a sum costs about one shuffle instead of five; the sums are then broadcast and
+// every lane updates m, l and its accumulator channels for all heads.
+template <int G, int U>
+__device__ __forceinline__ void window_fold(const float (&q)[G][4], const uint2 (&kk)[U], const uint2 (&vv)[U],
+                                            const bool (&ok)[U], float scale2, float (&m)[G], float (&l)[G],
+                                            float (&acc)[G][4], int lane) {
+    constexpr int V = U * G;                           // value index u * G + hh
+    static_assert((V & (V - 1)) == 0 && V <= 32, "U * G must be a power of two up to 32");
+    constexpr int LOGV = V == 1 ? 0 : V == 2 ? 1 : V == 4 ? 2 : V == 8 ? 3 : V == 16 ? 4 : 5;
+    float v[V];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const float k0 = __uint_as_float(kk[u].x << 16), k1 = __uint_as_float(kk[u].x & 0xffff0000u);
+        const float k2 = __uint_as_float(kk[u].y << 16), k3 = __uint_as_float(kk[u].y & 0xffff0000u);
+#pragma unroll
+        for (int hh = 0; hh < G; ++hh)
+            v[u * G + hh] = fmaf(q[hh][3], k3, fmaf(q[hh][2], k2, fmaf(q[hh][1], k1, q[hh][0] * k0)));
+    }
+    // reduce-scatter: at distance D = 16 >> k a lane keeps the upper half of its n values when
+    // lane & D, the lower half otherwise; after LOGV steps v[0] is value idx(lane), then plain sums
+#pragma unroll
+    for (int k = 0; k < 5; ++k) {
+        const int D = 16 >> k;
+        const int n = V >> k;
+        if (n > 1) {
+            const bool up = (lane & D) != 0;
+#pragma unroll
+            for (int i = 0; i < n / 2; ++i) {
+                const float send = up ? v[i] : v[i + n / 2];
+                const float keep = up ? v[i + n / 2] : v[i];
+                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, D);
+            }
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], D);
+        }
+    }
+    float t[V];                                        // every lane: all U x G logits (base 2)
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+        int src = 0;                                   // the lane holding value j
+#pragma unroll
+        for (int k = 0; k < LOGV; ++k) src |= ((j >> (LOGV - 1 - k)) & 1) * (16 >> k);
+        t[j] = __shfl_sync(0xffffffffu, v[0], src) * scale2;
+    }
+    float vf[U][4];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        vf[u][0] = __uint_as_float(vv[u].x << 16); vf[u][1] = __uint_as_float(vv[u].x & 0xffff0000u);
+        vf[u][2] = __uint_as_float(vv[u].y << 16); vf[u][3] = __uint_as_float(vv[u].y & 0xffff0000u);
+    }
+#pragma unroll
+    for (int hh = 0; hh < G; ++hh) {
+        float mx = m[hh];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            if (ok[u]) mx = fmaxf(mx, t[u * G + hh]);
+        if (mx == -INFINITY) continue;                  // nothing folded yet for this head
+        const float al = ex2_approx(m[hh] - mx);
+        float ls = 0.f, a4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const float pr = ok[u] ? ex2_approx(t[u * G + hh] - mx) : 0.f;
+            ls += pr;
+#pragma unroll
+            for (int c = 0; c < 4; ++c) a4[c] = fmaf(pr, vf[u][c], a4[c]);
+        }
+        l[hh] = fmaf(l[hh], al, ls);
+#pragma unroll
+        for (int c = 0; c < 4; ++c) acc[hh][c] = fmaf(acc[hh][c], al, a4[c]);
+        m[hh] = mx;
+    }
+}
+
 // ---- BF16 sink/recent window, on CUDA cores, in the CTAs after the history ones.
 // Window positions of request b, in order: [0, n0) then [lo1, T), n0 = min(sink, T),
 // lo1 = max(h_end, n0).  Window CTA wr of wc takes positions [wr*n/wc, (wr+1)*n/wc); warp w
@@ -190,18 +276,32 @@ __device__ void window_cta(const MmaArgs &a, float *wsm, float *res, int T, int 
             q[hh][0] = __uint_as_float(v.x << 16); q[hh][1] = __uint_as_float(v.x & 0xffff0000u);
             q[hh][2] = __uint_as_float(v.y << 16); q[hh][3] = __uint_as_float(v.y & 0xffff0000u);
         }
-        constexpr int U = 4;                     // tokens whose rows are loaded together
-        for (int i0 = i_lo + sub; i0 < i_hi; i0 += U * nsub) {
+        // Tokens in chunks of 64 per warp: the chunk's page ids are read once (two per lane), then
+        // U tokens' K/V rows are loaded together and folded one by one.
+        constexpr int U = 4;
+        for (int c0 = i_lo + sub; c0 < i_hi; c0 += 64 * nsub) {
+          int pg[2];
+#pragma unroll
+          for (int r = 0; r < 2; ++r) {
+              const int i = c0 + (lane + 32 * r) * nsub;
+              pg[r] = -1;
+              if (i < i_hi) {
+                  const int p = i < n0 ? i : lo1 + (i - n0);
+                  pg[r] = a.bpt[(size_t)b * a.max_pages + p / a.page_size];
+              }
+          }
+          for (int k0 = 0; k0 < 64 && c0 + k0 * nsub < i_hi; k0 += U) {
+            const int pgr = k0 < 32 ? pg[0] : pg[1];
             uint2 kk[U], vv[U];
             bool ok[U];
 #pragma unroll
             for (int u = 0; u < U; ++u) {
-                const int i = i0 + u * nsub;
+                const int i = c0 + (k0 + u) * nsub;
+                const int page = __shfl_sync(0xffffffffu, pgr, (k0 & 31) + u);
                 ok[u] = false;
                 kk[u] = vv[u] = make_uint2(0u, 0u);
                 if (i < i_hi) {
                     const int p = i < n0 ? i : lo1 + (i - n0);
-                    const int page = a.bpt[(size_t)b * a.max_pages + p / a.page_size];
                     if (page >= 0 && page < a.bpool.n_pages) {
                         const size_t row = ((size_t)page * a.page_size + p % a.page_size) * Hkv + h;
                         kk[u] = __ldg(reinterpret_cast<const uint2 *>(a.bpool.k + row * kHeadDim) + lane);
@@ -212,32 +312,8 @@ __device__ void window_cta(const MmaArgs &a, float *wsm, float *res, int T, int 
                     }
                 }
             }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                if (!ok[u]) continue;
-                const float k4[4] = {__uint_as_float(kk[u].x << 16), __uint_as_float(kk[u].x & 0xffff0000u),
-                                     __uint_as_float(kk[u].y << 16), __uint_as_float(kk[u].y & 0xffff0000u)};
-                const float v4[4] = {__uint_as_float(vv[u].x << 16), __uint_as_float(vv[u].x & 0xffff0000u),
-                                     __uint_as_float(vv[u].y << 16), __uint_as_float(vv[u].y & 0xffff0000u)};
-                float d[G];
-#pragma unroll
-                for (int hh = 0; hh < G; ++hh)
-                    d[hh] = fmaf(q[hh][3], k4[3], fmaf(q[hh][2], k4[2], fmaf(q[hh][1], k4[1], q[hh][0] * k4[0])));
-#pragma unroll
-                for (int o = 16; o; o >>= 1)
-#pragma unroll
-                    for (int hh = 0; hh < G; ++hh) d[hh] += __shfl_xor_sync(0xffffffffu, d[hh], o);
-#pragma unroll
-                for (int hh = 0; hh < G; ++hh) {
-                    const float t = d[hh] * a.scale2;
-                    const float mn = fmaxf(m[hh], t);
-                    const float al = exp2f(m[hh] - mn), pr = exp2f(t - mn);
-                    l[hh] = fmaf(l[hh], al, pr);
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) acc[hh][c] = fmaf(acc[hh][c], al, pr * v4[c]);
-                    m[hh] = mn;
-                }
-            }
+            window_fold<G, U>(q, kk, vv, ok, a.scale2, m, l, acc, lane);
+          }
         }
         // warp results: wsm = [warp][G] m, [warp][G] l, [warp][G][128] acc
         float *wm = wsm, *wl = wsm + kCW * G, *wa = wsm + 2 * kCW * G;
@@ -285,6 +361,74 @@ __device__ void window_cta(const MmaArgs &a, float *wsm, float *res, int T, int 
     if (to_res) cluster_combine(a, res, Hq, b, S);
 }
 
+// ---- Per-step demotion by the window CTAs: request b's position dem_pos[b] (one that left the
+// recent window; this launch still reads it from BF16) is rotated by R_K / R_V, clipped,
+// quantized and packed into the INT2 pool for kv heads wr, wr + wc, ...  The arithmetic is
+// oscar_demote's: y_j = fma-chain_i x_i * R[i][j] (i ascending, fp32), then the shared
+// quantizer.  R is staged through the stage area a chunk at a time.  All threads call this.
+__device__ void window_demote(const MmaArgs &a, float *small, uint8_t *area, int T, int he, int b, int wr, int wc) {
+    const int tid = threadIdx.x;
+    const int Hkv = a.n_kv, ps = a.page_size;
+    const int p = a.dem.dem_pos[b];
+    if (p < 0) return;
+    int sp = -1, dp = -1;
+    const bool in_range = p >= he && p < T && p / ps < a.max_pages;
+    if (in_range) {
+        sp = a.bpt[(size_t)b * a.max_pages + p / ps];
+        dp = a.pt[(size_t)b * a.max_pages + p / ps];
+    }
+    if (!in_range || sp < 0 || sp >= a.bpool.n_pages || dp < 0 || dp >= a.dem.dst.n_pages) {
+        if (tid == 0)
+            flag_status(a.status, !in_range ? OSCAR_DEV_BAD_LENGTH
+                                            : (sp < 0 || sp >= a.bpool.n_pages) ? OSCAR_DEV_BAD_BF16_PAGE
+                                                                                : OSCAR_DEV_BAD_INT2_PAGE);
+        return;
+    }
+    float *xs = small;                           // [128] the source row
+    float *red = small + kHeadDim;               // [8]
+    uint64_t *bar = reinterpret_cast<uint64_t *>(small + kHeadDim + 8);   // R chunk landed (expect-tx)
+    float *Rs = reinterpret_cast<float *>(area);
+    const int rpc = a.rk_chunk / (kHeadDim * 4), nch = kHeadDim / rpc;
+    const int gpr = kHeadDim / a.group;
+    const size_t srow = ((size_t)sp * ps + p % ps) * Hkv, drow = ((size_t)dp * ps + p % ps) * Hkv;
+    if (tid == 0) {
+        mbar_init(saddr(bar), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    int n = 0;                                   // bulk copies so far (phase parity)
+    for (int hk = wr; hk < Hkv; hk += wc) {
+        for (int which = 0; which < 2; ++which) {
+            const float *R = (which ? a.dem.RV : a.RK) + (size_t)hk * kHeadDim * kHeadDim;
+            __syncthreads();                     // the previous row's xs and Rs are consumed
+            if (tid < kHeadDim) xs[tid] = bf16_to_f32((which ? a.bpool.v : a.bpool.k)[(srow + hk) * kHeadDim + tid]);
+            float y = 0.f;
+            for (int c = 0; c < nch; ++c, ++n) {
+                if (c > 0) __syncthreads();
+                if (tid == 0) {                  // one bulk copy of the chunk (rows c*rpc ...)
+                    fence_proxy_async_smem();    // the area held the window's generic stores
+                    mbar_arrive_expect_tx(saddr(bar), a.rk_chunk);
+                    tma_load_1d(saddr(Rs), R + (size_t)c * rpc * kHeadDim, a.rk_chunk, saddr(bar));
+                }
+                if (!mbar_wait(saddr(bar), n & 1) && tid == 0) flag_status(a.status, OSCAR_DEV_WAIT_TIMEOUT);
+                __syncthreads();
+                if (tid < kHeadDim) {
+#pragma unroll 8
+                    for (int i = 0; i < rpc; ++i) y = __fmaf_rn(xs[c * rpc + i], Rs[i * kHeadDim + tid], y);
+                }
+            }
+            if (tid < kHeadDim) {                // warps 0..3: one channel each
+                uint8_t *codes = which ? a.dem.dst.codes_v : a.dem.dst.codes_k;
+                uint16_t *scale = which ? a.dem.dst.scale_v : a.dem.dst.scale_k;
+                uint16_t *zero = which ? a.dem.dst.zero_v : a.dem.dst.zero_k;
+                const size_t r = drow + hk;
+                quantize_row_store(y, which ? a.dem.cV : a.dem.cK, a.group, true, codes + r * (kHeadDim / 4),
+                                   scale + r * gpr, zero + r * gpr, red, tid,
+                                   [] { asm volatile("bar.sync 2, 128;" ::: "memory"); });
+            }
+        }
+    }
+}
+
 constexpr float kLazy = 8.0f;   // log2 headroom before the running maximum is raised
 // rotated-query rows in shared memory: element d of a row at d + d / 32 (row stride 132), so
 // that the operand reads of a warp (4 heads x 4 column groups) fall in distinct banks
@@ -292,11 +436,6 @@ constexpr int kQS = kHeadDim + kHeadDim / 32;
 __device__ __forceinline__ int qs_col(int d) { return d + (d >> 5); }
 constexpr int kWsWords = 20;    // words per P-operand column: 2 tiles x 8 + 4 (bank spread)
 
-__device__ __forceinline__ float ex2_approx(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
 
 // (v0, v1) -> f16x2 of the round-to-nearest values (hi) and f16x2 of their residuals (lo)
 __device__ __forceinline__ void split2(float v0, float v1, uint32_t &hi, uint32_t &lo) {
@@ -322,7 +461,9 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
     int *masks = reinterpret_cast<int *>(smem + 64);        // per stage: bit j = tile j holds data
     uint8_t *stage0 = smem + a.stage_off;
 
-    const int s = blockIdx.x, b = blockIdx.y;
+    // grid.x: the window cluster first (so that it starts at once and its work hides behind the
+    // history), then the history CTAs; s = this CTA's index among the history CTAs.
+    const int s = (int)blockIdx.x - a.win_ctas, b = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // With 8 kv heads (the tensor-map path) the stage layout is compile-time: addresses fold.
     const int Hkv = TMA ? 8 : a.n_kv, Hq = Hkv * G, S = a.out.S;
@@ -331,10 +472,13 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
     const int stage_bytes = TMA ? ((2 * 8 * 2048 + 4 * kStageTok * 8 * NGRP * 2 + 127) & ~127) : a.stage_bytes;
     int T, he;
     read_lengths(a.seq_len, a.hist_end, b, a.sink, a.max_pages * a.page_size, a.status, T, he);
-    if (s >= a.hist_ctas) {                    // a BF16 window CTA (uniform over the cluster)
+    if (s < 0) {                               // a BF16 window CTA (uniform over the cluster)
         pdl_wait();                            // q and the partials belong to the previous kernels
         window_cta<G>(a, reinterpret_cast<float *>(stage0 + a.win_off), reinterpret_cast<float *>(stage0 + a.res_off),
-                      T, he, b, s - a.hist_ctas, (int)gridDim.x - a.hist_ctas);
+                      T, he, b, (int)blockIdx.x, a.win_ctas);
+        // (after the cluster's last barrier: the stage area is free again)
+        if (a.dem.dem_pos)
+            window_demote(a, reinterpret_cast<float *>(smem + 128), stage0, T, he, b, (int)blockIdx.x, a.win_ctas);
         return;
     }
     const SplitRange r = history_split(a.sink, he, a.hist_ctas, s);   // C sub-splits per slot
@@ -483,7 +627,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
             if (lane == 0) mbar_arrive(saddr(&bars[st]));
         }
         asm volatile("cp.async.wait_all;" ::: "memory");
-        if (a.csize > 1) cluster_combine(a, reinterpret_cast<const float *>(stage0 + a.res_off), Hq, b, blockIdx.x / a.csize);
+        if (a.csize > 1) cluster_combine(a, reinterpret_cast<const float *>(stage0 + a.res_off), Hq, b, s / a.csize);
         return;
     }
 
@@ -882,7 +1026,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
                 }
             }
         }
-        if (to_res) cluster_combine(a, res, Hq, b, blockIdx.x / a.csize);
+        if (to_res) cluster_combine(a, res, Hq, b, s / a.csize);
         return;
     }
 
@@ -931,7 +1075,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
             }
         }
     }
-    if (to_res) cluster_combine(a, res, Hq, b, blockIdx.x / a.csize);
+    if (to_res) cluster_combine(a, res, Hq, b, s / a.csize);
 }
 
 // Largest cluster size C in {8, 4, 2} whose co-resident clusters still occupy at least 90% of
@@ -949,7 +1093,7 @@ int int2_cluster_size(const void *kern, int smem, int threads, int *active = nul
             return cache[i].c;
         }
     int best = 1, best_active = 1;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) == cudaSuccess) {
+    if (ensure_dyn_smem(kern, smem) == cudaSuccess) {
         int sms = 0, per_sm = 0;
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
         cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, smem);
@@ -1072,9 +1216,11 @@ cudaError_t launch_mma(const oscar_layout_t &L, MmaArgs a, int batch, bool histo
             return cudaErrorInvalidValue;
     }
     a.csize = int2_cluster_size(reinterpret_cast<const void *>(kern), smem, kThreads);
+    if (cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void *>(kern), smem)) return e;
     a.hist_ctas = history ? a.out.S * a.csize : 0;
+    a.win_ctas = window ? a.csize : 0;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.hist_ctas + (window ? a.csize : 0), batch);
+    cfg.gridDim = dim3(a.win_ctas + a.hist_ctas, batch);
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
@@ -1113,14 +1259,40 @@ bool int2_mma_supported(const oscar_layout_t &L) {
     return (H == 1 || H == 2 || H == 4 || H == 8) && L.head_dim == kHeadDim;
 }
 
+static cudaError_t decode_mma_impl(const oscar_layout_t &L, const float *RK, Int2PoolView pool, const int32_t *pt,
+                                   const uint16_t *q, Bf16PoolView bpool, const int32_t *bpt, int max_pages,
+                                   const int32_t *seq_len, const int32_t *hist_end, int batch, float sm_scale,
+                                   PartialsView out, int32_t *status, const FusedDemotion &dem, cudaStream_t st,
+                                   const float *q_rot, bool history, bool window);
+
 cudaError_t launch_decode_mma(const oscar_layout_t &L, const float *q_rot, const float *RK, Int2PoolView pool,
                               const int32_t *pt, const uint16_t *q, Bf16PoolView bpool, const int32_t *bpt,
                               int max_pages, const int32_t *seq_len, const int32_t *hist_end, int batch,
                               float sm_scale, PartialsView out, int32_t *status, bool history, bool window,
                               cudaStream_t st) {
+    FusedDemotion none{};
+    return decode_mma_impl(L, RK, pool, pt, q, bpool, bpt, max_pages, seq_len, hist_end, batch, sm_scale, out, status,
+                           none, st, q_rot, history, window);
+}
+
+cudaError_t launch_decode_mma_demote(const oscar_layout_t &L, const float *RK, Int2PoolView pool, const int32_t *pt,
+                                     const uint16_t *q, Bf16PoolView bpool, const int32_t *bpt, int max_pages,
+                                     const int32_t *seq_len, const int32_t *hist_end, int batch, float sm_scale,
+                                     PartialsView out, int32_t *status, const FusedDemotion &dem, cudaStream_t st) {
+    return decode_mma_impl(L, RK, pool, pt, q, bpool, bpt, max_pages, seq_len, hist_end, batch, sm_scale, out, status,
+                           dem, st, nullptr, true, true);
+}
+
+static cudaError_t decode_mma_impl(const oscar_layout_t &L, const float *RK, Int2PoolView pool, const int32_t *pt,
+                                   const uint16_t *q, Bf16PoolView bpool, const int32_t *bpt, int max_pages,
+                                   const int32_t *seq_len, const int32_t *hist_end, int batch, float sm_scale,
+                                   PartialsView out, int32_t *status, const FusedDemotion &dem, cudaStream_t st,
+                                   const float *q_rot, bool history, bool window) {
     if (batch <= 0 || (!history && !window)) return cudaSuccess;
     MmaArgs a{};
     a.RK = RK;
+    a.dem = dem;
+    a.group = L.group;
     a.q = q;
     a.bpool = bpool;
     a.bpt = bpt;

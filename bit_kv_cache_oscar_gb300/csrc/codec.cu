@@ -16,6 +16,7 @@
 
 #include "oscar_internal.cuh"
 #include "ptx.cuh"
+#include "quant.cuh"
 
 namespace oscar {
 namespace {
@@ -24,58 +25,12 @@ constexpr int kThreads = 128;
 constexpr int kTokPerPass = 8;       // rows rotated together (R element reused 8x)
 constexpr int kTokPerCta = 256;      // rows per CTA before the grid grows
 
-// Quantize one row held one channel per thread and store codes/scale/zero.
-// Every thread of the CTA must call this (it synchronizes when group > 32).
-// red: shared scratch of 8 floats.
+// Quantize one row held one channel per thread (thread j = channel j of a 128-thread CTA).
 __device__ __forceinline__ void quantize_row_store(float y, float clip, int group, bool store,
                                                    uint8_t *codes_row, uint16_t *scale_row,
                                                    uint16_t *zero_row, float *red) {
-    const int j = threadIdx.x, lane = j & 31, warp = j >> 5;
-    float mn = y, mx = y;
-#pragma unroll
-    for (int o = 16; o; o >>= 1) {
-        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    }
-    if (group > 32) {
-        __syncthreads();
-        if (lane == 0) {
-            red[warp] = mn;
-            red[4 + warp] = mx;
-        }
-        __syncthreads();
-        const int wpg = group >> 5;              // warps per group
-        const int w0 = (warp / wpg) * wpg;
-        mn = red[w0];
-        mx = red[4 + w0];
-        for (int w = w0 + 1; w < w0 + wpg; ++w) {
-            mn = fminf(mn, red[w]);
-            mx = fmaxf(mx, red[4 + w]);
-        }
-    }
-    mn = __fadd_rn(mn, 0.0f);                    // a signed zero is read as +0
-    mx = __fadd_rn(mx, 0.0f);
-    const float lo = __fmul_rn(clip, mn);        // clipped range c*[min, max]
-    const float hi = __fmul_rn(clip, mx);
-    const float step = __fdiv_rn(__fsub_rn(hi, lo), 3.0f);
-    const uint16_t zb = f32_to_bf16_rn(lo);
-    const uint16_t sb = f32_to_bf16_rn(step);
-    const float z = bf16_to_f32(zb), s = bf16_to_f32(sb);
-    int c = 0;
-    if (s != 0.0f) {
-        const float r = rintf(__fdiv_rn(__fsub_rn(y, z), s));
-        c = r >= 3.0f ? 3 : (r >= 0.0f ? (int)r : 0);
-    }
-    uint32_t v = (uint32_t)c << (2 * (lane & 3));
-    v |= __shfl_xor_sync(0xffffffffu, v, 1);
-    v |= __shfl_xor_sync(0xffffffffu, v, 2);
-    if (store) {
-        if ((lane & 3) == 0) codes_row[j >> 2] = (uint8_t)v;
-        if ((j % group) == 0) {
-            scale_row[j / group] = sb;
-            zero_row[j / group] = zb;
-        }
-    }
+    oscar::quantize_row_store(y, clip, group, store, codes_row, scale_row, zero_row, red, (int)threadIdx.x,
+                              [] { __syncthreads(); });
 }
 
 struct DemoteArgs {
@@ -97,6 +52,7 @@ struct DemoteArgs {
 // Dynamic smem: R (128 x 128 fp32) + kTokPerPass rows + small scratch.
 __global__ void __launch_bounds__(kThreads) demote_kernel(DemoteArgs a) {
     extern __shared__ __align__(16) float smem[];
+    __shared__ __align__(8) uint64_t rbar;              // R landed (expect-tx)
     float *Rs = smem;                                   // [128][128]
     float *xs = Rs + kHeadDim * kHeadDim;               // [kTokPerPass][128]
     float *red = xs + kTokPerPass * kHeadDim;           // [8]
@@ -112,8 +68,15 @@ __global__ void __launch_bounds__(kThreads) demote_kernel(DemoteArgs a) {
     uint16_t *zero = which ? a.zero_v : a.zero_k;
     const int gpr = kHeadDim / a.group;                 // groups per row
 
-    for (int i = j; i < kHeadDim * kHeadDim / 4; i += kThreads)
-        reinterpret_cast<float4 *>(Rs)[i] = __ldg(reinterpret_cast<const float4 *>(R) + i);
+    // R (64 KB) in one bulk copy: a loop of vector loads waits for each batch in turn
+    if (j == 0) {
+        mbar_init(saddr(&rbar), 1);
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        mbar_arrive_expect_tx(saddr(&rbar), kHeadDim * kHeadDim * 4);
+        tma_load_1d(saddr(Rs), R, kHeadDim * kHeadDim * 4, saddr(&rbar));
+    }
+    __syncthreads();
+    if (!mbar_wait(saddr(&rbar), 0) && j == 0) flag_status(a.status, OSCAR_DEV_WAIT_TIMEOUT);
 
     const int i0 = blockIdx.y * kTokPerCta;
     const int i1 = min(a.n, i0 + kTokPerCta);
@@ -249,14 +212,7 @@ cudaError_t launch_demote(const oscar_layout_t &L, Bf16PoolView src, const int32
     a.rot_out = rot_out;
     a.status = status;
     const size_t smem = sizeof(float) * (kHeadDim * kHeadDim + kTokPerPass * kHeadDim + 8) + sizeof(int) * kTokPerPass;
-    static thread_local int configured_device = -1;
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (configured_device != dev) {
-        cudaError_t e = cudaFuncSetAttribute(demote_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        configured_device = dev;
-    }
+    if (cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void *>(demote_kernel), (int)smem)) return e;
     dim3 grid(2 * L.n_kv_heads, (n + kTokPerCta - 1) / kTokPerCta);
     demote_kernel<<<grid, kThreads, smem, st>>>(a);
     return cudaGetLastError();

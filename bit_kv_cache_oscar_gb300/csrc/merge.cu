@@ -151,14 +151,7 @@ cudaError_t launch_merge(const oscar_layout_t &L, PartialsView p, const float *R
     if (batch <= 0) return cudaSuccess;
     const int hq = L.n_kv_heads * L.gqa;
     const size_t smem = sizeof(float) * ((RV ? kQuarter * kPad : 0) + kHeadDim + 2 * (p.S + 1) + 8);
-    static thread_local int configured[64] = {0};
-    int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 64 && configured[dev] < (int)smem) {
-        cudaError_t e = cudaFuncSetAttribute(merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-        if (e != cudaSuccess) return e;
-        configured[dev] = (int)smem;
-    }
+    if (cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void *>(merge_kernel), (int)smem)) return e;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attrs[1];
     cfg.gridDim = dim3(hq, batch, RV ? 4 : 1);

@@ -75,6 +75,11 @@ __device__ __forceinline__ void read_lengths(const int32_t *seq_len, const int32
 // Record the one-line reason returned by oscar_last_error_string() and return `code`.
 oscar_status_t set_last_error(oscar_status_t code, const char *msg);
 
+// Raise (never lower) a kernel's dynamic shared-memory limit on the current device to `smem`.
+// One kernel serves layouts of different sizes, and a lower setting would make an earlier,
+// larger launch configuration fail; process-wide, safe across host threads.
+cudaError_t ensure_dyn_smem(const void *kern, int smem);
+
 // Process-wide launch-overlap switch (programmatic dependent launch); see oscar.h.
 bool launch_overlap();
 
@@ -92,6 +97,13 @@ inline void add_overlap_attr(cudaLaunchConfig_t &cfg, cudaLaunchAttribute *attrs
 struct Int2PoolView {
     const uint8_t *codes_k, *codes_v;
     const uint16_t *scale_k, *zero_k, *scale_v, *zero_v;
+    int n_pages;
+};
+
+// The same pool, writable (the demotion's destination).
+struct Int2PoolMut {
+    uint8_t *codes_k, *codes_v;
+    uint16_t *scale_k, *zero_k, *scale_v, *zero_v;
     int n_pages;
 };
 
@@ -135,6 +147,20 @@ cudaError_t launch_decode_mma(const oscar_layout_t &L, const float *q_rot, const
                               int max_pages, const int32_t *seq_len, const int32_t *hist_end, int batch,
                               float sm_scale, PartialsView out, int32_t *status, bool history, bool window,
                               cudaStream_t st);
+
+// Per-step demotion folded into the window CTAs of launch_decode_mma: request b demotes
+// position dem_pos[b] (>= hist_end[b], or -1 for none) of every kv head, K and V, from the BF16
+// pool into dst (the INT2 pool).  Set on the launch through this descriptor.
+struct FusedDemotion {
+    const int32_t *dem_pos;     // NULL: no demotion
+    const float *RV;
+    float cK, cV;
+    Int2PoolMut dst;
+};
+cudaError_t launch_decode_mma_demote(const oscar_layout_t &L, const float *RK, Int2PoolView pool, const int32_t *pt,
+                                     const uint16_t *q, Bf16PoolView bpool, const int32_t *bpt, int max_pages,
+                                     const int32_t *seq_len, const int32_t *hist_end, int batch, float sm_scale,
+                                     PartialsView out, int32_t *status, const FusedDemotion &dem, cudaStream_t st);
 
 // Tensor-core BF16 kernel (mode 0 any n_kv_heads; mode 1 n_kv_heads in {1, 2, 4, 8}).
 bool bf16_mma_supported(const oscar_layout_t &L, int mode);

@@ -96,6 +96,10 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int 
         : "memory");
 }
 
+// Order this thread's earlier generic-proxy shared-memory accesses (made visible to it by a
+// barrier) before its following bulk-copy (async-proxy) writes to the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 // ---- programmatic dependent launch (no-ops when the kernel was launched without it)
 // Block until the grids this one depends on have completed and their writes are visible.
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }

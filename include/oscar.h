@@ -216,7 +216,7 @@ OSCAR_API oscar_status_t oscar_rotate_q(const oscar_layout_t *layout, const uint
  * n = ceil(h/16) - first, split s covers tiles [first + floor(s·n/S),
  * first + floor((s+1)·n/S)) clipped to [sink, h); the BF16 partial covers
  * [0, sink) ∪ [h, T).  When the tensor-core kernels support the layout (1, 2,
- * 4 or 8 kv heads) both parts are computed by one launch, whose last cluster
+ * 4 or 8 kv heads) both parts are computed by one launch, whose first cluster
  * per request takes the BF16 window.
  */
 OSCAR_API oscar_status_t oscar_decode_attention(const oscar_layout_t *layout,
@@ -238,6 +238,15 @@ OSCAR_API oscar_status_t oscar_decode_attention(const oscar_layout_t *layout,
  * tensor-core kernels take (n_kv_heads 1, 2, 4 or 8); otherwise returns
  * OSCAR_ERR_UNSUPPORTED and the caller uses the two calls.  No method page
  * describes this fusion; it removes one launch per layer.
+ *
+ * Optional per-step demotion ([news] online path: the token leaving the recent
+ * window is demoted): with demote_pos non-NULL (int32 [batch], -1 = none),
+ * position demote_pos[b] of request b is demoted for every kv head, K with R_K and
+ * c_K, V with R_V and c_V, exactly as oscar_demote would (same arithmetic, same
+ * bytes), by the CTAs that compute the BF16 window.  The position must be at or
+ * after hist_end[b] and before seq_len[b] (this launch still reads it from BF16);
+ * otherwise it is skipped and OSCAR_DEV_BAD_LENGTH is set.  demote_pos NULL: R_V,
+ * c_K, c_V are ignored.
  */
 OSCAR_API oscar_status_t oscar_decode_attention_fused(const oscar_layout_t *layout, const uint16_t *q,
                                                       const float *R_K, const oscar_bf16_pool_t *bf16_pool,
@@ -246,7 +255,9 @@ OSCAR_API oscar_status_t oscar_decode_attention_fused(const oscar_layout_t *layo
                                                       const int32_t *int2_page_table, int32_t max_pages_per_req,
                                                       const int32_t *seq_len, const int32_t *hist_end,
                                                       int32_t batch, float sm_scale,
-                                                      const oscar_partials_t *partials, void *stream);
+                                                      const oscar_partials_t *partials,
+                                                      const int32_t *demote_pos, const float *R_V, float c_K,
+                                                      float c_V, void *stream);
 
 /*
  * The two halves of oscar_decode_attention, for callers that run them on two

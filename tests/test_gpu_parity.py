@@ -302,6 +302,64 @@ def test_fused_rotation_matches_rotate_then_decode(n_kv, gqa, ps, group, seq, S)
     assert ob.oscar_get_device_status() == 0
 
 
+def _pool_bytes(i2):
+    return [t.clone() for t in (i2.codes_k, i2.codes_v, i2.scale_k, i2.zero_k, i2.scale_v, i2.zero_v)]
+
+
+@pytest.mark.parametrize("n_kv,gqa,ps,group,seq,S", [
+    (8, 4, 64, 128, (3000, 1700), 6),
+    (8, 8, 16, 32, (1400,), 3),
+    (4, 2, 32, 64, (1800, 900), 4),
+    (1, 4, 16, 128, (900,), 2),
+])
+def test_fused_demotion_matches_oscar_demote(n_kv, gqa, ps, group, seq, S):
+    """The per-step demotion done by the decode launch writes the bytes oscar_demote writes, and
+    leaves that step's partials unchanged."""
+    case = sc.make_case(n_kv=n_kv, gqa=gqa, page_size=ps, group=group, seq=seq)
+    sc.upload(case)
+    L, dev = case.layout, case.dev
+    B = len(seq)
+    pos = dev["hist_end"].clone()                      # the token that left the recent window
+    before = _pool_bytes(dev["int2"])
+    # reference: oscar_demote of the same positions
+    ob.oscar_demote(L, dev["bf16"], dev["bf16_table"], dev["int2"], dev["int2_table"],
+                    torch.arange(B, dtype=torch.int32, device="cuda"), pos, dev["RK"], dev["RV"],
+                    oracle.C_K, oracle.C_V)
+    torch.cuda.synchronize()
+    want = _pool_bytes(dev["int2"])
+    for t, b0 in zip((dev["int2"].codes_k, dev["int2"].codes_v, dev["int2"].scale_k, dev["int2"].zero_k,
+                      dev["int2"].scale_v, dev["int2"].zero_v), before):
+        t.copy_(b0)
+    ref = ob.Partials.empty(L, B, S)
+    ob.oscar_decode_attention_fused(L, dev["q"], dev["RK"], dev["bf16"], dev["bf16_table"], dev["int2"],
+                                    dev["int2_table"], dev["seq_len"], dev["hist_end"], case.sm_scale, ref)
+    torch.cuda.synchronize()
+    assert all(torch.equal(a, b) for a, b in zip(_pool_bytes(dev["int2"]), before))
+    part = ob.Partials.empty(L, B, S)
+    ob.oscar_decode_attention_fused(L, dev["q"], dev["RK"], dev["bf16"], dev["bf16_table"], dev["int2"],
+                                    dev["int2_table"], dev["seq_len"], dev["hist_end"], case.sm_scale, part,
+                                    demote_pos=pos, R_V=dev["RV"], c_K=oracle.C_K, c_V=oracle.C_V)
+    torch.cuda.synchronize()
+    assert all(torch.equal(a, b) for a, b in zip(_pool_bytes(dev["int2"]), want))
+    assert torch.equal(part.m, ref.m) and torch.equal(part.l, ref.l) and torch.equal(part.acc, ref.acc)
+    assert ob.oscar_get_device_status() == 0
+
+
+def test_fused_demotion_refuses_a_position_inside_the_history():
+    case = sc.make_case(n_kv=8, gqa=4, page_size=64, seq=(1500,))
+    sc.upload(case)
+    L, dev = case.layout, case.dev
+    before = _pool_bytes(dev["int2"])
+    pos = dev["hist_end"] - 10                          # still read from INT2 by this launch
+    part = ob.Partials.empty(L, 1, 2)
+    ob.oscar_decode_attention_fused(L, dev["q"], dev["RK"], dev["bf16"], dev["bf16_table"], dev["int2"],
+                                    dev["int2_table"], dev["seq_len"], dev["hist_end"], case.sm_scale, part,
+                                    demote_pos=pos, R_V=dev["RV"], c_K=oracle.C_K, c_V=oracle.C_V)
+    torch.cuda.synchronize()
+    assert ob.oscar_get_device_status() & 0x4
+    assert all(torch.equal(a, b) for a, b in zip(_pool_bytes(dev["int2"]), before))
+
+
 def test_fused_rotation_rejects_other_head_counts():
     case = sc.make_case(n_kv=3, gqa=2, page_size=16, seq=(400,))
     sc.upload(case)
@@ -337,6 +395,18 @@ def test_bf16_full_cache_parity():
                 exp.append(o)
     ok, r, m = sc.tolerance_ok(np.stack(got), np.stack(exp))
     assert ok, (r, m)
+
+
+def test_layouts_sharing_a_kernel_run_in_any_order():
+    """Layouts served by one kernel instance with different shared-memory sizes (4, 1 and 2 kv
+    heads at GQA 4): running a smaller one must not break a larger one run before it."""
+    cases = [sc.make_case(n_kv=h, gqa=4, page_size=16, seq=(700,)) for h in (4, 1, 2)]
+    for c in cases:
+        sc.upload(c)
+    for c in cases + cases[:1]:
+        out, out32, lse, _ = sc.run_decode(c, 3)
+        _check_outputs(c, out, out32, lse)
+    assert ob.oscar_get_device_status() == 0
 
 
 def test_bad_page_id_is_flagged_not_faulted():
