@@ -101,7 +101,7 @@ def lib():
     L.oscar_version.restype = ctypes.c_char_p
     L.oscar_decode_attention_fused.argtypes = [P(LayoutC), vp, vp, P(Bf16PoolC), vp, P(Int2PoolC), vp, i32, vp,
                                                vp, i32, ctypes.c_float, P(PartialsC), vp, vp, ctypes.c_float,
-                                               ctypes.c_float, vp]
+                                               ctypes.c_float, vp, vp, vp, vp, vp]
     L.oscar_decode_attention_fused.restype = st
     L.oscar_set_launch_overlap.argtypes = [i32]
     L.oscar_set_launch_overlap.restype = st
@@ -264,15 +264,21 @@ def oscar_decode_attention_fused(layout: Layout, q: torch.Tensor, R_K: torch.Ten
                                  bf16_page_table: torch.Tensor, int2_pool: Int2Pool, int2_page_table: torch.Tensor,
                                  seq_len: torch.Tensor, hist_end: torch.Tensor, sm_scale: float, partials: Partials,
                                  demote_pos: Optional[torch.Tensor] = None, R_V: Optional[torch.Tensor] = None,
-                                 c_K: float = 0.0, c_V: float = 0.0, stream=None):
+                                 c_K: float = 0.0, c_V: float = 0.0, out: Optional[torch.Tensor] = None,
+                                 out_f32: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                                 merge_counters: Optional[torch.Tensor] = None, stream=None):
     """oscar_decode_attention with q . R_K computed inside the launch (same partials bits); with
-    demote_pos ([batch] int32, -1 = none) also the per-step demotion of those positions."""
+    demote_pos ([batch] int32, -1 = none) also the per-step demotion of those positions; with
+    out / out_f32 also oscar_merge's output (inside the launch when merge_counters, int32 zeros
+    [batch], is given)."""
     _check("oscar_decode_attention_fused", lib().oscar_decode_attention_fused(
         ctypes.byref(layout.c()), _ptr(q), _ptr(R_K), ctypes.byref(bf16_pool.c()), _ptr(bf16_page_table),
         ctypes.byref(int2_pool.c()), _ptr(int2_page_table), int(int2_page_table.shape[-1]), _ptr(seq_len),
         _ptr(hist_end), int(q.shape[0]), float(sm_scale), ctypes.byref(partials.c()),
         _ptr(demote_pos) if demote_pos is not None else None, _ptr(R_V) if R_V is not None else None,
-        float(c_K), float(c_V), _stream(stream)))
+        float(c_K), float(c_V), _ptr(out) if out is not None else None,
+        _ptr(out_f32) if out_f32 is not None else None, _ptr(lse) if lse is not None else None,
+        _ptr(merge_counters) if merge_counters is not None else None, _stream(stream)))
 
 
 def oscar_decode_attention_history(layout: Layout, q_rot: torch.Tensor, int2_pool: Int2Pool,

@@ -265,7 +265,8 @@ oscar_status_t oscar_decode_attention_fused(const oscar_layout_t *layout, const 
                                             int32_t max_pages_per_req, const int32_t *seq_len,
                                             const int32_t *hist_end, int32_t batch, float sm_scale,
                                             const oscar_partials_t *partials, const int32_t *demote_pos,
-                                            const float *R_V, float c_K, float c_V, void *stream) {
+                                            const float *R_V, float c_K, float c_V, uint16_t *out,
+                                            float *out_f32, float *lse, int32_t *merge_counters, void *stream) {
     TRY(check_layout(layout));
     TRY(check_bf16_pool(bf16_pool));
     TRY(check_int2_pool(int2_pool));
@@ -289,11 +290,21 @@ oscar_status_t oscar_decode_attention_fused(const oscar_layout_t *layout, const 
         dem.dst = {int2_pool->codes_k, int2_pool->codes_v, int2_pool->scale_k, int2_pool->zero_k,
                    int2_pool->scale_v, int2_pool->zero_v, int2_pool->n_pages};
     }
-    return cuda_status(oscar::launch_decode_mma_demote(*layout, R_K, int2_view(int2_pool), int2_page_table, q,
-                                                       bf16_view(bf16_pool), bf16_page_table, max_pages_per_req,
-                                                       seq_len, hist_end, batch, sm_scale, part_view(partials),
-                                                       status_ptr(), dem, (cudaStream_t)stream),
-                       "fused decode attention launch");
+    const bool merge = out || out_f32;
+    if (merge && (!R_V || !aligned16(R_V))) return fail(OSCAR_ERR_INVALID_ARG, "the merge needs a 16-byte aligned R_V");
+    oscar::FusedMerge mg{merge_counters, R_V, out, out_f32, lse};
+    bool merged = false;
+    cudaError_t e = oscar::launch_decode_mma_demote(*layout, R_K, int2_view(int2_pool), int2_page_table, q,
+                                                    bf16_view(bf16_pool), bf16_page_table, max_pages_per_req,
+                                                    seq_len, hist_end, batch, sm_scale, part_view(partials),
+                                                    status_ptr(), dem, merge && merge_counters ? &mg : nullptr,
+                                                    &merged, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_status(e, "fused decode attention launch");
+    if (merge && !merged)                       // no counters, or the layout's stages cannot hold the merge
+        return cuda_status(oscar::launch_merge(*layout, part_view(partials), R_V, batch, out, out_f32, lse,
+                                               (cudaStream_t)stream),
+                           "oscar_merge launch");
+    return OSCAR_OK;
 }
 
 oscar_status_t oscar_decode_attention_history(const oscar_layout_t *layout, const float *q_rot,

@@ -157,10 +157,20 @@ struct FusedDemotion {
     float cK, cV;
     Int2PoolMut dst;
 };
+// Merge done by the last cluster of each request (fused launch).  counters: int32 [batch],
+// zero before the launch and left zero.  *merged tells whether the launch merged (the stage area
+// of small layouts cannot hold the merge's scratch: then the caller runs the merge).
+struct FusedMerge {
+    int32_t *counters;
+    const float *RV;
+    uint16_t *out;
+    float *out_f32, *lse;
+};
 cudaError_t launch_decode_mma_demote(const oscar_layout_t &L, const float *RK, Int2PoolView pool, const int32_t *pt,
                                      const uint16_t *q, Bf16PoolView bpool, const int32_t *bpt, int max_pages,
                                      const int32_t *seq_len, const int32_t *hist_end, int batch, float sm_scale,
-                                     PartialsView out, int32_t *status, const FusedDemotion &dem, cudaStream_t st);
+                                     PartialsView out, int32_t *status, const FusedDemotion &dem,
+                                     const FusedMerge *mg, bool *merged, cudaStream_t st);
 
 // Tensor-core BF16 kernel (mode 0 any n_kv_heads; mode 1 n_kv_heads in {1, 2, 4, 8}).
 bool bf16_mma_supported(const oscar_layout_t &L, int mode);

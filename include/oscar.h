@@ -245,8 +245,15 @@ OSCAR_API oscar_status_t oscar_decode_attention(const oscar_layout_t *layout,
  * c_K, V with R_V and c_V, exactly as oscar_demote would (same arithmetic, same
  * bytes), by the CTAs that compute the BF16 window.  The position must be at or
  * after hist_end[b] and before seq_len[b] (this launch still reads it from BF16);
- * otherwise it is skipped and OSCAR_DEV_BAD_LENGTH is set.  demote_pos NULL: R_V,
- * c_K, c_V are ignored.
+ * otherwise it is skipped and OSCAR_DEV_BAD_LENGTH is set.  demote_pos NULL: c_K,
+ * c_V are ignored.
+ *
+ * Optional merge: with out or out_f32 non-NULL the call also produces oscar_merge's
+ * output (same bits; R_V required, lse optional).  With merge_counters (int32
+ * [batch], all zero; the call leaves them zero) the cluster of each request that
+ * finishes last merges it inside the same launch; without them, or when the
+ * layout's stage buffers cannot hold the merge's scratch, oscar_merge runs as a
+ * second launch.  Calls that may run concurrently must not share merge_counters.
  */
 OSCAR_API oscar_status_t oscar_decode_attention_fused(const oscar_layout_t *layout, const uint16_t *q,
                                                       const float *R_K, const oscar_bf16_pool_t *bf16_pool,
@@ -257,7 +264,8 @@ OSCAR_API oscar_status_t oscar_decode_attention_fused(const oscar_layout_t *layo
                                                       int32_t batch, float sm_scale,
                                                       const oscar_partials_t *partials,
                                                       const int32_t *demote_pos, const float *R_V, float c_K,
-                                                      float c_V, void *stream);
+                                                      float c_V, uint16_t *out, float *out_f32, float *lse,
+                                                      int32_t *merge_counters, void *stream);
 
 /*
  * The two halves of oscar_decode_attention, for callers that run them on two

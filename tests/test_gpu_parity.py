@@ -345,6 +345,61 @@ def test_fused_demotion_matches_oscar_demote(n_kv, gqa, ps, group, seq, S):
     assert ob.oscar_get_device_status() == 0
 
 
+@pytest.mark.parametrize("n_kv,gqa,ps,group,seq,S", [
+    (8, 4, 64, 128, (3000, 1700), 6),     # the benchmark's shape
+    (8, 8, 16, 32, (1400,), 3),            # GQA 8, group 32
+    (4, 2, 32, 64, (1800, 900), 4),
+    (2, 4, 16, 128, (1200, 300), 3),        # a request with no history
+    (1, 1, 16, 128, (700,), 2),             # too small a stage area: the merge runs as its own launch
+])
+def test_fused_merge_matches_oscar_merge(n_kv, gqa, ps, group, seq, S):
+    """The merge done by the last cluster of each request inside the decode launch gives
+    oscar_merge's bits (out, out_f32, lse), leaves the counters at zero, and repeated or
+    graph-captured calls with launch overlap agree."""
+    case = sc.make_case(n_kv=n_kv, gqa=gqa, page_size=ps, group=group, seq=seq)
+    sc.upload(case)
+    L, dev = case.layout, case.dev
+    B, Hq = len(seq), L.n_q_heads
+    part = ob.Partials.empty(L, B, S)
+    ob.oscar_decode_attention_fused(L, dev["q"], dev["RK"], dev["bf16"], dev["bf16_table"], dev["int2"],
+                                    dev["int2_table"], dev["seq_len"], dev["hist_end"], case.sm_scale, part)
+    ref = [torch.empty((B, Hq, D), dtype=t, device="cuda") for t in (torch.bfloat16, torch.float32)]
+    ref_lse = torch.empty((B, Hq), dtype=torch.float32, device="cuda")
+    ob.oscar_merge(L, part, dev["RV"], ref[0], ref[1], ref_lse)
+    counters = torch.zeros(B, dtype=torch.int32, device="cuda")
+
+    def fused(p2, outs):
+        ob.oscar_decode_attention_fused(L, dev["q"], dev["RK"], dev["bf16"], dev["bf16_table"], dev["int2"],
+                                        dev["int2_table"], dev["seq_len"], dev["hist_end"], case.sm_scale, p2,
+                                        R_V=dev["RV"], out=outs[0], out_f32=outs[1], lse=outs[2],
+                                        merge_counters=counters)
+
+    runs = []
+    for _ in range(3):
+        outs = (torch.full_like(ref[0], float("nan")), torch.full_like(ref[1], float("nan")),
+                torch.full_like(ref_lse, float("nan")))
+        fused(ob.Partials.empty(L, B, S), outs)
+        runs.append(outs)
+    try:
+        ob.oscar_set_launch_overlap(True)
+        outs_g = (torch.empty_like(ref[0]), torch.empty_like(ref[1]), torch.empty_like(ref_lse))
+        p_g = ob.Partials.empty(L, B, S)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fused(p_g, outs_g)
+            fused(p_g, outs_g)
+        g.replay()
+        g.replay()
+    finally:
+        ob.oscar_set_launch_overlap(False)
+    torch.cuda.synchronize()
+    runs.append(outs_g)
+    for o in runs:
+        assert torch.equal(o[0], ref[0]) and torch.equal(o[1], ref[1]) and torch.equal(o[2], ref_lse)
+    assert not counters.any()
+    assert ob.oscar_get_device_status() == 0
+
+
 def test_fused_demotion_refuses_a_position_inside_the_history():
     case = sc.make_case(n_kv=8, gqa=4, page_size=64, seq=(1500,))
     sc.upload(case)
