@@ -35,6 +35,7 @@ import oscar_synthetic as syn  # noqa: E402
 
 METRIC = "INT2-history decode-attn tokens/s and HBM GB/s (% of roofline) at 100K ctx"
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 D = 128
 
 
@@ -84,8 +85,8 @@ def measured_peaks() -> dict:
     if os.path.exists(p):
         with open(p) as f:
             d = json.load(f)
-        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
-    return {"hbm_gbs": FALLBACK_HBM_GBS, "source": "fallback"}
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": d.get("bf16_tflops"), "source": "measured"}
+    return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS, "source": "fallback"}
 
 
 def stored_traffic(kernel: str, workload: str):
@@ -98,17 +99,27 @@ def stored_traffic(kernel: str, workload: str):
     e = d.get(kernel, {}).get(workload)
     if not e:
         return None
-    if e.get("source_sha256") != source_hash():
+    if e.get("source_sha256") != source_hash(kernel):
         return None
     return e.get("bytes_per_launch")
 
 
-def source_hash() -> str:
+# the sources each measured kernel is compiled from (its translation unit and the headers it includes)
+KERNEL_SOURCES = {
+    "decode_attention": ["attn_int2_mma.cu", "oscar_internal.cuh", "ptx.cuh", "quant.cuh", "merge_math.cuh",
+                         "tma.cuh"],
+    "bulk_demotion": ["demote_tc.cu", "oscar_internal.cuh", "ptx.cuh", "tma.cuh"],
+}
+
+
+def source_hash(kernel: str) -> str:
+    """sha256 over the kernel's source files; a stored ncu figure counts only while it matches."""
     h = hashlib.sha256()
     cs = os.path.join(ROOT, "bit_kv_cache_oscar_gb300", "csrc")
-    for f in sorted(os.listdir(cs)):
+    for f in sorted(KERNEL_SOURCES[kernel]):
         with open(os.path.join(cs, f), "rb") as fh:
             h.update(f.encode() + fh.read())
+    h.update(open(os.path.join(ROOT, "include", "oscar.h"), "rb").read())
     return h.hexdigest()
 
 
@@ -241,11 +252,10 @@ class Model:
                 st_table[0, :n_log] = torch.arange(n_log, dtype=torch.int32, device=device)
                 start = w.sink if b == 0 else max(w.sink, w.shared_prefix)
                 stop = int(self.hist_end[b]) + (1 if self.demote else 0)
-                if stop > start:
-                    pos = torch.arange(start, stop, dtype=torch.int32, device=device)
-                    req = torch.zeros_like(pos)
-                    ob.oscar_demote(L, stage, st_table, i2, self.int2_table[b:b + 1].contiguous(), req, pos,
-                                    RK, RV, 0.96, 0.92)
+                if stop > start:   # the prefill's history, demoted on the tensor cores
+                    rng = torch.tensor([[start], [stop]], dtype=torch.int32, device=device)
+                    ob.oscar_demote_range(L, stage, st_table, i2, self.int2_table[b:b + 1].contiguous(), rng[0],
+                                          rng[1], RK, RV, 0.96, 0.92)
                 for lp in range(n_log):
                     pg = int(self.pages.bf16_table[b, lp])
                     if pg >= 0:
@@ -418,9 +428,14 @@ def run_reference(args, w, rank):
 
 
 def bulk_demotion(model, w, args, dist) -> dict:
-    """oscar_demote over one layer's whole history of request 0 ([sink, hist_end), every kv head,
-    K and V) from a BF16 staging pool into a scratch INT2 pool: rows/s and the fp32 FMA roofline
-    (each row-head is two 128x128 fp32 FMA chains; peak = SMs x 128 FP32 lanes x 2 x clock)."""
+    """Bulk demotion of one layer's whole history of request 0 ([sink, hist_end), every kv head,
+    K and V) from a BF16 staging pool into a scratch INT2 pool, the pool fill of a prefix hit.
+
+    oscar_demote_range (tensor cores): rows/s; the HBM roofline of its algorithmic bytes (per
+    row-head and K/V: the 256-byte bf16 row in, 32 bytes of codes and the bf16 scale/zero out);
+    the tensor-pipe rate of the MMAs it issues (x . R_hi + x . R_lo: 2 x 2 x 128 x 128 flops per
+    row-head and K/V) against the measured bf16 peak.  oscar_demote's CUDA-core fp32 chain over
+    the same rows is timed beside it."""
     import torch
     from bit_kv_cache_oscar_gb300 import binding as ob
     L, dev, ps = model.L, model.dev, w.page_size
@@ -435,24 +450,36 @@ def bulk_demotion(model, w, args, dist) -> dict:
     del k, v
     table = torch.arange(n_log, dtype=torch.int32, device=dev).view(1, n_log)
     i2 = ob.Int2Pool.empty(L, n_log, dev)
+    st = model.layers[0]
+    pb = torch.tensor([w.sink], dtype=torch.int32, device=dev)
+    pe = torch.tensor([he], dtype=torch.int32, device=dev)
+    reps = max(3, min(args.steps, 20))
+    g = capture(lambda: ob.oscar_demote_range(L, stage, table, i2, table, pb, pe, st["RK"], st["RV"], 0.96, 0.92))
+    tb = time_graph(g, reps, args.warmup, dist) / reps
     pos = torch.arange(w.sink, he, dtype=torch.int32, device=dev)
     req = torch.zeros_like(pos)
-    st = model.layers[0]
-    fn = lambda: ob.oscar_demote(L, stage, table, i2, table, req, pos, st["RK"], st["RV"], 0.96, 0.92)
-    g = capture(fn)
-    reps = max(3, min(args.steps, 20))
-    tb = time_graph(g, reps, args.warmup, dist) / reps
-    n_rh = int(pos.numel()) * w.n_kv_heads
-    flops = n_rh * 2 * 2 * D * D
-    props = torch.cuda.get_device_properties(dev)
-    clk_mhz = ClockSampler.max_sm_mhz(dev.index or 0) or 2070.0
-    peak = props.multi_processor_count * 128 * 2 * clk_mhz * 1e6 / 1e12
-    achieved = flops / tb / 1e12
+    gl = capture(lambda: ob.oscar_demote(L, stage, table, i2, table, req, pos, st["RK"], st["RV"], 0.96, 0.92))
+    tl = time_graph(gl, reps, args.warmup, dist) / reps
+    n_rh = (he - w.sink) * w.n_kv_heads
+    unit_bytes = 2 * (D * 2 + D // 4 + 2 * 2 * (D // w.group))   # K and V: bf16 row in; codes, scale, zero out
+    bytes_launch = n_rh * unit_bytes
+    peaks = measured_peaks()
+    achieved = bytes_launch / tb / 1e9
+    mma_tflops = n_rh * 2 * 2 * 2 * D * D / tb / 1e12
+    bf16_peak = peaks.get("bf16_tflops")
     del stage, i2
-    return {"rows": int(pos.numel()), "row_heads": n_rh, "ms": tb * 1e3, "row_heads_per_s": n_rh / tb,
-            "roofline": {"bound": "alu", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak,
-                         "peak_source": "derived: SMs x 128 fp32 lanes x 2 flops x max SM clock (no tensor cores)"}}
+    return {"rows": he - w.sink, "row_heads": n_rh, "ms": tb * 1e3, "row_heads_per_s": n_rh / tb,
+            "kernel": "oscar_demote_range (bulk_demote_kernel: TMA + tcgen05.mma into TMEM + register quantizer)",
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                         "frac": achieved / peaks["hbm_gbs"], "bytes_per_launch": bytes_launch,
+                         "bytes_per_row_head": unit_bytes,
+                         "traffic": stored_traffic("bulk_demotion", w.name),
+                         "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs copy bandwidth)"},
+            "tensor": {"achieved": mma_tflops, "unit": "TFLOP/s", "peak": bf16_peak,
+                       "frac": (mma_tflops / bf16_peak) if bf16_peak else None,
+                       "peak_source": "measured (MEASURED_PEAKS.json bf16_tflops, cuBLAS burst)"},
+            "cuda_core_fp32_chain": {"ms": tl * 1e3, "row_heads_per_s": n_rh / tl,
+                                     "kernel": "oscar_demote (demote_kernel)"}}
 
 
 # ------------------------------------------------------------------- main ----

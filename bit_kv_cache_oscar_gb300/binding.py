@@ -50,6 +50,7 @@ EXPORTS = [
     "oscar_bf16_decode_attention", "oscar_get_device_status", "oscar_last_error_string", "oscar_version",
     "oscar_decode_attention_noalloc", "oscar_decode_attention_history", "oscar_decode_attention_window",
     "oscar_set_launch_overlap", "oscar_get_launch_overlap", "oscar_decode_attention_fused",
+    "oscar_demote_range",
 ]
 
 
@@ -72,6 +73,9 @@ def lib():
     L.oscar_demote.argtypes = [P(LayoutC), P(Bf16PoolC), vp, P(Int2PoolC), vp, i32, i32, vp, vp, i32, vp, vp,
                                ctypes.c_float, ctypes.c_float, vp, vp]
     L.oscar_demote.restype = st
+    L.oscar_demote_range.argtypes = [P(LayoutC), P(Bf16PoolC), vp, P(Int2PoolC), vp, i32, i32, vp, vp, vp, vp,
+                                     ctypes.c_float, ctypes.c_float, vp, vp]
+    L.oscar_demote_range.restype = st
     L.oscar_quantize_rotated.argtypes = [P(LayoutC), vp, i32, ctypes.c_float, vp, vp, vp, vp]
     L.oscar_quantize_rotated.restype = st
     L.oscar_rotate_q.argtypes = [P(LayoutC), vp, vp, i32, vp, vp]
@@ -235,6 +239,21 @@ def oscar_demote(layout: Layout, src: Bf16Pool, bf16_page_table: torch.Tensor, d
         ctypes.byref(layout.c()), ctypes.byref(src.c()), _ptr(bf16_page_table), ctypes.byref(dst.c()),
         _ptr(int2_page_table), max_pages, batch, _ptr(req_idx), _ptr(positions), int(positions.numel()),
         _ptr(R_K), _ptr(R_V), float(c_K), float(c_V), _ptr(rotated_out), _stream(stream)))
+
+
+def oscar_demote_range(layout: Layout, src: Bf16Pool, bf16_page_table: torch.Tensor, dst: Int2Pool,
+                       int2_page_table: torch.Tensor, pos_begin: torch.Tensor, pos_end: torch.Tensor,
+                       R_K: torch.Tensor, R_V: torch.Tensor, c_K: float, c_V: float,
+                       rotated_out: Optional[torch.Tensor] = None, stream=None):
+    if bf16_page_table.shape != int2_page_table.shape:
+        raise OscarError("oscar_demote_range: both page tables must be [batch, max_pages]")
+    batch, max_pages = int2_page_table.shape
+    if pos_begin.numel() != batch or pos_end.numel() != batch:
+        raise OscarError("oscar_demote_range: pos_begin and pos_end need one entry per request")
+    _check("oscar_demote_range", lib().oscar_demote_range(
+        ctypes.byref(layout.c()), ctypes.byref(src.c()), _ptr(bf16_page_table), ctypes.byref(dst.c()),
+        _ptr(int2_page_table), max_pages, batch, _ptr(pos_begin), _ptr(pos_end), _ptr(R_K), _ptr(R_V),
+        float(c_K), float(c_V), _ptr(rotated_out), _stream(stream)))
 
 
 def oscar_quantize_rotated(layout: Layout, x_rot: torch.Tensor, clip: float, codes: torch.Tensor,

@@ -203,6 +203,32 @@ oscar_status_t oscar_demote(const oscar_layout_t *layout, const oscar_bf16_pool_
                        "oscar_demote launch");
 }
 
+oscar_status_t oscar_demote_range(const oscar_layout_t *layout, const oscar_bf16_pool_t *src,
+                                  const int32_t *bf16_page_table, const oscar_int2_pool_t *dst,
+                                  const int32_t *int2_page_table, int32_t max_pages_per_req, int32_t batch,
+                                  const int32_t *pos_begin, const int32_t *pos_end, const float *R_K,
+                                  const float *R_V, float c_K, float c_V, float *rotated_out, void *stream) {
+    TRY(check_layout(layout));
+    TRY(check_bf16_pool(src));
+    TRY(check_int2_pool(dst));
+    if (batch < 0 || batch > 65535) return fail(OSCAR_ERR_INVALID_ARG, "batch %d outside 0..65535", batch);
+    if (batch == 0) return OSCAR_OK;
+    if (!bf16_page_table || !int2_page_table || !pos_begin || !pos_end || !R_K || !R_V)
+        return fail(OSCAR_ERR_INVALID_ARG, "NULL page table, range or rotation");
+    if (max_pages_per_req < 1) return fail(OSCAR_ERR_INVALID_ARG, "max_pages_per_req %d < 1", max_pages_per_req);
+    if (!(c_K > 0.0f) || !(c_V > 0.0f)) return fail(OSCAR_ERR_INVALID_ARG, "clip ratios must be > 0");
+    if (!aligned16(src->k) || !aligned16(src->v) || !aligned16(dst->codes_k) || !aligned16(dst->codes_v) ||
+        !aligned16(rotated_out))
+        return fail(OSCAR_ERR_INVALID_ARG, "pool arrays and rotated_out must be 16-byte aligned");
+    if (!oscar::demote_range_supported(*layout))
+        return fail(OSCAR_ERR_UNSUPPORTED, "page_size %d neither divides nor is a multiple of 128",
+                    layout->page_size);
+    return cuda_status(oscar::launch_demote_range(*layout, bf16_view(src), bf16_page_table, *dst, int2_page_table,
+                                                  max_pages_per_req, batch, pos_begin, pos_end, R_K, R_V, c_K, c_V,
+                                                  rotated_out, status_ptr(), (cudaStream_t)stream),
+                       "oscar_demote_range launch");
+}
+
 oscar_status_t oscar_quantize_rotated(const oscar_layout_t *layout, const float *x_rot, int32_t n, float clip,
                                       uint8_t *codes, uint16_t *scale, uint16_t *zero, void *stream) {
     TRY(check_layout(layout));

@@ -34,6 +34,7 @@
 #include "ptx.cuh"
 #include "quant.cuh"
 #include "merge_math.cuh"
+#include "tma.cuh"
 
 namespace oscar {
 namespace {
@@ -616,8 +617,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
     if (s < 0) {                               // a BF16 window CTA (uniform over the cluster)
         if (a.mcount && threadIdx.x == 0)      // R_V of this CTA's kv heads into L2 for the merge
             for (int k = blockIdx.x; k < Hkv; k += a.win_ctas)
-                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(a.RVm + (size_t)k * kHeadDim * kHeadDim),
-                             "r"(kHeadDim * kHeadDim * 4) : "memory");
+                prefetch_l2(a.RVm + (size_t)k * kHeadDim * kHeadDim, kHeadDim * kHeadDim * 4);
         pdl_wait();                            // q and the partials belong to the previous kernels
         window_cta<G>(a, reinterpret_cast<float *>(stage0 + a.win_off), reinterpret_cast<float *>(stage0 + a.res_off),
                       T, he, b, (int)blockIdx.x, a.win_ctas);
@@ -1306,25 +1306,6 @@ int mma_cluster_size(const oscar_layout_t &L, int *active) {
     const void *kern = L.n_kv_heads == 8 ? reinterpret_cast<const void *>(int2_mma_kernel<G, NGRP, true>)
                                          : reinterpret_cast<const void *>(int2_mma_kernel<G, NGRP, false>);
     return int2_cluster_size(kern, smem, kThreads, active);
-}
-
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
-                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
-                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-// cuTensorMapEncodeTiled from the driver, looked up once through the runtime.
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        EncodeTiledFn f = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            f = reinterpret_cast<EncodeTiledFn>(p);
-        cudaGetLastError();
-        return f;
-    }();
-    return fn;
 }
 
 // An INT2 codes array of 8 kv heads, [rows = n_pages * page_size][256 bytes], as a 2-D uint8 tensor

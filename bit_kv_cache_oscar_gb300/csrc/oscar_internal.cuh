@@ -123,6 +123,13 @@ cudaError_t launch_demote(const oscar_layout_t &L, Bf16PoolView src, const int32
                           const float *RV, float cK, float cV, float *rot_out, int32_t *status,
                           cudaStream_t st);
 
+// Tensor-core bulk demotion of position ranges (demote_tc.cu).
+bool demote_range_supported(const oscar_layout_t &L);
+cudaError_t launch_demote_range(const oscar_layout_t &L, Bf16PoolView src, const int32_t *bf16_pt,
+                                const oscar_int2_pool_t &dst, const int32_t *int2_pt, int max_pages, int batch,
+                                const int32_t *pos_begin, const int32_t *pos_end, const float *RK, const float *RV,
+                                float cK, float cV, float *rot_out, int32_t *status, cudaStream_t st);
+
 cudaError_t launch_quantize_rotated(const oscar_layout_t &L, const float *x, int n, float clip, uint8_t *codes,
                                     uint16_t *scale, uint16_t *zero, cudaStream_t st);
 

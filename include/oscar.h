@@ -182,6 +182,36 @@ OSCAR_API oscar_status_t oscar_demote(const oscar_layout_t *layout,
                             float *rotated_out, void *stream);
 
 /*
+ * Bulk demotion of position ranges on the tensor cores (the step that fills the
+ * INT2 history after prefill: [news] online path "rotate / clip / quantize /
+ * pack"; [notes] "核心要点" item 3).  For each request b, every position p in
+ * [pos_begin[b], pos_end[b]) is demoted as oscar_demote would, every kv head, K
+ * and V, with one difference: the rotation x · R runs on the tensor cores as
+ * x · R_hi + x · R_lo with R_hi = bf16(R), R_lo = bf16(R − R_hi) and fp32
+ * accumulation, so each rotated element lies within 2^-14 · ||x||_2 of the exact
+ * product (oscar_demote's fp32 chain lies closer); codes, scale and zero are the
+ * quantizer's output on these rotated rows, bit for bit.
+ *   pos_begin, pos_end  int32 [batch] device arrays; a range with
+ *                  pos_begin < 0, pos_end < pos_begin or pos_end beyond the page
+ *                  table is skipped and flagged (OSCAR_DEV_BAD_LENGTH); an empty
+ *                  range demotes nothing.
+ *   rotated_out    NULL or fp32 [int2 pool n_pages][page_size][2][n_kv_heads]
+ *                  [head_dim], indexed like the destination INT2 slot (index 0 =
+ *                  K, 1 = V): the rotated rows before quantization; slots not
+ *                  demoted are not written.
+ * Other arguments as for oscar_demote; both pools' arrays and rotated_out must
+ * be 16-byte aligned.  Positions that two requests map to the same INT2 slot
+ * race.
+ */
+OSCAR_API oscar_status_t oscar_demote_range(const oscar_layout_t *layout,
+                                  const oscar_bf16_pool_t *src, const int32_t *bf16_page_table,
+                                  const oscar_int2_pool_t *dst, const int32_t *int2_page_table,
+                                  int32_t max_pages_per_req, int32_t batch,
+                                  const int32_t *pos_begin, const int32_t *pos_end,
+                                  const float *R_K, const float *R_V, float c_K, float c_V,
+                                  float *rotated_out, void *stream);
+
+/*
  * The codec alone: quantize n fp32 rows x_rot [n][head_dim] that are already
  * rotated, with clip ratio `clip`, into codes [n][head_dim/4] and bf16
  * scale/zero [n][head_dim/group].  Bit-exact contract: given the same fp32
