@@ -86,13 +86,14 @@ struct TileWalk {
 // s != 0 and inv = 1/s rounded) as two 32-bit words, code i at bits 2i.
 // Per element: q' = clamp((y - z) * inv, 0, 3), rounded to an integer (ties to even) by adding
 // 1.5 * 2^23, whose low bits are then the code.  That is clamp(rint(q), 0, 3) of the correctly
-// rounded quotient q whenever q' lies more than 2^-18 from a half-integer (|q' - q| < 2^-21 there);
-// a chunk with any element closer is redone with the correctly rounded quotients.
-__device__ __forceinline__ void codes_chunk(const uint32_t (&v)[32], float z, float s, float inv, uint32_t &w0,
-                                            uint32_t &w1) {
+// rounded quotient q whenever q' lies more than 2^-18 from a half-integer (|q' - q| < 2^-21 there).
+// Returns the largest distance of a q' to its integer: at kFastMargin or above, the caller takes
+// the chunk again through codes_chunk_exact.
+__device__ __forceinline__ float codes_chunk(const uint32_t (&v)[32], float z, float inv, uint32_t &w0,
+                                             uint32_t &w1) {
     constexpr float kMagic = 12582912.0f;               // 1.5 * 2^23
     uint32_t w[2] = {0u, 0u};
-    float e4[4] = {0.0f, 0.0f, 0.0f, 0.0f};             // largest distance of a q' to its integer
+    float e4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
     for (int i = 0; i < 32; ++i) {
         const float d = __fsub_rn(__uint_as_float(v[i]), z);
@@ -101,14 +102,24 @@ __device__ __forceinline__ void codes_chunk(const uint32_t (&v)[32], float z, fl
         e4[i & 3] = fmaxf(e4[i & 3], fabsf(__fsub_rn(qc, __fsub_rn(y, kMagic))));
         w[i >> 4] |= (__float_as_uint(y) & 3u) << (2 * (i & 15));
     }
-    if (fmaxf(fmaxf(e4[0], e4[1]), fmaxf(e4[2], e4[3])) >= kFastMargin) {   // rare
-        w[0] = w[1] = 0u;
+    w0 = w[0];
+    w1 = w[1];
+    return fmaxf(fmaxf(e4[0], e4[1]), fmaxf(e4[2], e4[3]));
+}
+
+// The same codes from the correctly rounded quotients, the chunk read again from TMEM at taddr
+// (the whole warp calls it).  Kept out of line: it is rarely taken and long.
+__device__ __noinline__ void codes_chunk_exact(uint32_t taddr, float z, float s, uint32_t &w0, uint32_t &w1) {
+    __syncwarp();
+    uint32_t v[32];
+    tmem_ld32(taddr, v);
+    tmem_ld_wait();
+    uint32_t w[2] = {0u, 0u};
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-            const float r = rintf(__fdiv_rn(__fsub_rn(__uint_as_float(v[i]), z), s));
-            const uint32_t c = r >= 3.0f ? 3u : (r >= 0.0f ? (uint32_t)r : 0u);
-            w[i >> 4] |= c << (2 * (i & 15));
-        }
+    for (int i = 0; i < 32; ++i) {
+        const float r = rintf(__fdiv_rn(__fsub_rn(__uint_as_float(v[i]), z), s));
+        const uint32_t c = r >= 3.0f ? 3u : (r >= 0.0f ? (uint32_t)r : 0u);
+        w[i >> 4] |= c << (2 * (i & 15));
     }
     w0 = w[0];
     w1 = w[1];
@@ -182,40 +193,49 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
 
     if (warp == 0) {
         // ---------------------------------------------------------------- producer
-        if (lane == 0) {
-            const int ps = a.page_size;
-            const int rpl = ps < kTileRows ? ps : kTileRows;   // rows per copy: one page, or 128
-            TileWalk wk;
-            int b, t, lo, hi;
-            int n = 0;
-            for (int i = cta; wk.find(a, i, b, t, lo, hi); i += cpp, ++n) {
-                const int s = n % kStagesTC;
-                if (!mbar_wait(bar_empty + 8 * s, ((n / kStagesTC) & 1) ^ 1))
-                    flag_status(a.status, OSCAR_DEV_WAIT_TIMEOUT);
-                // pieces of rpl rows that meet [lo, hi) and whose page id is valid
-                uint32_t bytes = 0;
-                for (int j = 0; j < kTileRows / rpl; ++j) {
-                    const int p0 = t * kTileRows + j * rpl;
-                    if (p0 + rpl <= lo || p0 >= hi) continue;
-                    const int pg = a.bf16_pt[(size_t)b * a.max_pages + p0 / ps];
-                    if (pg < 0 || pg >= a.bf16_pages) {
-                        flag_status(a.status, OSCAR_DEV_BAD_BF16_PAGE);
-                        continue;
-                    }
-                    bytes += 2 * rpl * 128;
-                }
-                mbar_arrive_expect_tx(bar_full + 8 * s, bytes);
-                const uint32_t dst = sbase + kOffA + s * kStageBytes;
-                for (int j = 0; j < kTileRows / rpl; ++j) {
-                    const int p0 = t * kTileRows + j * rpl;
-                    if (p0 + rpl <= lo || p0 >= hi) continue;
-                    const int pg = a.bf16_pt[(size_t)b * a.max_pages + p0 / ps];
-                    if (pg < 0 || pg >= a.bf16_pages) continue;
-                    const int z = pg * ps + p0 % ps;
-                    tma_load_3d(dst + j * rpl * 128, tm, 0, head, z, bar_full + 8 * s);
-                    tma_load_3d(dst + kHalfBytes + j * rpl * 128, tm, 64, head, z, bar_full + 8 * s);
-                }
+        // Lane j copies piece j of the tile (rows of one page, or 128 rows); the page ids of the
+        // next tile are loaded while this one waits for its stage.
+        const int ps = a.page_size;
+        const int rpl = ps < kTileRows ? ps : kTileRows;        // rows per copy: one page, or 128
+        const int np = kTileRows / rpl;
+        // this lane's piece of tile t of request b: its tensor-map row, or -1 (none or outside the range)
+        auto piece_row = [&](int b, int t, int lo, int hi) -> int {
+            const int p0 = t * kTileRows + lane * rpl;
+            if (lane >= np || p0 + rpl <= lo || p0 >= hi) return -1;
+            const int pg = a.bf16_pt[(size_t)b * a.max_pages + p0 / ps];
+            if (pg < 0 || pg >= a.bf16_pages) {
+                flag_status(a.status, OSCAR_DEV_BAD_BF16_PAGE);
+                return -1;
             }
+            return pg * ps + p0 % ps;
+        };
+        TileWalk wk;
+        int b, t, lo, hi;
+        int i = cta;
+        bool have = wk.find(a, i, b, t, lo, hi);
+        int z = have ? piece_row(b, t, lo, hi) : -1;
+        for (int n = 0; have; ++n) {
+            int b2 = 0, t2 = 0, lo2 = 0, hi2 = 0;
+            const bool have2 = wk.find(a, i + cpp, b2, t2, lo2, hi2);
+            const int z2 = have2 ? piece_row(b2, t2, lo2, hi2) : -1;
+            const int s = n % kStagesTC;
+            if (!mbar_wait(bar_empty + 8 * s, ((n / kStagesTC) & 1) ^ 1) && lane == 0)
+                flag_status(a.status, OSCAR_DEV_WAIT_TIMEOUT);
+            const unsigned valid = __ballot_sync(0xffffffffu, z >= 0);
+            if (lane == 0) mbar_arrive_expect_tx(bar_full + 8 * s, (uint32_t)__popc(valid) * 2 * rpl * 128);
+            __syncwarp();
+            if (z >= 0) {
+                const uint32_t dst = sbase + kOffA + s * kStageBytes + lane * rpl * 128;
+                tma_load_3d(dst, tm, 0, head, z, bar_full + 8 * s);
+                tma_load_3d(dst + kHalfBytes, tm, 64, head, z, bar_full + 8 * s);
+            }
+            i += cpp;
+            have = have2;
+            b = b2;
+            t = t2;
+            lo = lo2;
+            hi = hi2;
+            z = z2;
         }
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
@@ -291,11 +311,11 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
                 gmn[g] = INFINITY;
                 gmx[g] = -INFINITY;
             }
-#pragma unroll
+            // (the chunk loops are not unrolled: unrolled, the epilogue outgrew the instruction cache)
+#pragma unroll 1
             for (int c = 0; c < 4; ++c) {
                 tmem_ld32(ta + 32 * c, v);
                 tmem_ld_wait();
-                constexpr int kPer = GROUP < 32 ? GROUP : 32;      // channels of one group in a chunk
                 float mn4[4], mx4[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) mn4[u] = mx4[u] = __uint_as_float(v[u]);
@@ -304,10 +324,14 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
                     mn4[k & 3] = fminf(mn4[k & 3], __uint_as_float(v[k]));
                     mx4[k & 3] = fmaxf(mx4[k & 3], __uint_as_float(v[k]));
                 }
-                static_assert(kPer == 32, "groups are whole chunks or several of them");
-                const int g = (32 * c) / GROUP;
-                gmn[g] = fminf(gmn[g], fminf(fminf(mn4[0], mn4[1]), fminf(mn4[2], mn4[3])));
-                gmx[g] = fmaxf(gmx[g], fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])));
+                const float cmn = fminf(fminf(mn4[0], mn4[1]), fminf(mn4[2], mn4[3]));
+                const float cmx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+#pragma unroll
+                for (int g = 0; g < kGroups; ++g)
+                    if (g == (32 * c) / GROUP) {
+                        gmn[g] = fminf(gmn[g], cmn);
+                        gmx[g] = fmaxf(gmx[g], cmx);
+                    }
                 if (a.rot_out && ok) {
                     float4 *o = reinterpret_cast<float4 *>(a.rot_out + ((slot_row * 2 + kind) * a.n_kv + head) * kHeadDim) + 8 * c;
 #pragma unroll
@@ -332,15 +356,36 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
             }
             uint32_t w[8];
 #pragma unroll
+            for (int k = 0; k < 8; ++k) w[k] = 0u;
+#pragma unroll 1
             for (int c = 0; c < 4; ++c) {
+                float z = zf[0], sc = sf[0], iv = inv[0];
+#pragma unroll
+                for (int g = 1; g < kGroups; ++g)
+                    if (g == (32 * c) / GROUP) {
+                        z = zf[g];
+                        sc = sf[g];
+                        iv = inv[g];
+                    }
                 tmem_ld32(ta + 32 * c, v);
                 tmem_ld_wait();
-                const int g = (32 * c) / GROUP;
-                if (sf[g] != 0.0f) {
-                    codes_chunk(v, zf[g], sf[g], inv[g], w[2 * c], w[2 * c + 1]);
-                } else {
-                    w[2 * c] = w[2 * c + 1] = 0u;                // degenerate group: code 0
+                uint32_t w0 = 0u, w1 = 0u;                       // a degenerate group (scale 0): code 0
+                float e = 0.0f;
+                if (sc != 0.0f) e = codes_chunk(v, z, iv, w0, w1);
+                if (__any_sync(0xffffffffu, e >= kFastMargin)) {   // rare: exact quotients (whole warp)
+                    uint32_t x0, x1;
+                    codes_chunk_exact(ta + 32 * c, z, sc != 0.0f ? sc : 1.0f, x0, x1);
+                    if (e >= kFastMargin) {
+                        w0 = x0;
+                        w1 = x1;
+                    }
                 }
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    if (k == c) {
+                        w[2 * k] = w0;
+                        w[2 * k + 1] = w1;
+                    }
             }
             tc_fence_before();
             mbar_arrive(bar_acce + 8 * eg);        // the MMA may overwrite the accumulator
