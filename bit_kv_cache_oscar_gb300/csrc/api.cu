@@ -191,8 +191,8 @@ oscar_status_t oscar_demote(const oscar_layout_t *layout, const oscar_bf16_pool_
     TRY(check_int2_pool(dst));
     if (n < 0 || n > 65535 * 256) return fail(OSCAR_ERR_INVALID_ARG, "n %d outside 0..%d", n, 65535 * 256);
     if (n == 0) return OSCAR_OK;
-    if (!bf16_page_table || !int2_page_table || !req_idx || !positions || !R_K || !R_V)
-        return fail(OSCAR_ERR_INVALID_ARG, "NULL page table, index or rotation");
+    if (!bf16_page_table || !int2_page_table || !req_idx || !positions || !R_K)
+        return fail(OSCAR_ERR_INVALID_ARG, "NULL page table, index or R_K");
     if (max_pages_per_req < 1) return fail(OSCAR_ERR_INVALID_ARG, "max_pages_per_req %d < 1", max_pages_per_req);
     if (batch < 1) return fail(OSCAR_ERR_INVALID_ARG, "batch %d < 1", batch);
     if (!aligned16(R_K) || !aligned16(R_V)) return fail(OSCAR_ERR_INVALID_ARG, "R_K/R_V not 16-byte aligned");
@@ -213,8 +213,8 @@ oscar_status_t oscar_demote_range(const oscar_layout_t *layout, const oscar_bf16
     TRY(check_int2_pool(dst));
     if (batch < 0 || batch > 65535) return fail(OSCAR_ERR_INVALID_ARG, "batch %d outside 0..65535", batch);
     if (batch == 0) return OSCAR_OK;
-    if (!bf16_page_table || !int2_page_table || !pos_begin || !pos_end || !R_K || !R_V)
-        return fail(OSCAR_ERR_INVALID_ARG, "NULL page table, range or rotation");
+    if (!bf16_page_table || !int2_page_table || !pos_begin || !pos_end || !R_K)
+        return fail(OSCAR_ERR_INVALID_ARG, "NULL page table, range or R_K");
     if (max_pages_per_req < 1) return fail(OSCAR_ERR_INVALID_ARG, "max_pages_per_req %d < 1", max_pages_per_req);
     if (!(c_K > 0.0f) || !(c_V > 0.0f)) return fail(OSCAR_ERR_INVALID_ARG, "clip ratios must be > 0");
     if (!aligned16(src->k) || !aligned16(src->v) || !aligned16(dst->codes_k) || !aligned16(dst->codes_v) ||
@@ -307,8 +307,8 @@ oscar_status_t oscar_decode_attention_fused(const oscar_layout_t *layout, const 
         return fail(OSCAR_ERR_UNSUPPORTED, "fused rotation needs 1, 2, 4 or 8 kv heads; use oscar_rotate_q + "
                                            "oscar_decode_attention");
     oscar::FusedDemotion dem{};
+    if (!aligned16(R_V)) return fail(OSCAR_ERR_INVALID_ARG, "R_V not 16-byte aligned");
     if (demote_pos) {
-        if (!R_V || !aligned16(R_V)) return fail(OSCAR_ERR_INVALID_ARG, "demotion needs a 16-byte aligned R_V");
         dem.dem_pos = demote_pos;
         dem.RV = R_V;
         dem.cK = c_K;
@@ -317,8 +317,8 @@ oscar_status_t oscar_decode_attention_fused(const oscar_layout_t *layout, const 
                    int2_pool->scale_v, int2_pool->zero_v, int2_pool->n_pages};
     }
     const bool merge = out || out_f32;
-    if (merge && (!R_V || !aligned16(R_V))) return fail(OSCAR_ERR_INVALID_ARG, "the merge needs a 16-byte aligned R_V");
     oscar::FusedMerge mg{merge_counters, R_V, out, out_f32, lse};
+    if (!R_V) merge_counters = nullptr;          // the in-launch merge rotates back: oscar_merge runs
     bool merged = false;
     cudaError_t e = oscar::launch_decode_mma_demote(*layout, R_K, int2_view(int2_pool), int2_page_table, q,
                                                     bf16_view(bf16_pool), bf16_page_table, max_pages_per_req,

@@ -371,8 +371,9 @@ __device__ void window_cta(const MmaArgs &a, float *wsm, float *res, int T, int 
 // ---- Per-step demotion by the window CTAs: request b's position dem_pos[b] (one that left the
 // recent window; this launch still reads it from BF16) is rotated by R_K / R_V, clipped,
 // quantized and packed into the INT2 pool for kv heads wr, wr + wc, ...  The arithmetic is
-// oscar_demote's: y_j = fma-chain_i x_i * R[i][j] (i ascending, fp32), then the shared
-// quantizer.  R is staged through the stage area a chunk at a time.  All threads call this.
+// oscar_demote's: y_j = fma-chain_i x_i * R[i][j] (i ascending, fp32), or y = x for values when
+// R_V is NULL, then the shared quantizer.  R is staged through the stage area a chunk at a time.
+// All threads call this.
 __device__ void window_demote(const MmaArgs &a, float *small, uint8_t *area, int T, int he, int b, int wr, int wc) {
     const int tid = threadIdx.x;
     const int Hkv = a.n_kv, ps = a.page_size;
@@ -405,11 +406,16 @@ __device__ void window_demote(const MmaArgs &a, float *small, uint8_t *area, int
     int n = 0;                                   // bulk copies so far (phase parity)
     for (int hk = wr; hk < Hkv; hk += wc) {
         for (int which = 0; which < 2; ++which) {
-            const float *R = (which ? a.dem.RV : a.RK) + (size_t)hk * kHeadDim * kHeadDim;
+            const float *Rb = which ? a.dem.RV : a.RK;       // NULL R_V: values stored as they are
+            const float *R = Rb ? Rb + (size_t)hk * kHeadDim * kHeadDim : nullptr;
             __syncthreads();                     // the previous row's xs and Rs are consumed
             if (tid < kHeadDim) xs[tid] = bf16_to_f32((which ? a.bpool.v : a.bpool.k)[(srow + hk) * kHeadDim + tid]);
             float y = 0.f;
-            for (int c = 0; c < nch; ++c, ++n) {
+            if (!R) {
+                __syncthreads();
+                if (tid < kHeadDim) y = xs[tid];
+            }
+            for (int c = 0; c < (R ? nch : 0); ++c, ++n) {
                 if (c > 0) __syncthreads();
                 if (tid == 0) {                  // one bulk copy of the chunk (rows c*rpc ...)
                     fence_proxy_async_smem();    // the area held the window's generic stores

@@ -60,7 +60,8 @@ __global__ void __launch_bounds__(kThreads) demote_kernel(DemoteArgs a) {
 
     const int h = blockIdx.x >> 1, which = blockIdx.x & 1;
     const int j = threadIdx.x;
-    const float *R = (which ? a.RV : a.RK) + (size_t)h * kHeadDim * kHeadDim;
+    const float *Rb = which ? a.RV : a.RK;               // NULL R_V: values stored as they are
+    const float *R = Rb ? Rb + (size_t)h * kHeadDim * kHeadDim : nullptr;
     const float clip = which ? a.cV : a.cK;
     const uint16_t *src = which ? a.src.v : a.src.k;
     uint8_t *codes = which ? a.codes_v : a.codes_k;
@@ -69,14 +70,14 @@ __global__ void __launch_bounds__(kThreads) demote_kernel(DemoteArgs a) {
     const int gpr = kHeadDim / a.group;                 // groups per row
 
     // R (64 KB) in one bulk copy: a loop of vector loads waits for each batch in turn
-    if (j == 0) {
+    if (R && j == 0) {
         mbar_init(saddr(&rbar), 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         mbar_arrive_expect_tx(saddr(&rbar), kHeadDim * kHeadDim * 4);
         tma_load_1d(saddr(Rs), R, kHeadDim * kHeadDim * 4, saddr(&rbar));
     }
     __syncthreads();
-    if (!mbar_wait(saddr(&rbar), 0) && j == 0) flag_status(a.status, OSCAR_DEV_WAIT_TIMEOUT);
+    if (R && !mbar_wait(saddr(&rbar), 0) && j == 0) flag_status(a.status, OSCAR_DEV_WAIT_TIMEOUT);
 
     const int i0 = blockIdx.y * kTokPerCta;
     const int i1 = min(a.n, i0 + kTokPerCta);
@@ -111,9 +112,9 @@ __global__ void __launch_bounds__(kThreads) demote_kernel(DemoteArgs a) {
 
         float acc[kTokPerPass];
 #pragma unroll
-        for (int t = 0; t < kTokPerPass; ++t) acc[t] = 0.0f;
+        for (int t = 0; t < kTokPerPass; ++t) acc[t] = R ? 0.0f : xs[t * kHeadDim + j];
 #pragma unroll 4
-        for (int i = 0; i < kHeadDim; i += 4) {
+        for (int i = 0; i < (R ? kHeadDim : 0); i += 4) {
             const float r0 = Rs[(i + 0) * kHeadDim + j], r1 = Rs[(i + 1) * kHeadDim + j];
             const float r2 = Rs[(i + 2) * kHeadDim + j], r3 = Rs[(i + 3) * kHeadDim + j];
 #pragma unroll

@@ -141,7 +141,8 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
     const int pairs = 2 * a.n_kv;
     const int pair = blockIdx.x % pairs, cta = blockIdx.x / pairs;
     const int kind = pair / a.n_kv, head = pair % a.n_kv;   // kind 0 = K, 1 = V
-    const float *R = (kind ? a.RV : a.RK) + (size_t)head * kHeadDim * kHeadDim;
+    const float *Rb = kind ? a.RV : a.RK;                   // NULL R_V: values stored as they are (R = I)
+    const float *R = Rb ? Rb + (size_t)head * kHeadDim * kHeadDim : nullptr;
     const CUtensorMap *tm = kind ? &tmv : &tmk;
     const int cpp = a.ctas_per_pair;
 
@@ -174,7 +175,8 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
         uint32_t hv[4], lv[4];
 #pragma unroll
         for (int u = 0; u < 8; u += 2) {
-            const float r0 = R[(k + u) * kHeadDim + n], r1 = R[(k + u + 1) * kHeadDim + n];
+            const float r0 = R ? R[(k + u) * kHeadDim + n] : (k + u == n ? 1.0f : 0.0f);
+            const float r1 = R ? R[(k + u + 1) * kHeadDim + n] : (k + u + 1 == n ? 1.0f : 0.0f);
             const uint16_t h0 = f32_to_bf16_rn(r0), h1 = f32_to_bf16_rn(r1);
             const uint16_t l0 = f32_to_bf16_rn(__fsub_rn(r0, bf16_to_f32(h0)));
             const uint16_t l1 = f32_to_bf16_rn(__fsub_rn(r1, bf16_to_f32(h1)));

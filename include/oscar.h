@@ -163,6 +163,11 @@ OSCAR_API int32_t oscar_suggest_splits(const oscar_layout_t *layout, int32_t bat
  * pool at (int2_page_table[b·max_pages_per_req + p/ps], p % ps, h); the value
  * row likewise with R_V[h] and c_V.
  *   R_K, R_V       fp32 [n_kv_heads][head_dim][head_dim], row-major R[i][j].
+ *                  R_V may be NULL when the value rotation is folded into the
+ *                  model's projections ([notes] "核心要点" item 3: the value
+ *                  rotation can be absorbed into the projection weights): the
+ *                  values then arrive already rotated and are quantized as
+ *                  stored (y = x; merge them with oscar_merge(R_V = NULL)).
  *   batch          rows of both page tables ([batch][max_pages_per_req]).
  *   req_idx, positions  int32 [n] device arrays; an entry with req_idx outside
  *                  [0, batch) or a position outside the page table is skipped
@@ -199,7 +204,8 @@ OSCAR_API oscar_status_t oscar_demote(const oscar_layout_t *layout,
  *                  [head_dim], indexed like the destination INT2 slot (index 0 =
  *                  K, 1 = V): the rotated rows before quantization; slots not
  *                  demoted are not written.
- * Other arguments as for oscar_demote; both pools' arrays and rotated_out must
+ * Other arguments as for oscar_demote (R_V may be NULL: values stored as they
+ * are, exactly); both pools' arrays and rotated_out must
  * be 16-byte aligned.  Positions that two requests map to the same INT2 slot
  * race.
  */
@@ -278,12 +284,15 @@ OSCAR_API oscar_status_t oscar_decode_attention(const oscar_layout_t *layout,
  * otherwise it is skipped and OSCAR_DEV_BAD_LENGTH is set.  demote_pos NULL: c_K,
  * c_V are ignored.
  *
+ * R_V NULL (the value rotation folded into the projections): the demotion
+ * stores values as they are and the merge does not rotate back.
+ *
  * Optional merge: with out or out_f32 non-NULL the call also produces oscar_merge's
- * output (same bits; R_V required, lse optional).  With merge_counters (int32
+ * output (same bits; lse optional).  With merge_counters (int32
  * [batch], all zero; the call leaves them zero) the cluster of each request that
- * finishes last merges it inside the same launch; without them, or when the
- * layout's stage buffers cannot hold the merge's scratch, oscar_merge runs as a
- * second launch.  Calls that may run concurrently must not share merge_counters.
+ * finishes last merges it inside the same launch; without them, with R_V NULL, or
+ * when the layout's stage buffers cannot hold the merge's scratch, oscar_merge
+ * runs as a second launch.  Calls that may run concurrently must not share merge_counters.
  */
 OSCAR_API oscar_status_t oscar_decode_attention_fused(const oscar_layout_t *layout, const uint16_t *q,
                                                       const float *R_K, const oscar_bf16_pool_t *bf16_pool,
@@ -328,8 +337,9 @@ OSCAR_API oscar_status_t oscar_decode_attention_window(const oscar_layout_t *lay
  *   A'_j = fma-chain over i of A_i·R_V[j][i]; then slot S with w_S; o = A'/L,
  * with 2^x computed by Cody–Waite reduction and a degree-7 Taylor polynomial
  * (not the hardware approximation).
- *   R_V  fp32 [n_kv_heads][head_dim][head_dim], or NULL for an all-BF16
- *        cache (then no slot is rotated).
+ *   R_V  fp32 [n_kv_heads][head_dim][head_dim], or NULL: no slot is rotated
+ *        back (an all-BF16 cache, or values stored in the rotated basis
+ *        because R_V is folded into the projections; o is then in that basis).
  *   out      NULL or bf16 [batch][Hq][head_dim]: o rounded to nearest even.
  *   out_f32  NULL or fp32 [batch][Hq][head_dim]: o before that rounding.
  *            At least one of out / out_f32 must be given.
