@@ -76,6 +76,12 @@ __device__ __forceinline__ uint32_t qk_reg(uint32_t w, uint32_t wb, int r) {
 // factors of registers 0..7: 1, 4, 16, 64, 256, 4, 16, 64
 __device__ __host__ constexpr float qk_factor(int r) { return r == 4 ? 256.f : (float)(1 << (2 * (r & 3))); }
 
+// Group-pure QK mapping (groups of 32 or 64 channels): in MMA m = 2 Gb + j a thread with lane
+// parity odd uses registers qk_rsel(j, 0, odd) (A k-columns 2t, 2t+1) and qk_rsel(j, 1, odd)
+// (2t+8, 2t+9) of its word W = 2 Gb + (t >> 1): even lanes registers 0, 1 / 4, 5, odd lanes 2, 3 /
+// 6, 7, so the two lanes that share a word take disjoint halves of it.
+__device__ __host__ __forceinline__ int qk_rsel(int j, int e, int odd) { return 4 * j + 2 * odd + e; }
+
 // PV operand: register i (0..15) of the pair (token x, token y) for channel 16W + i, from the
 // byte permutes P1..P4 of their words; value code * pv_factor(i) * 2^-24.
 __device__ __forceinline__ uint32_t pv_reg(uint32_t P1, uint32_t P2, uint32_t P3, uint32_t P4, int i) {
@@ -854,18 +860,35 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
         const int hh = nt * 4 + (gid >> 1), part = gid & 1;
         const bool valid = hh < G;
         const int hq = h * G + (valid ? hh : 0);
+        if constexpr (NGRP == 1) {
 #pragma unroll
-        for (int kap = 0; kap < 2; ++kap)
+            for (int kap = 0; kap < 2; ++kap)
 #pragma unroll
-            for (int sg = 0; sg < 4; ++sg)
+                for (int sg = 0; sg < 4; ++sg)
 #pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int rr = 2 * sg + e, W = 2 * t + kap;
-                    const float inv = 1.0f / qk_factor(rr);
-                    const float v0 = valid ? qrot(hq, 16 * W + rr) * inv : 0.f;
-                    const float v1 = valid ? qrot(hq, 16 * W + 8 + rr) * inv : 0.f;
-                    bq[nt][kap * 4 + sg][e] = pack2(split_part(v0, part), split_part(v1, part));
-                }
+                    for (int e = 0; e < 2; ++e) {
+                        const int rr = 2 * sg + e, W = 2 * t + kap;
+                        const float inv = 1.0f / qk_factor(rr);
+                        const float v0 = valid ? qrot(hq, 16 * W + rr) * inv : 0.f;
+                        const float v1 = valid ? qrot(hq, 16 * W + 8 + rr) * inv : 0.f;
+                        bq[nt][kap * 4 + sg][e] = pack2(split_part(v0, part), split_part(v1, part));
+                    }
+        } else {
+            // group-pure MMAs: MMA m = 2 Gb + j covers 32-channel block Gb; this thread's k-rows are
+            // channels 16 W + r (+ 8) of word W = 2 Gb + (t >> 1), registers r = qk_rsel(j, e, t & 1)
+#pragma unroll
+            for (int Gb = 0; Gb < 4; ++Gb)
+#pragma unroll
+                for (int j = 0; j < 2; ++j)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int rr = qk_rsel(j, e, t & 1), W = 2 * Gb + (t >> 1);
+                        const float inv = 1.0f / qk_factor(rr);
+                        const float v0 = valid ? qrot(hq, 16 * W + rr) * inv : 0.f;
+                        const float v1 = valid ? qrot(hq, 16 * W + 8 + rr) * inv : 0.f;
+                        bq[nt][2 * Gb + j][e] = pack2(split_part(v0, part), split_part(v1, part));
+                    }
+        }
     }
     // per-group sums of q_rot for the zero-point term, for the head this thread owns (nt*4 + t)
 #pragma unroll
@@ -903,6 +926,27 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
             kofs1 = kofs0 + 8 * 32;
 #pragma unroll
             for (int i = 0; i < 4; ++i) vofs[i] = vrow[i] * 32 + 4 * gid;
+        }
+    }
+    // group-pure mapping (NGRP > 1): word 2 Gb + (t >> 1) of K rows gid, gid + 8 and word
+    // 2 Gb + (gid >> 2) of V rows t, t + 8, t + 4, t + 12, for 32-channel blocks Gb = 0..3
+    int kofg[4], vofg[4][4];
+    if constexpr (NGRP > 1) {
+        const int vrow[4] = {t, t + 8, t + 4, t + 12};
+#pragma unroll
+        for (int Gb = 0; Gb < 4; ++Gb) {
+            const int wk = 2 * Gb + (t >> 1), wv = 2 * Gb + (gid >> 2);
+            if constexpr (TMA) {
+                const int hh = h & 3;
+                kofg[Gb] = gid * 128 + (((2 * hh + (wk >> 2)) ^ gid) << 4) + (wk & 3) * 4;
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    vofg[Gb][i] = vrow[i] * 128 + (((2 * hh + (wv >> 2)) ^ (vrow[i] & 7)) << 4) + (wv & 3) * 4;
+            } else {
+                kofg[Gb] = gid * 32 + 4 * wk;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) vofg[Gb][i] = vrow[i] * 32 + 4 * wv;
+            }
         }
     }
     auto tile_base = [&](const uint8_t *arr, int j) -> const uint8_t * {
@@ -944,42 +988,86 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
             const int jt[2] = {ja, jb_raw < kTilesPerStage ? jb_raw : ja};
             const bool uok[2] = {ua, ub};
 
-            // ---- S = K_codes . q_rot for both tiles (rows = tokens gid, gid+8; cols = 4 heads x hi/lo)
-            float sacc[2][NT][NGRP][4];
-#pragma unroll
-            for (int u = 0; u < 2; ++u)
-#pragma unroll
-                for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-                    for (int jg = 0; jg < NGRP; ++jg)
-#pragma unroll
-                        for (int c = 0; c < 4; ++c) sacc[u][nt][jg][c] = 0.f;
-            uint2 kw0[2], kw1[2];
-#pragma unroll
-            for (int u = 0; u < 2; ++u) {
-                const uint8_t *Kc = tile_base(sb, jt[u]);
-                kw0[u] = *reinterpret_cast<const uint2 *>(Kc + kofs0);
-                kw1[u] = *reinterpret_cast<const uint2 *>(Kc + kofs1);
-            }
-#pragma unroll
-            for (int kap = 0; kap < 2; ++kap) {
-                const int gk = (2 * t + kap) * NGRP / 8;
+            // ---- NGRP > 1: group-pure MMAs, each group's dot products folded into the logits at once:
+            // tq[u][nt][e] = sum over groups (ascending) of scale*csc*dot + zero*qz (tokens gid, gid+8)
+            float tq[2][NT][2];
+            if constexpr (NGRP > 1) {
+                constexpr int kBpg = 4 / NGRP;             // 32-channel blocks per group
+                const bool odd = t & 1;
+                const uint32_t mA0 = odd ? kM2 : kM0, mB0 = odd ? kM3 : kM1, mA1 = odd ? kM2 : kM4;
+                const uint32_t mB1 = odd ? kM3 : kM1;
 #pragma unroll
                 for (int u = 0; u < 2; ++u) {
-                    const uint32_t w0 = kap ? kw0[u].y : kw0[u].x, w1 = kap ? kw1[u].y : kw1[u].x;
-                    const uint32_t w0b = __byte_perm(w0, 0, 0x3321), w1b = __byte_perm(w1, 0, 0x3321);
+                    const uint8_t *Kc = tile_base(sb, jt[u]);
+                    const uint16_t *sk = reinterpret_cast<const uint16_t *>(sb + off_s) + jt[u] * kTileTokens * rs + h * NGRP;
+                    float sg[NT][4];
 #pragma unroll
-                    for (int sg = 0; sg < 4; ++sg) {
-                        const uint32_t a0 = qk_reg(w0, w0b, 2 * sg), a1 = qk_reg(w1, w1b, 2 * sg);
-                        const uint32_t a2 = qk_reg(w0, w0b, 2 * sg + 1), a3 = qk_reg(w1, w1b, 2 * sg + 1);
+                    for (int nt = 0; nt < NT; ++nt) tq[u][nt][0] = tq[u][nt][1] = 0.f;
 #pragma unroll
-                        for (int nt = 0; nt < NT; ++nt)
+                    for (int Gb = 0; Gb < 4; ++Gb) {
+                        const uint32_t w0 = *reinterpret_cast<const uint32_t *>(Kc + kofg[Gb]);
+                        const uint32_t w1 = *reinterpret_cast<const uint32_t *>(Kc + kofg[Gb] + (TMA ? 8 * 128 : 8 * 32));
+                        const uint32_t w0b = __byte_perm(w0, 0, 0x3321), w1b = __byte_perm(w1, 0, 0x3321);
+                        const uint32_t w0s = odd ? w0b : w0, w1s = odd ? w1b : w1;
+                        if (Gb % kBpg == 0) {
 #pragma unroll
-                            for (int jg = 0; jg < NGRP; ++jg) {
-                                const bool on = NGRP == 1 || gk == jg;
-                                mma16816(sacc[u][nt][jg], a0, a1, a2, a3, on ? bq[nt][kap * 4 + sg][0] : 0u,
-                                         on ? bq[nt][kap * 4 + sg][1] : 0u);
+                            for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                                for (int c = 0; c < 4; ++c) sg[nt][c] = 0.f;
+                        }
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            const uint32_t a0 = j ? (w0s & mA1) : (w0 & mA0), a1 = j ? (w1s & mA1) : (w1 & mA0);
+                            const uint32_t a2 = j ? (w0b & mB1) : (w0 & mB0), a3 = j ? (w1b & mB1) : (w1 & mB0);
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt)
+                                mma16816(sg[nt], a0, a1, a2, a3, bq[nt][2 * Gb + j][0], bq[nt][2 * Gb + j][1]);
+                        }
+                        if (Gb % kBpg == kBpg - 1) {
+                            const int jg = Gb / kBpg;
+#pragma unroll
+                            for (int e = 0; e < 2; ++e) {
+                                const int tok = gid + 8 * e;
+                                const float sc = bf16_to_f32(sk[tok * rs + jg]), zc = bf16_to_f32(sk[arr_el + tok * rs + jg]);
+#pragma unroll
+                                for (int nt = 0; nt < NT; ++nt)
+                                    tq[u][nt][e] += fmaf(sc * csc, sg[nt][2 * e] + sg[nt][2 * e + 1], zc * qz[nt][jg]);
                             }
+                        }
+                    }
+                }
+            }
+
+            // ---- S = K_codes . q_rot for both tiles (rows = tokens gid, gid+8; cols = 4 heads x hi/lo)
+            float sacc[2][NT][4];                        // (NGRP == 1)
+            if constexpr (NGRP == 1) {
+#pragma unroll
+                for (int u = 0; u < 2; ++u)
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) sacc[u][nt][c] = 0.f;
+                uint2 kw0[2], kw1[2];
+#pragma unroll
+                for (int u = 0; u < 2; ++u) {
+                    const uint8_t *Kc = tile_base(sb, jt[u]);
+                    kw0[u] = *reinterpret_cast<const uint2 *>(Kc + kofs0);
+                    kw1[u] = *reinterpret_cast<const uint2 *>(Kc + kofs1);
+                }
+#pragma unroll
+                for (int kap = 0; kap < 2; ++kap) {
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const uint32_t w0 = kap ? kw0[u].y : kw0[u].x, w1 = kap ? kw1[u].y : kw1[u].x;
+                        const uint32_t w0b = __byte_perm(w0, 0, 0x3321), w1b = __byte_perm(w1, 0, 0x3321);
+#pragma unroll
+                        for (int sg = 0; sg < 4; ++sg) {
+                            const uint32_t a0 = qk_reg(w0, w0b, 2 * sg), a1 = qk_reg(w1, w1b, 2 * sg);
+                            const uint32_t a2 = qk_reg(w0, w0b, 2 * sg + 1), a3 = qk_reg(w1, w1b, 2 * sg + 1);
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt)
+                                mma16816(sacc[u][nt], a0, a1, a2, a3, bq[nt][kap * 4 + sg][0], bq[nt][kap * 4 + sg][1]);
+                        }
                     }
                 }
             }
@@ -1005,11 +1093,11 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
                     for (int e = 0; e < 2; ++e) {
                         const int tok = gid + 8 * e;
                         float tt = 0.f;
-#pragma unroll
-                        for (int jg = 0; jg < NGRP; ++jg) {
-                            const float sc = bf16_to_f32(sk[tok * rs + jg]), zc = bf16_to_f32(sk[arr_el + tok * rs + jg]);
-                            const float dot = sacc[u][nt][jg][2 * e] + sacc[u][nt][jg][2 * e + 1];
-                            tt += fmaf(sc * csc, dot, zc * qz[nt][jg]);
+                        if constexpr (NGRP == 1) {
+                            const float sc = bf16_to_f32(sk[tok * rs]), zc = bf16_to_f32(sk[arr_el + tok * rs]);
+                            tt += fmaf(sc * csc, sacc[u][nt][2 * e] + sacc[u][nt][2 * e + 1], zc * qz[nt][0]);
+                        } else {
+                            tt = tq[u][nt][e];
                         }
                         tv[u][e] = tok < lim[u] ? tt : -INFINITY;
                     }
@@ -1076,20 +1164,13 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
             }
             __syncwarp();
 
-            // ---- O += V_codes^T . (P*scale)  (rows = channels 16*gid + i, k = tokens, cols = heads x hi/lo)
-            const int gv = gid * NGRP / 8;
+            // ---- O += V_codes^T . (P*scale)  (k = tokens, cols = heads x hi/lo).  Rows: with one group,
+            // m-tile mt row gid / gid + 8 = channel 16 gid + 2 mt / + 1; with NGRP > 1 (group-pure
+            // m-tiles, one group's P*scale each), m-tile 2 Gb + j row gid / gid + 8 = channel
+            // 32 Gb + 4 gid + 2 j / + 1 (byte 8 Gb + gid of the row)
 #pragma unroll
             for (int u = 0; u < 2; ++u) {
                 const uint8_t *Vc = tile_base(sb + off_v, jt[u]);
-                // k-columns 2t, 2t+1 <- tokens t, t+8; 2t+8, 2t+9 <- tokens t+4, t+12
-                const uint32_t X = *reinterpret_cast<const uint32_t *>(Vc + vofs[0]);
-                const uint32_t Y = *reinterpret_cast<const uint32_t *>(Vc + vofs[1]);
-                const uint32_t X2 = *reinterpret_cast<const uint32_t *>(Vc + vofs[2]);
-                const uint32_t Y2 = *reinterpret_cast<const uint32_t *>(Vc + vofs[3]);
-                const uint32_t P1 = __byte_perm(X, Y, 0x5410), P2 = __byte_perm(X, Y, 0x6521);
-                const uint32_t P3 = __byte_perm(X, Y, 0x7632), P4 = __byte_perm(X, Y, 0x7733);
-                const uint32_t Q1 = __byte_perm(X2, Y2, 0x5410), Q2 = __byte_perm(X2, Y2, 0x6521);
-                const uint32_t Q3 = __byte_perm(X2, Y2, 0x7632), Q4 = __byte_perm(X2, Y2, 0x7733);
                 uint32_t bw[NGRP][NT][2];
 #pragma unroll
                 for (int jg = 0; jg < NGRP; ++jg)
@@ -1099,17 +1180,42 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
                         bw[jg][nt][0] = col[t];
                         bw[jg][nt][1] = col[t + 4];
                     }
+                if constexpr (NGRP == 1) {
+                    // k-columns 2t, 2t+1 <- tokens t, t+8; 2t+8, 2t+9 <- tokens t+4, t+12
+                    const uint32_t X = *reinterpret_cast<const uint32_t *>(Vc + vofs[0]);
+                    const uint32_t Y = *reinterpret_cast<const uint32_t *>(Vc + vofs[1]);
+                    const uint32_t X2 = *reinterpret_cast<const uint32_t *>(Vc + vofs[2]);
+                    const uint32_t Y2 = *reinterpret_cast<const uint32_t *>(Vc + vofs[3]);
+                    const uint32_t P1 = __byte_perm(X, Y, 0x5410), P2 = __byte_perm(X, Y, 0x6521);
+                    const uint32_t P3 = __byte_perm(X, Y, 0x7632), P4 = __byte_perm(X, Y, 0x7733);
+                    const uint32_t Q1 = __byte_perm(X2, Y2, 0x5410), Q2 = __byte_perm(X2, Y2, 0x6521);
+                    const uint32_t Q3 = __byte_perm(X2, Y2, 0x7632), Q4 = __byte_perm(X2, Y2, 0x7733);
 #pragma unroll
-                for (int mt = 0; mt < 8; ++mt) {
-                    const uint32_t a0 = pv_reg(P1, P2, P3, P4, 2 * mt), a1 = pv_reg(P1, P2, P3, P4, 2 * mt + 1);
-                    const uint32_t a2 = pv_reg(Q1, Q2, Q3, Q4, 2 * mt), a3 = pv_reg(Q1, Q2, Q3, Q4, 2 * mt + 1);
+                    for (int mt = 0; mt < 8; ++mt) {
+                        const uint32_t a0 = pv_reg(P1, P2, P3, P4, 2 * mt), a1 = pv_reg(P1, P2, P3, P4, 2 * mt + 1);
+                        const uint32_t a2 = pv_reg(Q1, Q2, Q3, Q4, 2 * mt), a3 = pv_reg(Q1, Q2, Q3, Q4, 2 * mt + 1);
 #pragma unroll
-                    for (int jg = 0; jg < NGRP; ++jg) {
-                        const bool on = NGRP == 1 || gv == jg;
+                        for (int nt = 0; nt < NT; ++nt) mma16816(oacc[nt][mt], a0, a1, a2, a3, bw[0][nt][0], bw[0][nt][1]);
+                    }
+                } else {
+                    // byte gid & 3 of the word of token t (t + 4) low, of token t + 8 (t + 12) high
+                    const uint32_t selv = (uint32_t)(gid & 3) | ((uint32_t)(4 + (gid & 3)) << 8);
 #pragma unroll
-                        for (int nt = 0; nt < NT; ++nt)
-                            mma16816(oacc[nt][mt], on ? a0 : 0u, on ? a1 : 0u, on ? a2 : 0u, on ? a3 : 0u,
-                                     bw[jg][nt][0], bw[jg][nt][1]);
+                    for (int Gb = 0; Gb < 4; ++Gb) {
+                        const uint32_t X = *reinterpret_cast<const uint32_t *>(Vc + vofg[Gb][0]);
+                        const uint32_t Y = *reinterpret_cast<const uint32_t *>(Vc + vofg[Gb][1]);
+                        const uint32_t X2 = *reinterpret_cast<const uint32_t *>(Vc + vofg[Gb][2]);
+                        const uint32_t Y2 = *reinterpret_cast<const uint32_t *>(Vc + vofg[Gb][3]);
+                        const uint32_t P = __byte_perm(X, Y, selv), Q = __byte_perm(X2, Y2, selv);
+                        const int jg = Gb * NGRP / 4;
+#pragma unroll
+                        for (int j = 0; j < 2; ++j) {
+                            const uint32_t mlo = j ? kM2 : kM0, mhi = j ? kM3 : kM1;
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt)
+                                mma16816(oacc[nt][2 * Gb + j], P & mlo, P & mhi, Q & mlo, Q & mhi, bw[jg][nt][0],
+                                         bw[jg][nt][1]);
+                        }
                     }
                 }
             }
@@ -1132,7 +1238,8 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
             for (int jg = 0; jg < NGRP; ++jg) zs[nt][jg] += __shfl_xor_sync(0xffffffffu, zs[nt][jg], o);
         }
     }
-    const int gv = gid * NGRP / 8;
+    // output element i of this thread: channel and code factor (see the PV mapping above)
+    auto out_ch = [&](int i) { return NGRP == 1 ? 16 * gid + i : 32 * (i >> 2) + 4 * gid + (i & 3); };
     // back to the split's true maximum: l, the zero-point sum and the accumulators scale by 2^(m_run - m_true)
     float fix[NT];
 #pragma unroll
@@ -1144,14 +1251,23 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
     float outv[NT][16];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-        float z = zs[nt][0];
+        if constexpr (NGRP == 1) {
+            const float z = zs[nt][0];
 #pragma unroll
-        for (int jg = 1; jg < NGRP; ++jg)
-            if (gv == jg) z = zs[nt][jg];
+            for (int mt = 0; mt < 8; ++mt) {
+                outv[nt][2 * mt] = fmaf(oacc[nt][mt][0] + oacc[nt][mt][1], kTwo24 / pv_factor(2 * mt), z) * fix[nt];
+                outv[nt][2 * mt + 1] =
+                    fmaf(oacc[nt][mt][2] + oacc[nt][mt][3], kTwo24 / pv_factor(2 * mt + 1), z) * fix[nt];
+            }
+        } else {
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-            outv[nt][2 * mt] = fmaf(oacc[nt][mt][0] + oacc[nt][mt][1], kTwo24 / pv_factor(2 * mt), z) * fix[nt];
-            outv[nt][2 * mt + 1] = fmaf(oacc[nt][mt][2] + oacc[nt][mt][3], kTwo24 / pv_factor(2 * mt + 1), z) * fix[nt];
+            for (int mt = 0; mt < 8; ++mt) {
+                const float z = zs[nt][(mt >> 1) * NGRP / 4];
+                const float f0 = kTwo24 / (float)(1 << (2 * ((2 * mt) & 3)));
+                const float f1 = kTwo24 / (float)(1 << (2 * ((2 * mt + 1) & 3)));
+                outv[nt][2 * mt] = fmaf(oacc[nt][mt][0] + oacc[nt][mt][1], f0, z) * fix[nt];
+                outv[nt][2 * mt + 1] = fmaf(oacc[nt][mt][2] + oacc[nt][mt][3], f1, z) * fix[nt];
+            }
         }
     }
 
@@ -1167,12 +1283,11 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
             if (hh < G) {
                 const int hq = h * G + hh;
                 const size_t row = ((size_t)b * Hq + hq) * S1 + s;
-                float4 *dst = reinterpret_cast<float4 *>(to_res ? res + res_acc(Hq) + hq * kHeadDim + 16 * gid
-                                                                : a.out.acc + row * kHeadDim + 16 * gid);
+                float *dst = to_res ? res + res_acc(Hq) + hq * kHeadDim : a.out.acc + row * kHeadDim;
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4)
-                    dst[q4] = make_float4(outv[nt][4 * q4], outv[nt][4 * q4 + 1], outv[nt][4 * q4 + 2],
-                                          outv[nt][4 * q4 + 3]);
+                    *reinterpret_cast<float4 *>(dst + out_ch(4 * q4)) =
+                        make_float4(outv[nt][4 * q4], outv[nt][4 * q4 + 1], outv[nt][4 * q4 + 2], outv[nt][4 * q4 + 3]);
                 if (gid == 0) {
                     (to_res ? res + hq : a.out.m + row)[0] = m_run[nt];
                     (to_res ? res + Hq + hq : a.out.l + row)[0] = l_run[nt];
@@ -1196,7 +1311,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
             cl[warp * NT * 4 + nt * 4 + t] = l_run[nt];
         }
 #pragma unroll
-        for (int i = 0; i < 16; ++i) ca[(warp * NT * 4 + nt * 4 + t) * kHeadDim + 16 * gid + i] = outv[nt][i];
+        for (int i = 0; i < 16; ++i) ca[(warp * NT * 4 + nt * 4 + t) * kHeadDim + out_ch(i)] = outv[nt][i];
     }
     consumer_sync();
     if (sub == 0) {
