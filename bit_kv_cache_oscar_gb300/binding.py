@@ -288,8 +288,10 @@ def oscar_decode_attention_fused(layout: Layout, q: torch.Tensor, R_K: torch.Ten
                                  merge_counters: Optional[torch.Tensor] = None, stream=None):
     """oscar_decode_attention with q . R_K computed inside the launch (same partials bits); with
     demote_pos ([batch] int32, -1 = none) also the per-step demotion of those positions; with
-    out / out_f32 also oscar_merge's output (inside the launch when merge_counters, int32 zeros
-    [batch], is given)."""
+    out / out_f32 also oscar_merge's output, from a second launch that starts each request's
+    merge on its arrival count when merge_counters (int32 zeros [2 * batch]) is given."""
+    if merge_counters is not None and merge_counters.numel() < 2 * int(q.shape[0]):
+        raise OscarError("oscar_decode_attention_fused: merge_counters needs 2 * batch int32 entries")
     _check("oscar_decode_attention_fused", lib().oscar_decode_attention_fused(
         ctypes.byref(layout.c()), _ptr(q), _ptr(R_K), ctypes.byref(bf16_pool.c()), _ptr(bf16_page_table),
         ctypes.byref(int2_pool.c()), _ptr(int2_page_table), int(int2_page_table.shape[-1]), _ptr(seq_len),

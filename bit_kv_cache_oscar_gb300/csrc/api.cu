@@ -317,18 +317,16 @@ oscar_status_t oscar_decode_attention_fused(const oscar_layout_t *layout, const 
                    int2_pool->scale_v, int2_pool->zero_v, int2_pool->n_pages};
     }
     const bool merge = out || out_f32;
-    oscar::FusedMerge mg{merge_counters, R_V, out, out_f32, lse};
-    if (!R_V) merge_counters = nullptr;          // the in-launch merge rotates back: oscar_merge runs
-    bool merged = false;
+    int32_t *arrivals = merge && merge_counters ? merge_counters : nullptr;
+    int clusters = 0;
     cudaError_t e = oscar::launch_decode_mma_demote(*layout, R_K, int2_view(int2_pool), int2_page_table, q,
                                                     bf16_view(bf16_pool), bf16_page_table, max_pages_per_req,
                                                     seq_len, hist_end, batch, sm_scale, part_view(partials),
-                                                    status_ptr(), dem, merge && merge_counters ? &mg : nullptr,
-                                                    &merged, (cudaStream_t)stream);
+                                                    status_ptr(), dem, arrivals, &clusters, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_status(e, "fused decode attention launch");
-    if (merge && !merged)                       // no counters, or the layout's stages cannot hold the merge
+    if (merge)
         return cuda_status(oscar::launch_merge(*layout, part_view(partials), R_V, batch, out, out_f32, lse,
-                                               (cudaStream_t)stream),
+                                               (cudaStream_t)stream, arrivals, clusters, status_ptr()),
                            "oscar_merge launch");
     return OSCAR_OK;
 }

@@ -130,11 +130,8 @@ struct MmaArgs {
     const uint16_t *q;          // raw bf16 queries (window CTAs, and the rotation when RK is set)
     FusedDemotion dem;          // per-step demotion done by the window CTAs (dem.dem_pos NULL: none)
     int group;
-    // merge by the last cluster of each request (mcount NULL: the partials are left to oscar_merge)
-    int32_t *mcount;            // [batch] arrivals, zero before and after the launch
-    const float *RVm;           // R_V for the merge
-    uint16_t *mout;             // the merge's outputs (oscar_merge's out, out_f32, lse)
-    float *mout_f32, *mlse;
+    // per-request arrival counts for the merge launch (NULL: the merge waits for the whole grid)
+    int32_t *arrivals;          // [batch]: +1 per cluster once its partial slot is written
     Bf16PoolView bpool;         // BF16 sink/recent pool and its page table (window CTAs)
     const int32_t *bpt;
 };
@@ -448,138 +445,18 @@ __device__ void window_demote(const MmaArgs &a, float *small, uint8_t *area, int
     }
 }
 
-// ---- The merge, done by the last cluster of a request to finish (fused launch).
-// Every CTA calls this after its cluster has written its partial slot: the cluster counts itself
-// on mcount[b]; the one that counts last merges request b with oscar_merge's operations in
-// oscar_merge's order (M over non-empty slots; w_i = 2^(m_i - M) by the merge's own 2^x;
-// L, A fma chains over history slots ascending; A.R_V^T as an fma chain; the BF16 slot; o = A/L).
-// CTA rank r of that cluster takes kv heads r, r + C, ...: it stages R_V (row stride 132
-// floats, so that the chain's reads of 8 rows x 4 heads per warp are conflict-free) with one
-// bulk copy per row; the window CTAs prefetched it into L2.  All threads of the CTA call this.
-template <int G>
-__device__ void arrive_merge(const MmaArgs &a, uint8_t *smem, uint8_t *area, int b) {
-    constexpr int kRs = kHeadDim + 4;                 // padded row stride (floats)
-    constexpr int kPre = 48;                          // slots whose accumulators are loaded up front
-    const int C = a.csize, rank = C > 1 ? (int)cluster_ctarank() : 0;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    int *flag = reinterpret_cast<int *>(smem + 120);
-    __threadfence();                                  // this CTA's slot writes, before the count
+// ---- Arrival count for the merge launch: once every CTA of the cluster has written its part of
+// the cluster's partial slot, one thread adds 1 to arrivals[b].  The fence orders each thread's
+// slot writes before the cluster barrier, and the barrier before the count (release at gpu
+// scope), so a merge CTA that reads the full count with acquire sees every slot.  Every thread
+// of the CTA calls this.
+__device__ __forceinline__ void arrive_count(const MmaArgs &a, int b) {
+    const int C = a.csize;
+    __threadfence();
     if (C > 1) cluster_sync_all(); else __syncthreads();
-    if (rank == 0 && tid == 0) {
-        const int total = (a.hist_ctas + a.win_ctas) / C;
-        const int old = atomicAdd(a.mcount + b, 1);
-        const int is_last = old == total - 1;
-        if (is_last) a.mcount[b] = 0;                 // all of b's clusters have counted
-        // every CTA gets the answer in its own shared memory: after the barrier nobody reads a
-        // peer (which may exit as soon as it has passed the barrier)
-        if (C > 1) {
-            for (int q = 0; q < C; ++q) st_dsmem_f32(saddr(flag), (uint32_t)q, __int_as_float(is_last));
-        } else {
-            *flag = is_last;
-        }
-    }
-    if (C > 1) cluster_sync_all(); else __syncthreads();
-    const int last = *flag;
-    if (!last) return;
-    __threadfence();                                  // the other clusters' slots are now visible
-
-    const int Hkv = a.n_kv, Hq = Hkv * G, S = a.out.S, S1 = S + 1;
-    float *Rc = reinterpret_cast<float *>(area);      // [128][kRs] rows of R_V
-    float *As = Rc + kHeadDim * kRs;                  // [G][kRs] merged history accumulators
-    float *ws = As + G * kRs;                         // [G][S1] slot weights
-    float *ls = ws + G * S1;                          // [G][S1] slot l
-    float *Ms = ls + G * S1;                          // [G] M, then [G] L over the history slots
-    uint64_t *rb = reinterpret_cast<uint64_t *>(smem + 112);
-    if (tid == 0) {
-        mbar_init(saddr(rb), 1);
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    int nb = 0;
-    for (int k = rank; k < Hkv; k += C) {
-        __syncthreads();
-        for (int e = tid; e < G * S1; e += blockDim.x) {
-            const size_t row = ((size_t)b * Hq + k * G + e / S1) * S1 + e % S1;
-            ls[e] = a.out.l[row];
-            ws[e] = a.out.m[row];
-        }
-        __syncthreads();
-        if (warp < G) {                               // M of head `warp` over the non-empty slots
-            float mloc = -INFINITY;
-            for (int i = lane; i < S1; i += 32)
-                if (ls[warp * S1 + i] > 0.0f && ws[warp * S1 + i] > mloc) mloc = ws[warp * S1 + i];
-#pragma unroll
-            for (int o = 16; o; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
-            if (lane == 0) Ms[warp] = mloc;
-        }
-        __syncthreads();
-        for (int e = tid; e < G * S1; e += blockDim.x)
-            ws[e] = ls[e] > 0.0f ? exp2_taylor(__fsub_rn(ws[e], Ms[e / S1])) : 0.0f;
-        __syncthreads();
-        for (int e = tid; e < G * kHeadDim; e += blockDim.x) {
-            const int hh = e / kHeadDim, c = e % kHeadDim;
-            const float *acc = a.out.acc + ((size_t)b * Hq + k * G + hh) * S1 * kHeadDim + c;
-            float xs[kPre];
-#pragma unroll
-            for (int i = 0; i < kPre; ++i) xs[i] = i < S ? acc[(size_t)i * kHeadDim] : 0.0f;
-            float L = 0.0f, A = 0.0f;
-#pragma unroll
-            for (int i = 0; i < kPre; ++i) {
-                if (i < S) {
-                    const float li = ls[hh * S1 + i], w = ws[hh * S1 + i];
-                    const bool on = li > 0.0f;
-                    L = on ? __fmaf_rn(li, w, L) : L;
-                    A = on ? __fmaf_rn(xs[i], w, A) : A;
-                }
-            }
-            for (int i = kPre; i < S; ++i) {
-                const float li = ls[hh * S1 + i], w = ws[hh * S1 + i];
-                const float x = acc[(size_t)i * kHeadDim];
-                const bool on = li > 0.0f;
-                L = on ? __fmaf_rn(li, w, L) : L;
-                A = on ? __fmaf_rn(x, w, A) : A;
-            }
-            As[hh * kRs + c] = A;
-            if (c == 0) Ms[G + hh] = L;
-        }
-        // all 128 rows of R_V[k] (bulk copies, one per row, four per lane of the copy warp)
-        __syncthreads();                              // As / Ms written; the previous head's rows consumed
-        if (warp == kCW) {
-            fence_proxy_async_smem();                 // the area held generic-proxy data
-            if (lane == 0) mbar_arrive_expect_tx(saddr(rb), kHeadDim * kHeadDim * 4);
-            __syncwarp();
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int row = q * 32 + lane;
-                tma_load_1d(saddr(Rc + row * kRs), a.RVm + ((size_t)k * kHeadDim + row) * kHeadDim, kHeadDim * 4,
-                            saddr(rb));
-            }
-        }
-        if (!mbar_wait(saddr(rb), nb & 1) && tid == 0) flag_status(a.status, OSCAR_DEV_WAIT_TIMEOUT);
-        ++nb;
-        // outputs (row j, head hh): a warp takes 8 rows x 4 heads, so its chains read 8 distinct
-        // R_V rows and 4 distinct accumulator rows at each step, conflict-free
-        for (int o = tid; o < kHeadDim * 4 * ((G + 3) / 4); o += blockDim.x) {
-            const int ln = o & 31, wslot = o >> 5;
-            const int j = (wslot % 16) * 8 + (ln & 7), hh = (ln >> 3) + 4 * (wslot / 16);
-            if (hh >= G) continue;
-            float r = 0.0f;
-#pragma unroll 8
-            for (int i = 0; i < kHeadDim; ++i) r = __fmaf_rn(As[hh * kRs + i], Rc[j * kRs + i], r);
-            const int hq = k * G + hh;
-            const size_t slot_s = ((size_t)b * Hq + hq) * S1 + S;
-            float L = Ms[G + hh], Ar = r;
-            const float lS = ls[hh * S1 + S];
-            if (lS > 0.0f) {
-                const float w = ws[hh * S1 + S];
-                L = __fmaf_rn(lS, w, L);
-                Ar = __fmaf_rn(a.out.acc[slot_s * kHeadDim + j], w, Ar);
-            }
-            const float ov = L > 0.0f ? __fdiv_rn(Ar, L) : 0.0f;
-            const size_t orow = (size_t)b * Hq + hq;
-            if (a.mout) a.mout[orow * kHeadDim + j] = f32_to_bf16_rn(ov);
-            if (a.mout_f32) a.mout_f32[orow * kHeadDim + j] = ov;
-            if (a.mlse && j == 0) a.mlse[orow] = L > 0.0f ? (Ms[hh] + log2f(L)) * 0.6931471805599453f : -INFINITY;
-        }
+    if ((C > 1 ? cluster_ctarank() : 0) == 0 && threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(a.arrivals + b, 1);
     }
 }
 
@@ -627,16 +504,13 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
     int T, he;
     read_lengths(a.seq_len, a.hist_end, b, a.sink, a.max_pages * a.page_size, a.status, T, he);
     if (s < 0) {                               // a BF16 window CTA (uniform over the cluster)
-        if (a.mcount && threadIdx.x == 0)      // R_V of this CTA's kv heads into L2 for the merge
-            for (int k = blockIdx.x; k < Hkv; k += a.win_ctas)
-                prefetch_l2(a.RVm + (size_t)k * kHeadDim * kHeadDim, kHeadDim * kHeadDim * 4);
         pdl_wait();                            // q and the partials belong to the previous kernels
         window_cta<G>(a, reinterpret_cast<float *>(stage0 + a.win_off), reinterpret_cast<float *>(stage0 + a.res_off),
                       T, he, b, (int)blockIdx.x, a.win_ctas);
         // (after the cluster's last barrier: the stage area is free again)
         if (a.dem.dem_pos)
             window_demote(a, reinterpret_cast<float *>(smem + 128), stage0, T, he, b, (int)blockIdx.x, a.win_ctas);
-        if (a.mcount) arrive_merge<G>(a, smem, stage0, b);
+        if (a.arrivals) arrive_count(a, b);
         return;
     }
     const SplitRange r = history_split(a.sink, he, a.hist_ctas, s);   // C sub-splits per slot
@@ -786,7 +660,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
         }
         asm volatile("cp.async.wait_all;" ::: "memory");
         if (a.csize > 1) cluster_combine(a, reinterpret_cast<const float *>(stage0 + a.res_off), Hq, b, s / a.csize);
-        if (a.mcount) arrive_merge<G>(a, smem, stage0, b);
+        if (a.arrivals) arrive_count(a, b);
         return;
     }
 
@@ -1295,7 +1169,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
             }
         }
         if (to_res) cluster_combine(a, res, Hq, b, s / a.csize);
-        if (a.mcount) arrive_merge<G>(a, smem, stage0, b);
+        if (a.arrivals) arrive_count(a, b);
         return;
     }
 
@@ -1345,7 +1219,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
         }
     }
     if (to_res) cluster_combine(a, res, Hq, b, s / a.csize);
-    if (a.mcount) arrive_merge<G>(a, smem, stage0, b);
+    if (a.arrivals) arrive_count(a, b);
 }
 
 // Largest cluster size C in {8, 4, 2} whose co-resident clusters still occupy at least 90% of
@@ -1445,7 +1319,7 @@ bool codes_tensor_map(CUtensorMap *tm, const uint8_t *base, long long rows) {
 
 template <int G, int NGRP>
 cudaError_t launch_mma(const oscar_layout_t &L, MmaArgs a, int batch, bool history, bool window, cudaStream_t st,
-                       bool *merged) {
+                       int *clusters) {
     const int smem = mma_smem_plan<G, NGRP>(L, a);
     // the carve-up's invariants: vector and bulk-copy targets 16-byte aligned, tensor-map boxes
     // 1024-byte aligned, R_K chunks inside the stage area
@@ -1453,10 +1327,6 @@ cudaError_t launch_mma(const oscar_layout_t &L, MmaArgs a, int batch, bool histo
         (a.stage_off & 1023) || (a.stage_bytes & 1023 && L.n_kv_heads == 8) ||
         (a.RK && a.stages * a.stage_bytes < a.rk_chunk))
         return cudaErrorInvalidValue;
-    // the merge's scratch (32 padded R_V rows, G accumulator rows, per-slot weights) in the stage area
-    if (a.mcount && a.stages * a.stage_bytes < (kHeadDim + G) * (kHeadDim + 4) * 4 + 8 * G * (a.out.S + 1) + 8 * G)
-        a.mcount = nullptr;
-    if (merged) *merged = a.mcount != nullptr;
     const bool tma = L.n_kv_heads == 8;
     // the tensor-map kernel folds these for 8 kv heads
     if (tma && (a.off_v != 8 * 2048 || a.off_s != 2 * 8 * 2048 || a.arr_bytes != kStageTok * 8 * NGRP * 2 ||
@@ -1475,6 +1345,7 @@ cudaError_t launch_mma(const oscar_layout_t &L, MmaArgs a, int batch, bool histo
     if (cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void *>(kern), smem)) return e;
     a.hist_ctas = history ? a.out.S * a.csize : 0;
     a.win_ctas = window ? a.csize : 0;
+    if (clusters) *clusters = (a.hist_ctas + a.win_ctas) / a.csize;   // arrivals per request
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.win_ctas + a.hist_ctas, batch);
     cfg.blockDim = dim3(kThreads);
@@ -1519,8 +1390,8 @@ static cudaError_t decode_mma_impl(const oscar_layout_t &L, const float *RK, Int
                                    const uint16_t *q, Bf16PoolView bpool, const int32_t *bpt, int max_pages,
                                    const int32_t *seq_len, const int32_t *hist_end, int batch, float sm_scale,
                                    PartialsView out, int32_t *status, const FusedDemotion &dem, cudaStream_t st,
-                                   const float *q_rot, bool history, bool window, const FusedMerge *mg,
-                                   bool *merged);
+                                   const float *q_rot, bool history, bool window, int32_t *arrivals,
+                                   int *clusters);
 
 cudaError_t launch_decode_mma(const oscar_layout_t &L, const float *q_rot, const float *RK, Int2PoolView pool,
                               const int32_t *pt, const uint16_t *q, Bf16PoolView bpool, const int32_t *bpt,
@@ -1536,27 +1407,21 @@ cudaError_t launch_decode_mma_demote(const oscar_layout_t &L, const float *RK, I
                                      const uint16_t *q, Bf16PoolView bpool, const int32_t *bpt, int max_pages,
                                      const int32_t *seq_len, const int32_t *hist_end, int batch, float sm_scale,
                                      PartialsView out, int32_t *status, const FusedDemotion &dem,
-                                     const FusedMerge *mg, bool *merged, cudaStream_t st) {
+                                     int32_t *arrivals, int *clusters, cudaStream_t st) {
     return decode_mma_impl(L, RK, pool, pt, q, bpool, bpt, max_pages, seq_len, hist_end, batch, sm_scale, out, status,
-                           dem, st, nullptr, true, true, mg, merged);
+                           dem, st, nullptr, true, true, arrivals, clusters);
 }
 
 static cudaError_t decode_mma_impl(const oscar_layout_t &L, const float *RK, Int2PoolView pool, const int32_t *pt,
                                    const uint16_t *q, Bf16PoolView bpool, const int32_t *bpt, int max_pages,
                                    const int32_t *seq_len, const int32_t *hist_end, int batch, float sm_scale,
                                    PartialsView out, int32_t *status, const FusedDemotion &dem, cudaStream_t st,
-                                   const float *q_rot, bool history, bool window, const FusedMerge *mg,
-                                   bool *merged) {
-    if (merged) *merged = false;
+                                   const float *q_rot, bool history, bool window, int32_t *arrivals,
+                                   int *clusters) {
+    if (clusters) *clusters = 0;
     if (batch <= 0 || (!history && !window)) return cudaSuccess;
     MmaArgs a{};
-    if (mg && mg->counters && history && window) {
-        a.mcount = mg->counters;
-        a.RVm = mg->RV;
-        a.mout = mg->out;
-        a.mout_f32 = mg->out_f32;
-        a.mlse = mg->lse;
-    }
+    if (history && window) a.arrivals = arrivals;
     a.RK = RK;
     a.dem = dem;
     a.group = L.group;
@@ -1577,7 +1442,7 @@ static cudaError_t decode_mma_impl(const oscar_layout_t &L, const float *RK, Int
     a.status = status;
     const int ngrp = kHeadDim / L.group;
 #define OSCAR_MMA_CASE(GG, NN) \
-    if (L.gqa == GG && ngrp == NN) return launch_mma<GG, NN>(L, a, batch, history, window, st, merged);
+    if (L.gqa == GG && ngrp == NN) return launch_mma<GG, NN>(L, a, batch, history, window, st, clusters);
     OSCAR_MMA_CASE(1, 1) OSCAR_MMA_CASE(2, 1) OSCAR_MMA_CASE(4, 1) OSCAR_MMA_CASE(8, 1)
     OSCAR_MMA_CASE(1, 2) OSCAR_MMA_CASE(2, 2) OSCAR_MMA_CASE(4, 2) OSCAR_MMA_CASE(8, 2)
     OSCAR_MMA_CASE(1, 4) OSCAR_MMA_CASE(2, 4) OSCAR_MMA_CASE(4, 4) OSCAR_MMA_CASE(8, 4)

@@ -32,7 +32,8 @@ constexpr int kQuarter = kHeadDim / 4;
 // from the 32 rows of R_V that it staged before waiting for the partials' producer.
 // Dynamic smem: [R_V 32 x 129 if RV] [A 128] [w S+1] [l S+1] [red 8].
 __global__ void __launch_bounds__(128) merge_kernel(PartialsView p, const float *RV, int n_q_heads, int gqa,
-                                                    uint16_t *out, float *out_f32, float *lse) {
+                                                    uint16_t *out, float *out_f32, float *lse, int32_t *counters,
+                                                    int expected, int batch, int32_t *status) {
     extern __shared__ __align__(16) float smem[];
     const int hq = blockIdx.x, b = blockIdx.y, z = blockIdx.z, j = threadIdx.x;
     const int S = p.S;
@@ -53,7 +54,31 @@ __global__ void __launch_bounds__(128) merge_kernel(PartialsView p, const float 
             dst[0] = v.x; dst[1] = v.y; dst[2] = v.z; dst[3] = v.w;
         }
     }
-    pdl_wait();                                  // the partials come from the previous kernels
+    if (!counters) {
+        pdl_wait();                              // the partials come from the previous kernels
+    } else {
+        // Request b's partials are complete once its clusters have all counted (each counts after
+        // its slot writes, with release): wait for that rather than for the whole decode grid.
+        // This grid launched only after every decode CTA had passed its loop, so all of them are
+        // running and the count arrives; the wait is bounded all the same.
+        if (j == 0) {
+            int32_t n = 0;
+            for (long i = 0; i < kSpinLimit; ++i) {
+                asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(n) : "l"(counters + b) : "memory");
+                if (n >= expected) break;
+                __nanosleep(32);
+            }
+            if (n < expected) flag_status(status, OSCAR_DEV_WAIT_TIMEOUT);
+            // the last of b's merge CTAs to get here resets both counts for the next launch
+            const int per_req = gridDim.x * gridDim.z;
+            if (atomicAdd(counters + batch + b, 1) == per_req - 1) {
+                counters[b] = 0;
+                counters[batch + b] = 0;
+                __threadfence();
+            }
+        }
+        __syncthreads();
+    }
 
     // Issue the loads of this thread's accumulator column (history slots < kPre and the BF16
     // slot) before anything that depends on them, so that they are all in flight at once.
@@ -127,7 +152,8 @@ __global__ void __launch_bounds__(128) merge_kernel(PartialsView p, const float 
 }  // namespace
 
 cudaError_t launch_merge(const oscar_layout_t &L, PartialsView p, const float *RV, int batch, uint16_t *out,
-                         float *out_f32, float *lse, cudaStream_t st) {
+                         float *out_f32, float *lse, cudaStream_t st, int32_t *counters, int expected,
+                         int32_t *status) {
     if (batch <= 0) return cudaSuccess;
     const int hq = L.n_kv_heads * L.gqa;
     const size_t smem = sizeof(float) * ((RV ? kQuarter * kPad : 0) + kHeadDim + 2 * (p.S + 1) + 8);
@@ -140,7 +166,8 @@ cudaError_t launch_merge(const oscar_layout_t &L, PartialsView p, const float *R
     cfg.stream = st;
     cfg.attrs = attrs;
     add_overlap_attr(cfg, attrs);
-    return cudaLaunchKernelEx(&cfg, merge_kernel, p, RV, hq, L.gqa, out, out_f32, lse);
+    return cudaLaunchKernelEx(&cfg, merge_kernel, p, RV, hq, L.gqa, out, out_f32, lse, counters, expected, batch,
+                              status);
 }
 
 }  // namespace oscar

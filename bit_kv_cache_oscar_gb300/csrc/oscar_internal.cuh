@@ -164,20 +164,13 @@ struct FusedDemotion {
     float cK, cV;
     Int2PoolMut dst;
 };
-// Merge done by the last cluster of each request (fused launch).  counters: int32 [batch],
-// zero before the launch and left zero.  *merged tells whether the launch merged (the stage area
-// of small layouts cannot hold the merge's scratch: then the caller runs the merge).
-struct FusedMerge {
-    int32_t *counters;
-    const float *RV;
-    uint16_t *out;
-    float *out_f32, *lse;
-};
 cudaError_t launch_decode_mma_demote(const oscar_layout_t &L, const float *RK, Int2PoolView pool, const int32_t *pt,
                                      const uint16_t *q, Bf16PoolView bpool, const int32_t *bpt, int max_pages,
                                      const int32_t *seq_len, const int32_t *hist_end, int batch, float sm_scale,
                                      PartialsView out, int32_t *status, const FusedDemotion &dem,
-                                     const FusedMerge *mg, bool *merged, cudaStream_t st);
+                                     int32_t *arrivals, int *clusters, cudaStream_t st);
+// (arrivals: NULL, or int32 [batch] to which each cluster of request b adds 1 once its partial
+// slot is written; *clusters gets the count per request that the merge then waits for)
 
 // Tensor-core BF16 kernel (mode 0 any n_kv_heads; mode 1 n_kv_heads in {1, 2, 4, 8}).
 bool bf16_mma_supported(const oscar_layout_t &L, int mode);
@@ -192,7 +185,12 @@ cudaError_t launch_bf16_attention(const oscar_layout_t &L, const uint16_t *q, Bf
                                   const int32_t *hist_end, int batch, float sm_scale, PartialsView out,
                                   int mode, int32_t *status, cudaStream_t st);
 
+// counters NULL: the merge waits for the previous kernel (programmatic dependent launch).  Else
+// int32 [2][batch], zero before the call and left zero: each request's merge starts once
+// counters[b] reaches `expected` (the decode launch's arrivals); counters[batch + b] counts the
+// merge CTAs of b that have seen it, and the last one resets both.
 cudaError_t launch_merge(const oscar_layout_t &L, PartialsView p, const float *RV, int batch, uint16_t *out,
-                         float *out_f32, float *lse, cudaStream_t st);
+                         float *out_f32, float *lse, cudaStream_t st, int32_t *counters = nullptr,
+                         int expected = 0, int32_t *status = nullptr);
 
 }  // namespace oscar

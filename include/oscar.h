@@ -287,12 +287,16 @@ OSCAR_API oscar_status_t oscar_decode_attention(const oscar_layout_t *layout,
  * R_V NULL (the value rotation folded into the projections): the demotion
  * stores values as they are and the merge does not rotate back.
  *
- * Optional merge: with out or out_f32 non-NULL the call also produces oscar_merge's
- * output (same bits; lse optional).  With merge_counters (int32
- * [batch], all zero; the call leaves them zero) the cluster of each request that
- * finishes last merges it inside the same launch; without them, with R_V NULL, or
- * when the layout's stage buffers cannot hold the merge's scratch, oscar_merge
- * runs as a second launch.  Calls that may run concurrently must not share merge_counters.
+ * Optional merge: with out or out_f32 non-NULL the call also runs oscar_merge (same
+ * bits; lse optional) as a second launch.  Without merge_counters that launch waits
+ * for the whole decode grid (programmatic dependent launch when launch overlap is
+ * on).  With merge_counters (int32 [2·batch], all zero; the call leaves them zero)
+ * each cluster of request b adds 1 to merge_counters[b] once its partial slot is
+ * written, and the merge of request b starts as soon as the count is complete
+ * (acquire load, bounded wait: OSCAR_DEV_WAIT_TIMEOUT), without waiting for the
+ * rest of the grid; merge_counters[batch + b] counts the merge CTAs that have
+ * passed, and the last one resets both.  Calls that may run concurrently must not
+ * share merge_counters.
  */
 OSCAR_API oscar_status_t oscar_decode_attention_fused(const oscar_layout_t *layout, const uint16_t *q,
                                                       const float *R_K, const oscar_bf16_pool_t *bf16_pool,

@@ -1,8 +1,8 @@
 """Parity at the workloads' full sizes, on sampled (request, query head) outputs.
 
 Each case runs the decode step exactly as bench.py does (oscar_decode_attention_fused
--> oscar_merge on one stream, launch overlap on, the library's split suggestion for
-the batch), then compares sampled heads with the
+with its merge started on the clusters' arrival counts, launch overlap on, the
+library's split suggestion for the batch), then compares sampled heads with the
 oracle's fp64 attention over its own demotion of those heads' history.  Samples
 always include the shortest and the longest request.  K/V are drawn on the GPU
 (the oracle reads back the sampled heads), so the same tensors feed both sides.
@@ -30,10 +30,12 @@ def _run_like_bench(case):
     out = torch.empty((B, L.n_q_heads, D), dtype=torch.bfloat16, device="cuda")
     try:
         ob.oscar_set_launch_overlap(True)
+        counters = torch.zeros(2 * B, dtype=torch.int32, device="cuda")
         ob.oscar_decode_attention_fused(L, dev["q"], dev["RK"], dev["bf16"], dev["bf16_table"], dev["int2"],
-                                        dev["int2_table"], dev["seq_len"], dev["hist_end"], case.sm_scale, part)
-        ob.oscar_merge(L, part, dev["RV"], out, out32, None)
+                                        dev["int2_table"], dev["seq_len"], dev["hist_end"], case.sm_scale, part,
+                                        R_V=dev["RV"], out=out, out_f32=out32, merge_counters=counters)
         torch.cuda.synchronize()
+        assert not counters.any()
     finally:
         ob.oscar_set_launch_overlap(False)
     assert ob.oscar_get_device_status() == 0

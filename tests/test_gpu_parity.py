@@ -350,12 +350,12 @@ def test_fused_demotion_matches_oscar_demote(n_kv, gqa, ps, group, seq, S):
     (8, 8, 16, 32, (1400,), 3),            # GQA 8, group 32
     (4, 2, 32, 64, (1800, 900), 4),
     (2, 4, 16, 128, (1200, 300), 3),        # a request with no history
-    (1, 1, 16, 128, (700,), 2),             # too small a stage area: the merge runs as its own launch
+    (1, 1, 16, 128, (700,), 2),             # one kv head
 ])
 def test_fused_merge_matches_oscar_merge(n_kv, gqa, ps, group, seq, S):
-    """The merge done by the last cluster of each request inside the decode launch gives
-    oscar_merge's bits (out, out_f32, lse), leaves the counters at zero, and repeated or
-    graph-captured calls with launch overlap agree."""
+    """The merge launched by the fused call, started per request on the decode clusters' arrival
+    counts, gives oscar_merge's bits (out, out_f32, lse), leaves the counters at zero, and repeated
+    or graph-captured calls (back to back on the same partials) with launch overlap agree."""
     case = sc.make_case(n_kv=n_kv, gqa=gqa, page_size=ps, group=group, seq=seq)
     sc.upload(case)
     L, dev = case.layout, case.dev
@@ -366,7 +366,7 @@ def test_fused_merge_matches_oscar_merge(n_kv, gqa, ps, group, seq, S):
     ref = [torch.empty((B, Hq, D), dtype=t, device="cuda") for t in (torch.bfloat16, torch.float32)]
     ref_lse = torch.empty((B, Hq), dtype=torch.float32, device="cuda")
     ob.oscar_merge(L, part, dev["RV"], ref[0], ref[1], ref_lse)
-    counters = torch.zeros(B, dtype=torch.int32, device="cuda")
+    counters = torch.zeros(2 * B, dtype=torch.int32, device="cuda")
 
     def fused(p2, outs):
         ob.oscar_decode_attention_fused(L, dev["q"], dev["RK"], dev["bf16"], dev["bf16_table"], dev["int2"],
