@@ -673,48 +673,55 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
     const int C = a.csize, rank = C > 1 ? (int)cluster_ctarank() : 0;
     float *qrot_s = reinterpret_cast<float *>(smem + a.rot_off);     // [Hq][kQS] rotated queries of the request
     if (a.RK) {
-        // q_rot = q . R_K for kv heads rank, rank + C, ...: thread (g0, j) runs the fp32 chain
-        // acc = fma(q[g][i], R_K[i][j], acc), i ascending, for heads g0, g0 + 2, ... (the same
-        // operations, in the same order, as oscar_rotate_q).
+        // q_rot = q . R_K for kv heads rank, rank + C, ...: thread j < 128 runs the fp32 chains
+        // acc_g = fma(q[g][i], R_K[i][j], acc_g), i ascending, for every query head g of the kv
+        // head (the same operations, in the same order, as oscar_rotate_q).  Each R_K element is
+        // read once and the queries come as 4-wide broadcast loads: the loop is bound by shared-
+        // memory issue, not by the chains.
         const uint32_t rk_full = saddr(smem + 96), rk_free = saddr(smem + 104);
         float *qs = reinterpret_cast<float *>(smem + 128);           // [G][128] (P-buffer area, free until the loop)
-        const int ctid = threadIdx.x, j = ctid & (kHeadDim - 1), g0 = ctid >> 7;
+        const int ctid = threadIdx.x, j = ctid & (kHeadDim - 1);
+        const bool rot = ctid < kHeadDim;
         const int rpc = a.rk_chunk / (kHeadDim * 4), nch = kHeadDim / rpc;
-        constexpr int NG = (G + 1) / 2;
         int n = 0;
         for (int hk = rank; hk < Hkv; hk += C) {
             consumer_sync();
             for (int e = ctid; e < G * kHeadDim; e += kCW * 32)
                 qs[e] = bf16_to_f32(a.q[((size_t)b * Hq + hk * G) * kHeadDim + e]);
             consumer_sync();
-            float racc[NG];
+            float racc[G];
 #pragma unroll
-            for (int k = 0; k < NG; ++k) racc[k] = 0.f;
+            for (int g = 0; g < G; ++g) racc[g] = 0.f;
             for (int c = 0; c < nch; ++c, ++n) {
                 if (!mbar_wait(rk_full, n & 1) && lane == 0) flag_status(a.status, OSCAR_DEV_WAIT_TIMEOUT);
                 const float *R = reinterpret_cast<const float *>(stage0);
-#pragma unroll 8
-                for (int i = 0; i < rpc; ++i) {
-                    const float rv = R[i * kHeadDim + j];
+                if (rot) {
+#pragma unroll 2
+                    for (int i = 0; i < rpc; i += 4) {
+                        const float r0 = R[(i + 0) * kHeadDim + j], r1 = R[(i + 1) * kHeadDim + j];
+                        const float r2 = R[(i + 2) * kHeadDim + j], r3 = R[(i + 3) * kHeadDim + j];
 #pragma unroll
-                    for (int k = 0; k < NG; ++k) {
-                        const int g = g0 + 2 * k;
-                        if (g < G) racc[k] = __fmaf_rn(qs[g * kHeadDim + c * rpc + i], rv, racc[k]);
+                        for (int g = 0; g < G; ++g) {
+                            const float4 qv = *reinterpret_cast<const float4 *>(qs + g * kHeadDim + c * rpc + i);
+                            racc[g] = __fmaf_rn(qv.x, r0, racc[g]);
+                            racc[g] = __fmaf_rn(qv.y, r1, racc[g]);
+                            racc[g] = __fmaf_rn(qv.z, r2, racc[g]);
+                            racc[g] = __fmaf_rn(qv.w, r3, racc[g]);
+                        }
                     }
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(rk_free);
             }
             // every CTA of the cluster gets the rows: stores to the peers need no round trip
+            if (rot) {
 #pragma unroll
-            for (int k = 0; k < NG; ++k) {
-                const int g = g0 + 2 * k;
-                if (g < G) {
+                for (int g = 0; g < G; ++g) {
                     float *dst = qrot_s + (hk * G + g) * kQS + qs_col(j);
                     if (C == 1) {
-                        *dst = racc[k];
+                        *dst = racc[g];
                     } else {
-                        for (int q = 0; q < C; ++q) st_dsmem_f32(saddr(dst), (uint32_t)q, racc[k]);
+                        for (int q = 0; q < C; ++q) st_dsmem_f32(saddr(dst), (uint32_t)q, racc[g]);
                     }
                 }
             }
