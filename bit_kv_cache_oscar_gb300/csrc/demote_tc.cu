@@ -91,7 +91,10 @@ struct TileWalk {
 // the chunk again through codes_chunk_exact.
 __device__ __forceinline__ float codes_chunk(const uint32_t (&v)[32], float z, float inv, uint32_t &w0,
                                              uint32_t &w1) {
-    constexpr float kMagic = 12582912.0f;               // 1.5 * 2^23
+    constexpr float kMagic = 12582912.0f;               // 1.5 * 2^23: y = kMagic + code, bits 0x4B400000 + code
+    // sum over the 16 codes of a word of bits(y) * 4^i carries 0x4B400000 * (4^16 - 1) / 3 (mod 2^32)
+    // besides the codes' own sum of code * 4^i; one subtraction per word removes it
+    constexpr uint32_t kBias = 0x4B400000u * 0x55555555u;
     uint32_t w[2] = {0u, 0u};
     float e4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
@@ -100,10 +103,10 @@ __device__ __forceinline__ float codes_chunk(const uint32_t (&v)[32], float z, f
         const float qc = fminf(fmaxf(__fmul_rn(d, inv), 0.0f), 3.0f);
         const float y = __fadd_rn(qc, kMagic);
         e4[i & 3] = fmaxf(e4[i & 3], fabsf(__fsub_rn(qc, __fsub_rn(y, kMagic))));
-        w[i >> 4] |= (__float_as_uint(y) & 3u) << (2 * (i & 15));
+        w[i >> 4] += __float_as_uint(y) * (1u << (2 * (i & 15)));
     }
-    w0 = w[0];
-    w1 = w[1];
+    w0 = w[0] - kBias;
+    w1 = w[1] - kBias;
     return fmaxf(fmaxf(e4[0], e4[1]), fmaxf(e4[2], e4[3]));
 }
 
@@ -286,22 +289,17 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
         int b, t, lo, hi;
         int n = 0;
         for (int i = cta + eg * cpp; wk.find(a, i, b, t, lo, hi); i += kEpiGroups * cpp, ++n) {
-            // where this row goes (all threads still take part in the warp-wide TMEM loads)
+            // where this row goes (all threads still take part in the warp-wide TMEM loads): the page
+            // ids are loaded now, for a position inside the range, and looked at after the passes
             const int p = t * kTileRows + r;
-            bool ok = p >= lo && p < hi;
-            size_t slot_row = 0;
-            if (ok) {
-                const int lp = p / ps, slot = p % ps;
-                const int sp = a.bf16_pt[(size_t)b * a.max_pages + lp];
-                const int dp = a.int2_pt[(size_t)b * a.max_pages + lp];
-                if (sp < 0 || sp >= a.bf16_pages) {
-                    ok = false;                    // flagged by the producer
-                } else if (dp < 0 || dp >= a.dst.n_pages) {
-                    flag_status(a.status, OSCAR_DEV_BAD_INT2_PAGE);
-                    ok = false;
-                }
-                slot_row = (size_t)dp * ps + slot;
-            }
+            const bool in_range = p >= lo && p < hi;
+            const int lp = (in_range ? p : lo) / ps, slot = p % ps;
+            const int sp = a.bf16_pt[(size_t)b * a.max_pages + lp];
+            const int dp = a.int2_pt[(size_t)b * a.max_pages + lp];
+            auto row_ok = [&]() {                  // (a bad BF16 page is flagged by the producer)
+                return in_range && sp >= 0 && sp < a.bf16_pages && dp >= 0 && dp < a.dst.n_pages;
+            };
+            const size_t slot_row = (size_t)(dp < 0 ? 0 : dp) * ps + slot;
             if (!mbar_wait(bar_accf + 8 * eg, n & 1) && lane == 0) flag_status(a.status, OSCAR_DEV_WAIT_TIMEOUT);
             __syncwarp();
             tc_fence_after();
@@ -334,7 +332,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
                         gmn[g] = fminf(gmn[g], cmn);
                         gmx[g] = fmaxf(gmx[g], cmx);
                     }
-                if (a.rot_out && ok) {
+                if (a.rot_out && row_ok()) {
                     float4 *o = reinterpret_cast<float4 *>(a.rot_out + ((slot_row * 2 + kind) * a.n_kv + head) * kHeadDim) + 8 * c;
 #pragma unroll
                     for (int k = 0; k < 8; ++k)
@@ -391,7 +389,9 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
             }
             tc_fence_before();
             mbar_arrive(bar_acce + 8 * eg);        // the MMA may overwrite the accumulator
-            if (!ok) continue;
+            if (in_range && sp >= 0 && sp < a.bf16_pages && (dp < 0 || dp >= a.dst.n_pages))
+                flag_status(a.status, OSCAR_DEV_BAD_INT2_PAGE);
+            if (!row_ok()) continue;
             const size_t row = slot_row * a.n_kv + head;
             uint4 *cdst = reinterpret_cast<uint4 *>(codes + row * (kHeadDim / 4));
             cdst[0] = make_uint4(w[0], w[1], w[2], w[3]);
