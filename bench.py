@@ -2,7 +2,8 @@
 """Decode-attention benchmark of the OSCAR INT2 KV-cache path on GB300.
 
 One step = the attention of one decode token for every layer of the model:
-per layer, q·R_K + INT2 history + BF16 sink/recent partials in one launch
+per layer, q·R_K + INT2 history (64-token units taken dynamically by the
+history CTAs) + BF16 sink/recent partials in one launch
 (oscar_decode_attention_fused), then the online-softmax merge with R_V^T
 (oscar_merge); for workloads that demote every step, the demotion of the
 token leaving the recent window runs inside the same decode launch.
@@ -218,6 +219,7 @@ class Model:
         self.out_all = torch.empty((w.layers, B, w.n_q_heads, D), dtype=torch.bfloat16, device=device)
         self.q_rot = torch.empty((B, w.n_q_heads, D), dtype=torch.float32, device=device)
         self.part = ob.Partials.empty(L, B, self.S, device)
+        self.tiles = torch.zeros(2 * B, dtype=torch.int32, device=device)   # dynamic history scheduling
         self.layers = []
         self.bf16_full = [] if with_bf16_cache else None
         max_pages = self.pages.int2_table.shape[1]
@@ -280,14 +282,15 @@ class Model:
         for l, st in enumerate(self.layers):
             if events is not None:
                 events[l][0].record()
-            # query rotation, history splits, the BF16 window (and the per-step demotion) in one
-            # launch, the merge in a second one after the whole grid (programmatic dependent launch).
-            # Starting each request's merge on its clusters' arrival counts (merge_counters=...)
-            # measured 3 % slower per step at batch 1, the in-launch merge by the last cluster 34 %.
+            # query rotation, the history in 64-token units taken dynamically by the history CTAs,
+            # the BF16 window (and the per-step demotion) in one launch; the merge in a second one
+            # after the whole grid (programmatic dependent launch).  Starting each request's merge on
+            # its clusters' arrival counts (merge_counters=...) measured 3 % slower per step at
+            # batch 1; fixed history splits (tile_counters=None) 1.4 % slower.
             ob.oscar_decode_attention_fused(L, self.q_all[l], st["RK"], st["bf16"], self.bf16_table, st["int2"],
                                             self.int2_table, self.seq_len, self.hist_dev, self.sm_scale, self.part,
                                             demote_pos=self.dem_pos if demote else None, R_V=st["RV"],
-                                            c_K=0.96, c_V=0.92)
+                                            c_K=0.96, c_V=0.92, tile_counters=self.tiles)
             if events is not None:
                 events[l][1].record()
             ob.oscar_merge(L, self.part, st["RV"], self.out_all[l])
@@ -607,7 +610,7 @@ def main():
             "bytes_per_step": bts["per_step"],
             "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                          "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                         "kernel": "oscar_decode_attention_fused (q.R_K + INT2 history split-K + BF16 window, one layer, one launch)",
+                         "kernel": "oscar_decode_attention_fused (q.R_K + INT2 history split-K in dynamic 64-token units + BF16 window, one layer, one launch)",
                          "bytes_per_launch": unit_bytes, "launch_us": dur * 1e6,
                          "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs copy bandwidth)"},
             "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": model.launches_per_step() * args.steps,

@@ -105,7 +105,7 @@ def lib():
     L.oscar_version.restype = ctypes.c_char_p
     L.oscar_decode_attention_fused.argtypes = [P(LayoutC), vp, vp, P(Bf16PoolC), vp, P(Int2PoolC), vp, i32, vp,
                                                vp, i32, ctypes.c_float, P(PartialsC), vp, vp, ctypes.c_float,
-                                               ctypes.c_float, vp, vp, vp, vp, vp]
+                                               ctypes.c_float, vp, vp, vp, vp, vp, vp]
     L.oscar_decode_attention_fused.restype = st
     L.oscar_set_launch_overlap.argtypes = [i32]
     L.oscar_set_launch_overlap.restype = st
@@ -285,13 +285,16 @@ def oscar_decode_attention_fused(layout: Layout, q: torch.Tensor, R_K: torch.Ten
                                  demote_pos: Optional[torch.Tensor] = None, R_V: Optional[torch.Tensor] = None,
                                  c_K: float = 0.0, c_V: float = 0.0, out: Optional[torch.Tensor] = None,
                                  out_f32: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
-                                 merge_counters: Optional[torch.Tensor] = None, stream=None):
+                                 merge_counters: Optional[torch.Tensor] = None,
+                                 tile_counters: Optional[torch.Tensor] = None, stream=None):
     """oscar_decode_attention with q . R_K computed inside the launch (same partials bits); with
     demote_pos ([batch] int32, -1 = none) also the per-step demotion of those positions; with
     out / out_f32 also oscar_merge's output, from a second launch that starts each request's
-    merge on its arrival count when merge_counters (int32 zeros [2 * batch]) is given."""
-    if merge_counters is not None and merge_counters.numel() < 2 * int(q.shape[0]):
-        raise OscarError("oscar_decode_attention_fused: merge_counters needs 2 * batch int32 entries")
+    merge on its arrival count when merge_counters (int32 zeros [2 * batch]) is given; with
+    tile_counters (int32 zeros [2 * batch]) the history CTAs take 64-token units dynamically."""
+    for name, t in (("merge_counters", merge_counters), ("tile_counters", tile_counters)):
+        if t is not None and t.numel() < 2 * int(q.shape[0]):
+            raise OscarError(f"oscar_decode_attention_fused: {name} needs 2 * batch int32 entries")
     _check("oscar_decode_attention_fused", lib().oscar_decode_attention_fused(
         ctypes.byref(layout.c()), _ptr(q), _ptr(R_K), ctypes.byref(bf16_pool.c()), _ptr(bf16_page_table),
         ctypes.byref(int2_pool.c()), _ptr(int2_page_table), int(int2_page_table.shape[-1]), _ptr(seq_len),
@@ -299,7 +302,8 @@ def oscar_decode_attention_fused(layout: Layout, q: torch.Tensor, R_K: torch.Ten
         _ptr(demote_pos) if demote_pos is not None else None, _ptr(R_V) if R_V is not None else None,
         float(c_K), float(c_V), _ptr(out) if out is not None else None,
         _ptr(out_f32) if out_f32 is not None else None, _ptr(lse) if lse is not None else None,
-        _ptr(merge_counters) if merge_counters is not None else None, _stream(stream)))
+        _ptr(merge_counters) if merge_counters is not None else None,
+        _ptr(tile_counters) if tile_counters is not None else None, _stream(stream)))
 
 
 def oscar_decode_attention_history(layout: Layout, q_rot: torch.Tensor, int2_pool: Int2Pool,

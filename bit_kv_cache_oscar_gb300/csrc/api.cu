@@ -292,7 +292,8 @@ oscar_status_t oscar_decode_attention_fused(const oscar_layout_t *layout, const 
                                             const int32_t *hist_end, int32_t batch, float sm_scale,
                                             const oscar_partials_t *partials, const int32_t *demote_pos,
                                             const float *R_V, float c_K, float c_V, uint16_t *out,
-                                            float *out_f32, float *lse, int32_t *merge_counters, void *stream) {
+                                            float *out_f32, float *lse, int32_t *merge_counters,
+                                            int32_t *tile_counters, void *stream) {
     TRY(check_layout(layout));
     TRY(check_bf16_pool(bf16_pool));
     TRY(check_int2_pool(int2_pool));
@@ -322,7 +323,8 @@ oscar_status_t oscar_decode_attention_fused(const oscar_layout_t *layout, const 
     cudaError_t e = oscar::launch_decode_mma_demote(*layout, R_K, int2_view(int2_pool), int2_page_table, q,
                                                     bf16_view(bf16_pool), bf16_page_table, max_pages_per_req,
                                                     seq_len, hist_end, batch, sm_scale, part_view(partials),
-                                                    status_ptr(), dem, arrivals, &clusters, (cudaStream_t)stream);
+                                                    status_ptr(), dem, arrivals, &clusters, tile_counters,
+                                                    (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_status(e, "fused decode attention launch");
     if (merge)
         return cuda_status(oscar::launch_merge(*layout, part_view(partials), R_V, batch, out, out_f32, lse,

@@ -132,6 +132,8 @@ struct MmaArgs {
     int group;
     // per-request arrival counts for the merge launch (NULL: the merge waits for the whole grid)
     int32_t *arrivals;          // [batch]: +1 per cluster once its partial slot is written
+    // dynamic tile scheduling (NULL: fixed splits): [batch] units taken, [batch] CTAs done
+    int32_t *sched;
     Bf16PoolView bpool;         // BF16 sink/recent pool and its page table (window CTAs)
     const int32_t *bpt;
 };
@@ -445,6 +447,58 @@ __device__ void window_demote(const MmaArgs &a, float *small, uint8_t *area, int
     }
 }
 
+// ---- The same per-step demotion of kv head hk (K and V), done by the consumer warps 0..3 of a
+// history CTA before its main loop (with dynamic history units, whose sharing absorbs the delay).
+// R is read from global memory (L2: every request's demotion reads it); the stage area holds
+// the KV stream.  xs: 136 floats of free shared memory.  Threads 0..127 call this.
+__device__ void history_demote(const MmaArgs &a, float *xs, int T, int he, int b, int hk) {
+    const int tid = threadIdx.x;
+    const int Hkv = a.n_kv, ps = a.page_size;
+    const int p = a.dem.dem_pos[b];
+    if (p < 0) return;
+    int sp = -1, dp = -1;
+    const bool in_range = p >= he && p < T && p / ps < a.max_pages;
+    if (in_range) {
+        sp = a.bpt[(size_t)b * a.max_pages + p / ps];
+        dp = a.pt[(size_t)b * a.max_pages + p / ps];
+    }
+    if (!in_range || sp < 0 || sp >= a.bpool.n_pages || dp < 0 || dp >= a.dem.dst.n_pages) {
+        if (tid == 0)
+            flag_status(a.status, !in_range ? OSCAR_DEV_BAD_LENGTH
+                                            : (sp < 0 || sp >= a.bpool.n_pages) ? OSCAR_DEV_BAD_BF16_PAGE
+                                                                                : OSCAR_DEV_BAD_INT2_PAGE);
+        return;
+    }
+    float *red = xs + kHeadDim;
+    const int gpr = kHeadDim / a.group;
+    const size_t srow = ((size_t)sp * ps + p % ps) * Hkv + hk, drow = ((size_t)dp * ps + p % ps) * Hkv + hk;
+    auto sync128 = [] { asm volatile("bar.sync 2, 128;" ::: "memory"); };
+    for (int which = 0; which < 2; ++which) {
+        const float *Rb = which ? a.dem.RV : a.RK;       // NULL R_V: values stored as they are
+        sync128();                                       // the previous row's xs is consumed
+        xs[tid] = bf16_to_f32((which ? a.bpool.v : a.bpool.k)[srow * kHeadDim + tid]);
+        sync128();
+        float y = 0.f;
+        if (!Rb) {
+            y = xs[tid];
+        } else {
+            const float *R = Rb + (size_t)hk * kHeadDim * kHeadDim + tid;
+            for (int i0 = 0; i0 < kHeadDim; i0 += 16) {
+                float rv[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u) rv[u] = __ldg(R + (size_t)(i0 + u) * kHeadDim);
+#pragma unroll
+                for (int u = 0; u < 16; ++u) y = __fmaf_rn(xs[i0 + u], rv[u], y);
+            }
+        }
+        uint8_t *codes = which ? a.dem.dst.codes_v : a.dem.dst.codes_k;
+        uint16_t *scale = which ? a.dem.dst.scale_v : a.dem.dst.scale_k;
+        uint16_t *zero = which ? a.dem.dst.zero_v : a.dem.dst.zero_k;
+        quantize_row_store(y, which ? a.dem.cV : a.dem.cK, a.group, true, codes + drow * (kHeadDim / 4),
+                           scale + drow * gpr, zero + drow * gpr, red, tid, sync128);
+    }
+}
+
 // ---- Arrival count for the merge launch: once every CTA of the cluster has written its part of
 // the cluster's partial slot, one thread adds 1 to arrivals[b].  The fence orders each thread's
 // slot writes before the cluster barrier, and the barrier before the count (release at gpu
@@ -508,13 +562,22 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
         window_cta<G>(a, reinterpret_cast<float *>(stage0 + a.win_off), reinterpret_cast<float *>(stage0 + a.res_off),
                       T, he, b, (int)blockIdx.x, a.win_ctas);
         // (after the cluster's last barrier: the stage area is free again)
-        if (a.dem.dem_pos)
+        if (a.dem.dem_pos && !(a.sched && a.hist_ctas >= Hkv))
             window_demote(a, reinterpret_cast<float *>(smem + 128), stage0, T, he, b, (int)blockIdx.x, a.win_ctas);
         if (a.arrivals) arrive_count(a, b);
         return;
     }
     const SplitRange r = history_split(a.sink, he, a.hist_ctas, s);   // C sub-splits per slot
     const int n_iters = (r.tile_hi - r.tile_lo + kTilesPerStage - 1) / kTilesPerStage;
+    // Dynamic scheduling: the copy warps of all of b's history CTAs take units of kTilesPerStage
+    // tiles of the whole history [sink, he) from a shared counter, so that CTAs that run faster
+    // (an SM to themselves) take more; each stage carries its first tile (or -1: no more).
+    const bool dyn = a.sched != nullptr;
+    const int hist_first = a.sink / kTileTokens;   // the history starts on a tile boundary
+    const int hist_tile_hi = (he + kTileTokens - 1) / kTileTokens;
+    const int dyn_units = hist_tile_hi > hist_first ? (hist_tile_hi - hist_first + kTilesPerStage - 1) / kTilesPerStage : 0;
+    const int tok_hi = dyn ? he : r.hi, tile_hi = dyn ? hist_tile_hi : r.tile_hi;
+    int *stage_tile = reinterpret_cast<int *>(smem + 80);     // per stage: first tile, -1 = the end
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < a.stages; ++i) {
@@ -563,14 +626,48 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
         const int tpp = a.page_size / kTileTokens;           // tiles per page
         const int tile_bytes = 2 * kTileTokens * 8 * 32 + 4 * kTileTokens * 8 * NGRP * 2;   // TMA path (8 heads)
         const int32_t *prow = a.pt + (size_t)b * a.max_pages;
-        int pg_base = r.tile_lo / tpp;
+        int pg_base = (dyn ? hist_first : r.tile_lo) / tpp;
         int pg_reg = (pg_base + lane < a.max_pages) ? prow[pg_base + lane] : -1;
+        // dynamic units: the next unit and its tiles' page ids (lane j < kTilesPerStage: tile
+        // t0 + j) are taken one stage ahead, so that the count and the table loads overlap the wait
+        auto take_unit = [&](int &nt0, int &npg) {
+            int u = 0;
+            if (lane == 0) u = atomicAdd(a.sched + b, 1);
+            u = __shfl_sync(0xffffffffu, u, 0);
+            nt0 = u < dyn_units ? hist_first + u * kTilesPerStage : -1;
+            const int tile = nt0 + lane;
+            npg = (nt0 >= 0 && lane < kTilesPerStage && tile < tile_hi) ? prow[tile / tpp] : -1;
+        };
+        int nxt_t0 = -1, nxt_pg = -1;
+        if (dyn) take_unit(nxt_t0, nxt_pg);
         bool ok = true;
-        for (int it = 0; it < n_iters && ok; ++it) {
+        for (int it = 0; ok; ++it) {
             const int st = it % a.stages;
             if (it >= a.stages && !mbar_wait(saddr(&bars[4 + st]), ((it / a.stages) - 1) & 1)) {
                 if (lane == 0) flag_status(a.status, OSCAR_DEV_WAIT_TIMEOUT);
                 ok = false;
+                break;
+            }
+            int t0, unit_pg = -1;                              // this stage's first tile, -1: no more
+            if (dyn) {
+                t0 = nxt_t0;
+                unit_pg = nxt_pg;
+                if (t0 >= 0) take_unit(nxt_t0, nxt_pg);
+            } else {
+                t0 = it < n_iters ? r.tile_lo + it * kTilesPerStage : -1;
+            }
+            if (lane == 0) stage_tile[st] = t0;
+            if (t0 < 0) {                                      // an empty stage marks the end
+                if constexpr (TMA) {
+                    if (lane == 0) {
+                        masks[st] = 0;
+                        mbar_arrive_expect_tx(saddr(&bars[st]), 0);
+                    }
+                } else {
+                    if (lane == 0) masks[st] = 0;
+                    cp_async_arrive(saddr(&bars[st]));
+                    if (lane == 0) mbar_arrive(saddr(&bars[st]));
+                }
                 break;
             }
             uint8_t *sb = stage0 + st * stage_bytes;
@@ -580,14 +677,15 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
                 const int jl = lane >> 3, op = lane & 7;
                 int row0 = 0;
                 for (int j = 0; j < kTilesPerStage; ++j) {
-                    const int tile = r.tile_lo + it * kTilesPerStage + j;
-                    if (tile >= r.tile_hi) break;
+                    const int tile = t0 + j;
+                    if (tile >= tile_hi) break;
                     const int lp = tile / tpp;
-                    if (lp - pg_base >= 32) {
+                    if (!dyn && lp - pg_base >= 32) {
                         pg_base = lp;
                         pg_reg = (pg_base + lane < a.max_pages) ? prow[pg_base + lane] : -1;
                     }
-                    const int page = __shfl_sync(0xffffffffu, pg_reg, lp - pg_base);
+                    const int page = dyn ? __shfl_sync(0xffffffffu, unit_pg, j)
+                                         : __shfl_sync(0xffffffffu, pg_reg, lp - pg_base);
                     if (page < 0 || page >= a.pool.n_pages) {
                         if (lane == 0) flag_status(a.status, OSCAR_DEV_BAD_INT2_PAGE);
                         continue;
@@ -617,15 +715,16 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
                 continue;
             }
             for (int j = 0; j < kTilesPerStage; ++j) {
-                const int tile = r.tile_lo + it * kTilesPerStage + j;
-                if (tile >= r.tile_hi) break;
+                const int tile = t0 + j;
+                if (tile >= tile_hi) break;
                 const int pos0 = tile * kTileTokens;
                 const int lp = tile / tpp;
-                if (lp - pg_base >= 32) {                      // warp-uniform refill of the page window
+                if (!dyn && lp - pg_base >= 32) {              // warp-uniform refill of the page window
                     pg_base = lp;
                     pg_reg = (pg_base + lane < a.max_pages) ? prow[pg_base + lane] : -1;
                 }
-                const int page = __shfl_sync(0xffffffffu, pg_reg, lp - pg_base);
+                const int page = dyn ? __shfl_sync(0xffffffffu, unit_pg, j)
+                                     : __shfl_sync(0xffffffffu, pg_reg, lp - pg_base);
                 if (page < 0 || page >= a.pool.n_pages) {
                     if (lane == 0) flag_status(a.status, OSCAR_DEV_BAD_INT2_PAGE);
                     continue;
@@ -659,6 +758,12 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
             if (lane == 0) mbar_arrive(saddr(&bars[st]));
         }
         asm volatile("cp.async.wait_all;" ::: "memory");
+        // the last of b's history CTAs to stop taking units resets b's counters for the next launch
+        if (dyn && lane == 0 && atomicAdd(a.sched + gridDim.y + b, 1) == a.hist_ctas - 1) {
+            a.sched[b] = 0;
+            a.sched[gridDim.y + b] = 0;
+            __threadfence();
+        }
         if (a.csize > 1) cluster_combine(a, reinterpret_cast<const float *>(stage0 + a.res_off), Hq, b, s / a.csize);
         if (a.arrivals) arrive_count(a, b);
         return;
@@ -728,6 +833,9 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
         }
         if (C > 1) cluster_sync_all(); else consumer_sync();
     }
+    // with dynamic history units the per-step demotion of kv head s is done here, by history CTA s
+    if (a.dem.dem_pos && a.sched && a.hist_ctas >= Hkv && s < Hkv && threadIdx.x < kHeadDim)
+        history_demote(a, reinterpret_cast<float *>(smem + 128), T, he, b, s);
     // rotated query element (hq, d): the previous kernel's q_rot, or this CTA's copy of the rows
     auto qrot = [&](int hq, int d) -> float {
         return a.RK ? qrot_s[hq * kQS + qs_col(d)] : a.q_rot[((size_t)b * Hq + hq) * kHeadDim + d];
@@ -853,11 +961,13 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
     }
 
     int st = 0, ph = 0;                          // stage and its phase parity, stepped (no division)
-    for (int it = 0; it < n_iters; ++it, st = (st + 1 == a.stages) ? 0 : st + 1, ph ^= (st == 0)) {
+    for (;; st = (st + 1 == a.stages) ? 0 : st + 1, ph ^= (st == 0)) {
         if (!mbar_wait(saddr(&bars[st]), ph)) {
             if (lane == 0) flag_status(a.status, OSCAR_DEV_WAIT_TIMEOUT);
             break;
         }
+        const int t0 = stage_tile[st];
+        if (t0 < 0) break;                        // the copy warp has no more tiles
         const uint8_t *sb = stage0 + st * stage_bytes;
         const int mask = masks[st];
         // this warp's tiles of the stage: sub, sub + nsub, ...; taken two at a time (32 tokens)
@@ -954,15 +1064,15 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
             }
 
             // ---- logits of 4 tokens per thread, online softmax over the 32 tokens, P*scale -> Ws.
-            // Tiles start inside [r.lo, r.hi) (r.lo is a tile boundary), so a token is valid when its
-            // tile holds data and it lies below r.hi.  The running maximum is raised only when the
+            // Tiles start inside the range (its start is a tile boundary), so a token is valid when
+            // its tile holds data and it lies below the range's end.  The running maximum is raised only when the
             // pass's maximum exceeds it by more than kLazy (so P <= 2^kLazy and most passes skip the
             // rescale); the true maximum is tracked alongside and restored at the end.
             float alpha[NT];
             int lim[2];
 #pragma unroll
             for (int u = 0; u < 2; ++u)
-                lim[u] = uok[u] ? r.hi - (r.tile_lo + it * kTilesPerStage + jt[u]) * kTileTokens : 0;
+                lim[u] = uok[u] ? tok_hi - (t0 + jt[u]) * kTileTokens : 0;
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) {
                 float tv[2][2];
@@ -1398,7 +1508,7 @@ static cudaError_t decode_mma_impl(const oscar_layout_t &L, const float *RK, Int
                                    const int32_t *seq_len, const int32_t *hist_end, int batch, float sm_scale,
                                    PartialsView out, int32_t *status, const FusedDemotion &dem, cudaStream_t st,
                                    const float *q_rot, bool history, bool window, int32_t *arrivals,
-                                   int *clusters);
+                                   int *clusters, int32_t *sched);
 
 cudaError_t launch_decode_mma(const oscar_layout_t &L, const float *q_rot, const float *RK, Int2PoolView pool,
                               const int32_t *pt, const uint16_t *q, Bf16PoolView bpool, const int32_t *bpt,
@@ -1407,16 +1517,16 @@ cudaError_t launch_decode_mma(const oscar_layout_t &L, const float *q_rot, const
                               cudaStream_t st) {
     FusedDemotion none{};
     return decode_mma_impl(L, RK, pool, pt, q, bpool, bpt, max_pages, seq_len, hist_end, batch, sm_scale, out, status,
-                           none, st, q_rot, history, window, nullptr, nullptr);
+                           none, st, q_rot, history, window, nullptr, nullptr, nullptr);
 }
 
 cudaError_t launch_decode_mma_demote(const oscar_layout_t &L, const float *RK, Int2PoolView pool, const int32_t *pt,
                                      const uint16_t *q, Bf16PoolView bpool, const int32_t *bpt, int max_pages,
                                      const int32_t *seq_len, const int32_t *hist_end, int batch, float sm_scale,
                                      PartialsView out, int32_t *status, const FusedDemotion &dem,
-                                     int32_t *arrivals, int *clusters, cudaStream_t st) {
+                                     int32_t *arrivals, int *clusters, int32_t *sched, cudaStream_t st) {
     return decode_mma_impl(L, RK, pool, pt, q, bpool, bpt, max_pages, seq_len, hist_end, batch, sm_scale, out, status,
-                           dem, st, nullptr, true, true, arrivals, clusters);
+                           dem, st, nullptr, true, true, arrivals, clusters, sched);
 }
 
 static cudaError_t decode_mma_impl(const oscar_layout_t &L, const float *RK, Int2PoolView pool, const int32_t *pt,
@@ -1424,11 +1534,12 @@ static cudaError_t decode_mma_impl(const oscar_layout_t &L, const float *RK, Int
                                    const int32_t *seq_len, const int32_t *hist_end, int batch, float sm_scale,
                                    PartialsView out, int32_t *status, const FusedDemotion &dem, cudaStream_t st,
                                    const float *q_rot, bool history, bool window, int32_t *arrivals,
-                                   int *clusters) {
+                                   int *clusters, int32_t *sched) {
     if (clusters) *clusters = 0;
     if (batch <= 0 || (!history && !window)) return cudaSuccess;
     MmaArgs a{};
     if (history && window) a.arrivals = arrivals;
+    if (history) a.sched = sched;
     a.RK = RK;
     a.dem = dem;
     a.group = L.group;

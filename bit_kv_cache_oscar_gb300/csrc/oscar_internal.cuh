@@ -168,9 +168,11 @@ cudaError_t launch_decode_mma_demote(const oscar_layout_t &L, const float *RK, I
                                      const uint16_t *q, Bf16PoolView bpool, const int32_t *bpt, int max_pages,
                                      const int32_t *seq_len, const int32_t *hist_end, int batch, float sm_scale,
                                      PartialsView out, int32_t *status, const FusedDemotion &dem,
-                                     int32_t *arrivals, int *clusters, cudaStream_t st);
+                                     int32_t *arrivals, int *clusters, int32_t *sched, cudaStream_t st);
 // (arrivals: NULL, or int32 [batch] to which each cluster of request b adds 1 once its partial
-// slot is written; *clusters gets the count per request that the merge then waits for)
+// slot is written; *clusters gets the count per request that the merge then waits for.
+// sched: NULL (fixed history splits) or int32 [2][batch], zero and left zero: the history CTAs
+// take 64-token units from a shared per-request counter)
 
 // Tensor-core BF16 kernel (mode 0 any n_kv_heads; mode 1 n_kv_heads in {1, 2, 4, 8}).
 bool bf16_mma_supported(const oscar_layout_t &L, int mode);

@@ -297,6 +297,17 @@ OSCAR_API oscar_status_t oscar_decode_attention(const oscar_layout_t *layout,
  * rest of the grid; merge_counters[batch + b] counts the merge CTAs that have
  * passed, and the last one resets both.  Calls that may run concurrently must not
  * share merge_counters.
+ *
+ * Optional dynamic scheduling: with tile_counters (int32 [2·batch], all zero; the
+ * call leaves them zero) the history is not cut into fixed splits: the CTAs of
+ * request b take units of 64 tokens of [sink, hist_end[b]) in turn from the shared
+ * count tile_counters[b] (tile_counters[batch + b] counts the CTAs that are done;
+ * the last one resets both), so that CTAs that run faster take more.  Each history
+ * slot then holds the partial of whichever units its CTAs took: only the merged
+ * result is defined (the same up to fp32 rounding order).  The per-step demotion,
+ * if any, then runs in the first history CTAs of the request (one kv head each),
+ * whose delay the shared units absorb; its bytes are the same.  Calls that may run
+ * concurrently must not share tile_counters.
  */
 OSCAR_API oscar_status_t oscar_decode_attention_fused(const oscar_layout_t *layout, const uint16_t *q,
                                                       const float *R_K, const oscar_bf16_pool_t *bf16_pool,
@@ -308,7 +319,8 @@ OSCAR_API oscar_status_t oscar_decode_attention_fused(const oscar_layout_t *layo
                                                       const oscar_partials_t *partials,
                                                       const int32_t *demote_pos, const float *R_V, float c_K,
                                                       float c_V, uint16_t *out, float *out_f32, float *lse,
-                                                      int32_t *merge_counters, void *stream);
+                                                      int32_t *merge_counters, int32_t *tile_counters,
+                                                      void *stream);
 
 /*
  * The two halves of oscar_decode_attention, for callers that run them on two

@@ -1,8 +1,8 @@
 """Parity at the workloads' full sizes, on sampled (request, query head) outputs.
 
 Each case runs the decode step exactly as bench.py does (oscar_decode_attention_fused
-with its merge started on the clusters' arrival counts, launch overlap on, the
-library's split suggestion for the batch), then compares sampled heads with the
+with the history taken in dynamic 64-token units, then oscar_merge, launch overlap on,
+the library's split suggestion for the batch), then compares sampled heads with the
 oracle's fp64 attention over its own demotion of those heads' history.  Samples
 always include the shortest and the longest request.  K/V are drawn on the GPU
 (the oracle reads back the sampled heads), so the same tensors feed both sides.
@@ -20,7 +20,7 @@ pytestmark = pytest.mark.gpu
 D = 128
 
 
-def _run_like_bench(case):
+def _run_like_bench(case, dynamic=True):
     L, dev = case.layout, case.dev
     B = len(case.seq)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
@@ -30,12 +30,13 @@ def _run_like_bench(case):
     out = torch.empty((B, L.n_q_heads, D), dtype=torch.bfloat16, device="cuda")
     try:
         ob.oscar_set_launch_overlap(True)
-        counters = torch.zeros(2 * B, dtype=torch.int32, device="cuda")
+        tiles = torch.zeros(2 * B, dtype=torch.int32, device="cuda") if dynamic else None
         ob.oscar_decode_attention_fused(L, dev["q"], dev["RK"], dev["bf16"], dev["bf16_table"], dev["int2"],
                                         dev["int2_table"], dev["seq_len"], dev["hist_end"], case.sm_scale, part,
-                                        R_V=dev["RV"], out=out, out_f32=out32, merge_counters=counters)
+                                        tile_counters=tiles)
+        ob.oscar_merge(L, part, dev["RV"], out, out32, None)
         torch.cuda.synchronize()
-        assert not counters.any()
+        assert tiles is None or not tiles.any()
     finally:
         ob.oscar_set_launch_overlap(False)
     assert ob.oscar_get_device_status() == 0
@@ -64,13 +65,15 @@ def _pairs(seq, gqa, kv_heads, per_head=2):
     return pairs
 
 
-def test_fullsize_qwen3_8b_100k():
-    """The benchmark's workload: 32 q / 8 kv heads, one request of 100,000 tokens, page 64."""
+@pytest.mark.parametrize("dynamic", [False, True])
+def test_fullsize_qwen3_8b_100k(dynamic):
+    """The benchmark's workload: 32 q / 8 kv heads, one request of 100,000 tokens, page 64; fixed
+    history splits and dynamic 64-token units."""
     w = syn.WORKLOADS["qwen3_8b_100k"]
     case = sc.make_case(n_kv=w.n_kv_heads, gqa=w.n_q_heads // w.n_kv_heads, page_size=w.page_size,
                         group=w.group, seq=(w.context,), gen_device="cuda")
     sc.upload(case, keep_rotated=False)
-    out, out32 = _run_like_bench(case)
+    out, out32 = _run_like_bench(case, dynamic)
     pairs = [(0, hq) for hq in (0, 3, 9, 14, 17, 22, 28, 31)]     # kv heads 0, 2, 4, 7
     _check(case, out, out32, pairs)
 

@@ -314,7 +314,8 @@ def _pool_bytes(i2):
 ])
 def test_fused_demotion_matches_oscar_demote(n_kv, gqa, ps, group, seq, S):
     """The per-step demotion done by the decode launch writes the bytes oscar_demote writes, and
-    leaves that step's partials unchanged."""
+    leaves that step's partials unchanged; with dynamic history units (the demotion then runs in
+    the first history CTAs) it writes the same bytes."""
     case = sc.make_case(n_kv=n_kv, gqa=gqa, page_size=ps, group=group, seq=seq)
     sc.upload(case)
     L, dev = case.layout, case.dev
@@ -342,6 +343,18 @@ def test_fused_demotion_matches_oscar_demote(n_kv, gqa, ps, group, seq, S):
     torch.cuda.synchronize()
     assert all(torch.equal(a, b) for a, b in zip(_pool_bytes(dev["int2"]), want))
     assert torch.equal(part.m, ref.m) and torch.equal(part.l, ref.l) and torch.equal(part.acc, ref.acc)
+    # dynamic history units: the same bytes
+    for t, b0 in zip((dev["int2"].codes_k, dev["int2"].codes_v, dev["int2"].scale_k, dev["int2"].zero_k,
+                      dev["int2"].scale_v, dev["int2"].zero_v), before):
+        t.copy_(b0)
+    tiles = torch.zeros(2 * B, dtype=torch.int32, device="cuda")
+    ob.oscar_decode_attention_fused(L, dev["q"], dev["RK"], dev["bf16"], dev["bf16_table"], dev["int2"],
+                                    dev["int2_table"], dev["seq_len"], dev["hist_end"], case.sm_scale,
+                                    ob.Partials.empty(L, B, S), demote_pos=pos, R_V=dev["RV"], c_K=oracle.C_K,
+                                    c_V=oracle.C_V, tile_counters=tiles)
+    torch.cuda.synchronize()
+    assert all(torch.equal(a, b) for a, b in zip(_pool_bytes(dev["int2"]), want))
+    assert not tiles.any()
     assert ob.oscar_get_device_status() == 0
 
 
@@ -485,3 +498,63 @@ def test_host_validation_errors():
         ob.oscar_quantize_rotated(L, x, 0.96, c, s, s)
     with pytest.raises(ob.OscarError, match="clip"):
         ob.oscar_quantize_rotated(ob.Layout(2, 4, 16), x, 0.0, c, s, s)
+
+
+@pytest.mark.parametrize("n_kv,gqa,ps,group,seq,S", [
+    (8, 4, 64, 128, (3000, 1700), 6),     # the benchmark's layout
+    (2, 4, 16, 32, (1200, 300), 3),        # group 32, a request with no history
+    (8, 8, 16, 64, (1400,), 4),            # GQA 8, group 64
+    (1, 1, 32, 128, (900, 2100), 2),       # one kv head (no tensor maps)
+])
+def test_dynamic_tile_scheduling(n_kv, gqa, ps, group, seq, S):
+    """History CTAs taking 64-token units from a shared per-request counter: the merged output
+    meets the bar against the oracle and agrees with the fixed splits' up to fp32 rounding order;
+    eager, repeated and graph-captured (launch overlap) calls leave the counters at zero."""
+    case = sc.make_case(n_kv=n_kv, gqa=gqa, page_size=ps, group=group, seq=seq)
+    sc.upload(case)
+    L, dev = case.layout, case.dev
+    B, Hq = len(seq), L.n_q_heads
+    tiles = torch.zeros(2 * B, dtype=torch.int32, device="cuda")
+
+    def run(p2, outs, dyn):
+        ob.oscar_decode_attention_fused(L, dev["q"], dev["RK"], dev["bf16"], dev["bf16_table"], dev["int2"],
+                                        dev["int2_table"], dev["seq_len"], dev["hist_end"], case.sm_scale, p2,
+                                        R_V=dev["RV"], out=outs[0], out_f32=outs[1], lse=outs[2],
+                                        tile_counters=tiles if dyn else None)
+
+    def fresh():
+        return (torch.empty((B, Hq, D), dtype=torch.bfloat16, device="cuda"),
+                torch.empty((B, Hq, D), dtype=torch.float32, device="cuda"),
+                torch.empty((B, Hq), dtype=torch.float32, device="cuda"))
+    fixed = fresh()
+    run(ob.Partials.empty(L, B, S), fixed, False)
+    runs = []
+    for _ in range(3):
+        o = fresh()
+        run(ob.Partials.empty(L, B, S), o, True)
+        runs.append(o)
+    try:
+        ob.oscar_set_launch_overlap(True)
+        og = fresh()
+        pg = ob.Partials.empty(L, B, S)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            run(pg, og, True)
+            run(pg, og, True)
+        g.replay()
+        g.replay()
+    finally:
+        ob.oscar_set_launch_overlap(False)
+    torch.cuda.synchronize()
+    runs.append(og)
+    assert not tiles.any()
+    assert ob.oscar_get_device_status() == 0
+    ref = sc.oracle_outputs(case)
+    f32 = fixed[1].cpu().numpy()
+    for o in runs:
+        o32 = o[1].cpu().numpy()
+        assert np.array_equal(bf16_bits(o[0]), oracle.f32_to_bf16(o32))
+        assert np.allclose(o32, f32, rtol=1e-5, atol=1e-5 * np.abs(f32).max())
+        for (b, hq), (oref, lref) in ref.items():
+            ok, r, m = sc.tolerance_ok(o32[b, hq], oref)
+            assert ok, ((b, hq), r, m)
