@@ -126,6 +126,7 @@ struct MmaArgs {
     int win_off;      // byte offset (from the first stage) of the window CTAs' warp results
     const float *RK;            // non-null: history CTAs rotate q themselves (q_rot unused)
     int rot_off;                // byte offset (from the aligned base) of the rotated-query rows [Hq][128]
+    int wbuf_off, wbuf_tok;     // window CTAs: two row buffers (from the first stage), tokens per buffer
     int rk_chunk;               // bytes of R_K staged per step in the stage area (16, 32 or 64 KB)
     const uint16_t *q;          // raw bf16 queries (window CTAs, and the rotation when RK is set)
     FusedDemotion dem;          // per-step demotion done by the window CTAs (dem.dem_pos NULL: none)
@@ -265,7 +266,8 @@ __device__ __forceinline__ void window_fold(const float (&q)[G][4], const uint2 
 // head are combined in a fixed order, and the CTA's result goes to `res` (cluster) or
 // straight to partial slot S.  Every thread of the CTA calls this.
 template <int G>
-__device__ void window_cta(const MmaArgs &a, float *wsm, float *res, int T, int he, int b, int wr, int wc) {
+__device__ void window_cta(const MmaArgs &a, float *wsm, float *res, uint8_t *wbuf, uint64_t *wbar, int T, int he,
+                           int b, int wr, int wc) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int Hkv = a.n_kv, Hq = Hkv * G, nsub = kCW / Hkv, S = a.out.S;
     const int n0 = min(a.sink, T), lo1 = max(he, n0);
@@ -279,18 +281,95 @@ __device__ void window_cta(const MmaArgs &a, float *wsm, float *res, int T, int 
 #pragma unroll
         for (int c = 0; c < 4; ++c) acc[hh][c] = 0.f;
     }
+    const int h = warp % Hkv, sub = warp / Hkv;
+    float q[G][4];
     if (warp < kCW) {
-        const int h = warp % Hkv, sub = warp / Hkv;
-        float q[G][4];
 #pragma unroll
         for (int hh = 0; hh < G; ++hh) {
             const uint2 v = reinterpret_cast<const uint2 *>(a.q + ((size_t)b * Hq + h * G + hh) * kHeadDim)[lane];
             q[hh][0] = __uint_as_float(v.x << 16); q[hh][1] = __uint_as_float(v.x & 0xffff0000u);
             q[hh][2] = __uint_as_float(v.y << 16); q[hh][3] = __uint_as_float(v.y & 0xffff0000u);
         }
-        // Tokens in chunks of 64 per warp: the chunk's page ids are read once (two per lane), then
-        // U tokens' K/V rows are loaded together and folded one by one.
-        constexpr int U = 4;
+    }
+    constexpr int U = 4;
+    if (a.wbuf_tok >= U) {
+        // The CTA's rows go through shared memory: chunks of CH tokens (all kv heads, K then V) in two
+        // buffers, each filled by one thread with bulk copies of the chunk's page pieces, so a chunk
+        // costs one round trip; the warps fold a chunk while the next one lands.
+        const int CH = a.wbuf_tok, nt = i_hi - i_lo, nch = (nt + CH - 1) / CH;
+        const int rowb = Hkv * kHeadDim * 2;                  // one token's K (or V) row, all heads
+        uint32_t *valid = reinterpret_cast<uint32_t *>(wbar + 2);   // per buffer: bit j = token j's page is valid
+        auto fill = [&](int k) {                              // thread 0
+            const int buf = k & 1, j0 = k * CH, n = min(CH, nt - j0);
+            uint8_t *dk = wbuf + (size_t)buf * 2 * CH * rowb, *dv = dk + (size_t)CH * rowb;
+            fence_proxy_async_smem();                         // the warps' reads of this buffer came first
+            uint32_t bytes = 0, vbits = 0;
+            for (int j = 0; j < n;) {                         // page pieces of contiguous positions
+                const int i = i_lo + j0 + j;
+                const int p = i < n0 ? i : lo1 + (i - n0);
+                const int run_end = i < n0 ? n0 : T;
+                const int cnt = min(min((p / a.page_size + 1) * a.page_size, run_end) - p, n - j);
+                const int page = p / a.page_size < a.max_pages ? a.bpt[(size_t)b * a.max_pages + p / a.page_size] : -1;
+                if (page >= 0 && page < a.bpool.n_pages) {
+                    vbits |= (cnt == 32 ? 0xffffffffu : (1u << cnt) - 1u) << j;
+                    bytes += 2u * cnt * rowb;
+                } else {
+                    flag_status(a.status, OSCAR_DEV_BAD_BF16_PAGE);
+                }
+                j += cnt;
+            }
+            valid[buf] = vbits;
+            mbar_arrive_expect_tx(saddr(&wbar[buf]), bytes);
+            for (int j = 0; j < n;) {
+                const int i = i_lo + j0 + j;
+                const int p = i < n0 ? i : lo1 + (i - n0);
+                const int run_end = i < n0 ? n0 : T;
+                const int cnt = min(min((p / a.page_size + 1) * a.page_size, run_end) - p, n - j);
+                const int page = p / a.page_size < a.max_pages ? a.bpt[(size_t)b * a.max_pages + p / a.page_size] : -1;
+                if (page >= 0 && page < a.bpool.n_pages) {
+                    const size_t row = ((size_t)page * a.page_size + p % a.page_size) * Hkv;
+                    tma_load_1d(saddr(dk + (size_t)j * rowb), a.bpool.k + row * kHeadDim, (uint32_t)cnt * rowb,
+                                saddr(&wbar[buf]));
+                    tma_load_1d(saddr(dv + (size_t)j * rowb), a.bpool.v + row * kHeadDim, (uint32_t)cnt * rowb,
+                                saddr(&wbar[buf]));
+                }
+                j += cnt;
+            }
+        };
+        if (threadIdx.x == 0) {
+            mbar_init(saddr(&wbar[0]), 1);
+            mbar_init(saddr(&wbar[1]), 1);
+            asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+            for (int k = 0; k < 2 && k < nch; ++k) fill(k);
+        }
+        __syncthreads();
+        for (int k = 0; k < nch; ++k) {
+            const int buf = k & 1, n = min(CH, nt - k * CH);
+            if (!mbar_wait(saddr(&wbar[buf]), (k >> 1) & 1) && threadIdx.x == 0)
+                flag_status(a.status, OSCAR_DEV_WAIT_TIMEOUT);
+            if (warp < kCW) {
+                const uint32_t vb = valid[buf];
+                const uint8_t *dk = wbuf + (size_t)buf * 2 * CH * rowb, *dv = dk + (size_t)CH * rowb;
+                for (int j0 = sub * U; j0 < n; j0 += U * nsub) {
+                    uint2 kk[U], vv[U];
+                    bool ok[U];
+#pragma unroll
+                    for (int u = 0; u < U; ++u) {
+                        const int j = j0 + u;
+                        ok[u] = j < n && ((vb >> j) & 1);
+                        const size_t off = (size_t)(ok[u] ? j : 0) * rowb + h * kHeadDim * 2;
+                        kk[u] = reinterpret_cast<const uint2 *>(dk + off)[lane];
+                        vv[u] = reinterpret_cast<const uint2 *>(dv + off)[lane];
+                    }
+                    window_fold<G, U>(q, kk, vv, ok, a.scale2, m, l, acc, lane);
+                }
+            }
+            __syncthreads();                                  // buffer `buf` is consumed
+            if (threadIdx.x == 0 && k + 2 < nch) fill(k + 2);
+        }
+    } else if (warp < kCW) {
+        // (buffers too small for the layout) Tokens in chunks of 64 per warp: the chunk's page ids
+        // are read once (two per lane), then U tokens' K/V rows are loaded together and folded.
         for (int c0 = i_lo + sub; c0 < i_hi; c0 += 64 * nsub) {
           int pg[2];
 #pragma unroll
@@ -327,6 +406,8 @@ __device__ void window_cta(const MmaArgs &a, float *wsm, float *res, int T, int 
             window_fold<G, U>(q, kk, vv, ok, a.scale2, m, l, acc, lane);
           }
         }
+    }
+    if (warp < kCW) {
         // warp results: wsm = [warp][G] m, [warp][G] l, [warp][G][128] acc
         float *wm = wsm, *wl = wsm + kCW * G, *wa = wsm + 2 * kCW * G;
 #pragma unroll
@@ -560,7 +641,8 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
     if (s < 0) {                               // a BF16 window CTA (uniform over the cluster)
         pdl_wait();                            // q and the partials belong to the previous kernels
         window_cta<G>(a, reinterpret_cast<float *>(stage0 + a.win_off), reinterpret_cast<float *>(stage0 + a.res_off),
-                      T, he, b, (int)blockIdx.x, a.win_ctas);
+                      stage0 + a.wbuf_off, reinterpret_cast<uint64_t *>(smem + 112), T, he, b, (int)blockIdx.x,
+                      a.win_ctas);
         // (after the cluster's last barrier: the stage area is free again)
         if (a.dem.dem_pos && !(a.sched && a.hist_ctas >= Hkv))
             window_demote(a, reinterpret_cast<float *>(smem + 128), stage0, T, he, b, (int)blockIdx.x, a.win_ctas);
@@ -1407,6 +1489,12 @@ int mma_smem_plan(const oscar_layout_t &L, MmaArgs &a) {
     const int area = stages * a.stage_bytes;             // R_K is staged here a chunk at a time
     a.rk_chunk = area >= 65536 ? 65536 : area >= 32768 ? 32768 : 16384;
     a.rot_off = a.stage_off + (area > tail ? area : tail);
+    // the window CTAs stage their K/V rows in what lies beyond their warp results (they use neither
+    // the stages nor the rotated-query rows): two buffers of wbuf_tok tokens (K rows, then V rows)
+    a.wbuf_off = (tail + 15) & ~15;
+    const int wfree = a.rot_off + rot_bytes - a.stage_off - a.wbuf_off;
+    a.wbuf_tok = wfree / (2 * 2 * Hkv * kHeadDim * 2);
+    if (a.wbuf_tok > 32) a.wbuf_tok = 32;
     // + 1024: the kernel rounds the dynamic shared memory base up to a 1024-byte boundary
     return 1024 + a.rot_off + rot_bytes;
 }
