@@ -609,7 +609,7 @@ def main():
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         cpu = oracle_sample(w, args.cpu_seconds)
-        cpu = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        cpu = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample", "single_core_value")}
 
     if rank == 0:
         line = {
