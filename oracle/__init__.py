@@ -378,4 +378,6 @@ PINS = {
     "merge_f32/exp2f": "against fp64 merge and exp2 within ulp bounds; exact at integers",
     "rotation_from_covariance": "Hadamard/permutation closed forms, orthogonality, diagonalisation, q=0 rank-one C_S",
     "bits_per_element": "page values 2.28 / 2.38 bits and 0.24% BF16 share (tests/golden/pages_numbers.json)",
+    "score_weighted_value_covariance": "the value rotation built from it lowers the attention-weighted value "
+                                       "error below H·P_br alone on synthetic data (tests/test_oracle_quality.py)",
 }

@@ -28,7 +28,7 @@ def _worker(rank, world, port, out):
 
 def test_max_over_ranks_two_gloo_ranks():
     world = 2
-    out = mp.Manager().dict()
+    out = mp.get_context("spawn").Manager().dict()
     mp.spawn(_worker, args=(world, _free_port(), out), nprocs=world, join=True)
     assert out[0] == out[1] == 2.0
 
