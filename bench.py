@@ -55,6 +55,10 @@ def parse_args():
     ap.add_argument("--layers", type=int, default=0, help="profiling aid: run only this many layers (0 = all)")
     ap.add_argument("--no-overlap", action="store_true",
                     help="launch every kernel after the previous one completes (no programmatic dependent launch)")
+    ap.add_argument("--bf16-budget", action="store_true",
+                    help="run the all-BF16 comparison at this workload's cache footprint: the largest batch of "
+                         "its requests whose BF16 cache (shared-prefix pages once) fits in the HBM that the "
+                         "INT2 + BF16-window cache takes; report job-level tokens/s of both")
     return ap.parse_args()
 
 
@@ -80,6 +84,49 @@ def bytes_per_step(w: syn.Workload, seq, hist_end) -> dict:
     return {"int2_per_layer": hist * per_tok_int2, "bf16_per_layer": bf * per_tok_bf16, "qo_per_layer": qo,
             "per_layer": per_layer, "per_step": per_layer * w.layers,
             "bf16_cache_per_step": (sum(seq) * per_tok_bf16 + qo) * w.layers}
+
+
+def cache_page_bytes(w: syn.Workload) -> tuple:
+    """Bytes of one page of the INT2 pool (codes of K and V, scale/zero of both) and of one BF16 page (K and V)."""
+    ps, H, D = w.page_size, w.n_kv_heads, w.head_dim
+    return ps * H * (2 * D // 4 + 4 * 2 * (D // w.group)), ps * H * D * 2 * 2
+
+
+def bf16_budget_batch(w: syn.Workload, seq, n_int2_pages: int, n_bf16_pages: int) -> dict:
+    """The all-BF16 cache at a fixed HBM budget: the budget is what this workload's mixed cache holds
+    (its INT2 pages and BF16 window pages, all layers); the BF16 batch is the largest n >= 1 such
+    that requests 0..n-1 fit it with every page in BF16, shared-prefix pages counted once."""
+    ps = w.page_size
+    int2_page, bf16_page = cache_page_bytes(w)
+    budget = n_int2_pages * int2_page + n_bf16_pages * bf16_page
+    shared = w.shared_prefix // ps
+    pages, n = 0, 0
+    for b, t in enumerate(seq):
+        n_log = (int(t) + ps - 1) // ps
+        need = n_log - (min(shared, n_log) if b > 0 else 0)
+        if n >= 1 and (pages + need) * bf16_page > budget:
+            break
+        pages += need
+        n += 1
+    return {"batch": n, "budget_bytes": budget * w.layers, "bf16_cache_bytes": pages * bf16_page * w.layers}
+
+
+def bf16_cache_table(w: syn.Workload, seq, max_pages: int) -> tuple:
+    """Page table [n, max_pages] of an all-BF16 cache for requests with contexts `seq`; logical pages
+    below the shared prefix map to request 0's pages, the rest get their own; -1 past each context.
+    Returns (table, number of physical pages)."""
+    ps = w.page_size
+    shared = w.shared_prefix // ps
+    table = -np.ones((len(seq), max_pages), dtype=np.int32)
+    n = 0
+    for b, t in enumerate(seq):
+        for lp in range((int(t) + ps - 1) // ps):
+            if b > 0 and lp < shared:
+                table[b, lp] = table[0, lp]
+            else:
+                table[b, lp] = n
+                n += 1
+    return table, n
 
 
 def measured_peaks() -> dict:
@@ -194,7 +241,7 @@ class ClockSampler:
 class Model:
     """Caches, rotations and buffers of every layer for one batch (device memory)."""
 
-    def __init__(self, w: syn.Workload, device, n_splits: int, with_bf16_cache: bool):
+    def __init__(self, w: syn.Workload, device, n_splits: int, with_bf16_cache: bool, bf16_budget: bool = False):
         import torch
         from bit_kv_cache_oscar_gb300 import binding as ob
         from bit_kv_cache_oscar_gb300 import calibrate
@@ -224,12 +271,21 @@ class Model:
         self.layers = []
         self.bf16_full = [] if with_bf16_cache else None
         max_pages = self.pages.int2_table.shape[1]
+        self.bf16_fit, self.bf16_batch, n_full_pages = None, B, B * max_pages
         if with_bf16_cache:
-            self.full_table = torch.arange(B * max_pages, dtype=torch.int32, device=device).view(B, max_pages)
+            if bf16_budget:
+                # the all-BF16 cache of the first requests that fit this cache's HBM footprint
+                self.bf16_fit = bf16_budget_batch(w, self.seq, self.pages.n_int2_pages, self.pages.n_bf16_pages)
+                self.bf16_batch = self.bf16_fit["batch"]
+                table, n_full_pages = bf16_cache_table(w, self.seq[:self.bf16_batch], max_pages)
+                self.full_table = torch.from_numpy(table).to(device)
+            else:
+                self.full_table = torch.arange(B * max_pages, dtype=torch.int32, device=device).view(B, max_pages)
+            nb = self.bf16_batch
             # the all-BF16 kernel runs one CTA per split, one resident CTA per SM
-            self.S_full = max(1, min(1024, sms // B))
-            self.part_full = ob.Partials.empty(L, B, self.S_full, device)
-            self.out_full = torch.empty((w.layers, B, w.n_q_heads, D), dtype=torch.bfloat16, device=device)
+            self.S_full = max(1, min(1024, sms // nb))
+            self.part_full = ob.Partials.empty(L, nb, self.S_full, device)
+            self.out_full = torch.empty((w.layers, nb, w.n_q_heads, D), dtype=torch.bfloat16, device=device)
         # per-step demotion: position hist_end of each request (left the recent window this step)
         self.dem_req = torch.arange(B, dtype=torch.int32, device=device)
         self.dem_pos = torch.from_numpy(self.hist_end.astype(np.int32)).to(device)
@@ -240,16 +296,23 @@ class Model:
             del qc, kc, vc
             i2 = ob.Int2Pool.empty(L, self.pages.n_int2_pages, device)
             bf = ob.Bf16Pool.empty(L, self.pages.n_bf16_pages, device)
-            full = ob.Bf16Pool.empty(L, B * max_pages, device) if with_bf16_cache else None
+            full = ob.Bf16Pool.empty(L, n_full_pages, device) if with_bf16_cache else None
             for b, T in enumerate(self.seq):
                 k, v = syn.kv_rows(w.seed, l, b, 0, T, prof, device=device, shared_prefix=w.shared_prefix)
                 n_log = (T + ps - 1) // ps
                 stage = ob.Bf16Pool.empty(L, n_log, device)
                 stage.k.view(-1, w.n_kv_heads, D)[:T] = k
                 stage.v.view(-1, w.n_kv_heads, D)[:T] = v
-                if full is not None:
+                if full is not None and self.bf16_fit is None:
                     full.k[b * max_pages:b * max_pages + n_log] = stage.k
                     full.v[b * max_pages:b * max_pages + n_log] = stage.v
+                elif full is not None and b < self.bf16_batch:
+                    # this request's own pages (request 0 also holds the shared prefix)
+                    first = 0 if b == 0 else min(w.shared_prefix // ps, n_log)
+                    src = torch.arange(first, n_log, device=device)
+                    dst = self.full_table[b, first:n_log].long()
+                    full.k[dst] = stage.k[src]
+                    full.v[dst] = stage.v[src]
                 st_table = torch.full((1, max_pages), -1, dtype=torch.int32, device=device)
                 st_table[0, :n_log] = torch.arange(n_log, dtype=torch.int32, device=device)
                 start = w.sink if b == 0 else max(w.sink, w.shared_prefix)
@@ -305,8 +368,9 @@ class Model:
 
     def step_bf16(self):
         from bit_kv_cache_oscar_gb300 import binding as ob
+        nb = self.bf16_batch
         for l, full in enumerate(self.bf16_full):
-            ob.oscar_bf16_decode_attention(self.L, self.q_all[l], full, self.full_table, self.seq_len,
+            ob.oscar_bf16_decode_attention(self.L, self.q_all[l, :nb], full, self.full_table, self.seq_len[:nb],
                                            self.sm_scale, self.part_full)
             ob.oscar_merge(self.L, self.part_full, None, self.out_full[l])
 
@@ -522,7 +586,8 @@ def main():
         dist.init_process_group("nccl", device_id=torch.device("cuda", local))
     from bit_kv_cache_oscar_gb300 import binding as ob
     ob.lib()
-    model = Model(w, torch.device("cuda", local), args.splits, with_bf16_cache=not args.no_bf16)
+    model = Model(w, torch.device("cuda", local), args.splits, with_bf16_cache=not args.no_bf16,
+                  bf16_budget=args.bf16_budget)
     torch.cuda.synchronize()
     # The step's kernels read pools, tables and lengths that no kernel of the step writes
     # (the per-step demotion runs on its own stream and writes positions the step does not
@@ -600,10 +665,17 @@ def main():
     if model.bf16_full is not None:
         gb = capture(model.step_bf16)
         tb = time_graph(gb, args.steps, args.warmup, dist)
-        vb = job_throughput(world, w.batch, tb, args.steps)
+        nb = model.bf16_batch
+        vb = job_throughput(world, nb, tb, args.steps)
+        bb = bts["bf16_cache_per_step"]
+        if model.bf16_fit is not None:     # the first nb requests' caches and q/out
+            bb = (sum(model.seq[:nb]) * w.n_kv_heads * w.head_dim * 4
+                  + nb * w.n_q_heads * w.head_dim * 4) * w.layers
         bf16 = {"value": vb, "unit": "tokens/s", "ms_per_step": 1e3 * tb / args.steps,
-                "bytes_per_step": bts["bf16_cache_per_step"], "int2_speedup": value / vb,
-                "gbs": bts["bf16_cache_per_step"] / (tb / args.steps) / 1e9}
+                "bytes_per_step": bb, "int2_speedup": value / vb, "gbs": bb / (tb / args.steps) / 1e9}
+        if model.bf16_fit is not None:
+            bf16.update({"batch": nb, "fixed_hbm_budget": model.bf16_fit,
+                         "comparison": "job-level tokens/s of both caches in the same HBM footprint"})
     assert ob.oscar_get_device_status() == 0
 
     cpu = None
