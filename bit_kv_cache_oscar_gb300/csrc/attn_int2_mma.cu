@@ -127,7 +127,7 @@ struct MmaArgs {
     const float *RK;            // non-null: history CTAs rotate q themselves (q_rot unused)
     int rot_off;                // byte offset (from the aligned base) of the rotated-query rows [Hq][128]
     int wbuf_off, wbuf_tok;     // window CTAs: two row buffers (from the first stage), tokens per buffer
-    int rk_chunk;               // bytes of R_K staged per step in the stage area (16, 32 or 64 KB)
+    int rk_chunk;               // bytes of R staged per step in the stage area by the window CTAs' demotion
     const uint16_t *q;          // raw bf16 queries (window CTAs, and the rotation when RK is set)
     FusedDemotion dem;          // per-step demotion done by the window CTAs (dem.dem_pos NULL: none)
     int group;
@@ -666,42 +666,17 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
             mbar_init(saddr(&bars[i]), TMA ? 1 : 33);   // TMA: the expect-tx arrival; else 32 cp.async + mask
             mbar_init(saddr(&bars[4 + i]), kCW);
         }
-        if (a.RK) {
-            mbar_init(saddr(smem + 96), 1);        // R_K chunk landed (expect-tx)
-            mbar_init(saddr(smem + 104), kCW);     // R_K chunk consumed by every consumer warp
-        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
+    // phase 0 of the cluster barrier: the rotated queries pushed by every CTA are in place
+    const bool rot_phase = a.RK && a.csize > 1;
 
     // ------------------------------------------------------------ producer --
     if (warp == kCW) {
-        if (a.RK) {
-            // Stage R_K of the kv heads this CTA rotates (rank, rank + C, ...) in the stage area,
-            // a chunk at a time, before any KV copy lands there.  R_K is fixed: no wait needed.
-            const int C = a.csize, rank = C > 1 ? (int)cluster_ctarank() : 0;
-            const uint32_t rk_full = saddr(smem + 96), rk_free = saddr(smem + 104);
-            const int nch = kHeadDim * kHeadDim * 4 / a.rk_chunk;
-            int n = 0;
-            bool ok_rk = true;
-            for (int hk = rank; hk < Hkv && ok_rk; hk += C)
-                for (int c = 0; c < nch; ++c, ++n) {
-                    if (n > 0 && !mbar_wait(rk_free, (n - 1) & 1)) {
-                        if (lane == 0) flag_status(a.status, OSCAR_DEV_WAIT_TIMEOUT);
-                        ok_rk = false;
-                        break;
-                    }
-                    if (lane == 0) {
-                        mbar_arrive_expect_tx(rk_full, a.rk_chunk);
-                        tma_load_1d(saddr(stage0), reinterpret_cast<const uint8_t *>(a.RK + (size_t)hk * kHeadDim * kHeadDim) +
-                                                       (size_t)c * a.rk_chunk, a.rk_chunk, rk_full);
-                    }
-                    __syncwarp();
-                }
-            if (ok_rk && n > 0 && !mbar_wait(rk_free, (n - 1) & 1) && lane == 0)
-                flag_status(a.status, OSCAR_DEV_WAIT_TIMEOUT);
-            if (C > 1) cluster_sync_all();         // phase 0: the cluster's rotated queries are in place
-        }
+        // The copy warp takes no part in the rotation: it arrives on phase 0 at once and streams the
+        // KV pages from the start (it waits on the phase only before the cluster's final combine).
+        if (rot_phase) cluster_arrive();
         const int lgH = Hkv == 1 ? 0 : Hkv == 2 ? 1 : Hkv == 4 ? 2 : 3;
         // Page ids of 32 consecutive logical pages, lane i holding page pg_base + i: one load
         // serves 32 pages (128 tiles at 64-token pages), so the copies never wait on the table.
@@ -846,74 +821,70 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
             a.sched[gridDim.y + b] = 0;
             __threadfence();
         }
+        if (rot_phase) cluster_wait();
         if (a.csize > 1) cluster_combine(a, reinterpret_cast<const float *>(stage0 + a.res_off), Hq, b, s / a.csize);
         if (a.arrivals) arrive_count(a, b);
         return;
     }
 
     // ----------------------------------------------------------- consumers --
-    // The copies above read only the pool, the page table and the lengths; q_rot and the
-    // partials belong to the previous kernels in the stream.
-    pdl_wait();
+    // The copies above read only the pool, the page table and the lengths (and R_K below is as
+    // fixed as they are); q, q_rot and the partials belong to the previous kernels in the stream.
     const int h = warp % Hkv, sub = warp / Hkv, nsub = kCW / Hkv;
     const int gid = lane >> 2, t = lane & 3;
     const int C = a.csize, rank = C > 1 ? (int)cluster_ctarank() : 0;
     float *qrot_s = reinterpret_cast<float *>(smem + a.rot_off);     // [Hq][kQS] rotated queries of the request
-    if (a.RK) {
-        // q_rot = q . R_K for kv heads rank, rank + C, ...: thread j < 128 runs the fp32 chains
-        // acc_g = fma(q[g][i], R_K[i][j], acc_g), i ascending, for every query head g of the kv
-        // head (the same operations, in the same order, as oscar_rotate_q).  Each R_K element is
-        // read once and the queries come as 4-wide broadcast loads: the loop is bound by shared-
-        // memory issue, not by the chains.
-        const uint32_t rk_full = saddr(smem + 96), rk_free = saddr(smem + 104);
-        float *qs = reinterpret_cast<float *>(smem + 128);           // [G][128] (P-buffer area, free until the loop)
-        const int ctid = threadIdx.x, j = ctid & (kHeadDim - 1);
-        const bool rot = ctid < kHeadDim;
-        const int rpc = a.rk_chunk / (kHeadDim * 4), nch = kHeadDim / rpc;
-        int n = 0;
+    if (!a.RK) {
+        pdl_wait();
+    } else {
+        // q_rot = q . R_K for kv heads rank, rank + C, ... of this CTA, with R_K read straight from
+        // global memory (it stays in L2), so that the stages fill with KV pages meanwhile.  Consumer
+        // warp w sums rows [16 w, 16 w + 16) of R_K for columns 4 l .. 4 l + 3 (lane l) of every
+        // query head of the kv head, as fp32 FMA chains in ascending row order; q_rot is the sum of
+        // the eight partial sums in warp order, and it is written into every CTA of the cluster.
+        float *part = reinterpret_cast<float *>(smem + 128);          // [kCW][G][128] partial sums
+        float4 r[16];
+        auto load_r = [&](int hk) {
+            const float4 *R4 = reinterpret_cast<const float4 *>(a.RK + ((size_t)hk * kHeadDim + 16 * warp) * kHeadDim) + lane;
+#pragma unroll
+            for (int k = 0; k < 16; ++k) r[k] = __ldg(R4 + k * (kHeadDim / 4));
+        };
+        if (rank < Hkv) load_r(rank);
+        pdl_wait();                                                  // q may come from the previous kernel
         for (int hk = rank; hk < Hkv; hk += C) {
-            consumer_sync();
-            for (int e = ctid; e < G * kHeadDim; e += kCW * 32)
-                qs[e] = bf16_to_f32(a.q[((size_t)b * Hq + hk * G) * kHeadDim + e]);
-            consumer_sync();
-            float racc[G];
+            if (hk != rank) load_r(hk);
 #pragma unroll
-            for (int g = 0; g < G; ++g) racc[g] = 0.f;
-            for (int c = 0; c < nch; ++c, ++n) {
-                if (!mbar_wait(rk_full, n & 1) && lane == 0) flag_status(a.status, OSCAR_DEV_WAIT_TIMEOUT);
-                const float *R = reinterpret_cast<const float *>(stage0);
-                if (rot) {
-#pragma unroll 2
-                    for (int i = 0; i < rpc; i += 4) {
-                        const float r0 = R[(i + 0) * kHeadDim + j], r1 = R[(i + 1) * kHeadDim + j];
-                        const float r2 = R[(i + 2) * kHeadDim + j], r3 = R[(i + 3) * kHeadDim + j];
+            for (int g = 0; g < G; ++g) {
+                const uint4 *qp = reinterpret_cast<const uint4 *>(a.q + ((size_t)b * Hq + hk * G + g) * kHeadDim + 16 * warp);
+                const uint4 qa = qp[0], qb = qp[1];
+                const uint32_t qw[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-                        for (int g = 0; g < G; ++g) {
-                            const float4 qv = *reinterpret_cast<const float4 *>(qs + g * kHeadDim + c * rpc + i);
-                            racc[g] = __fmaf_rn(qv.x, r0, racc[g]);
-                            racc[g] = __fmaf_rn(qv.y, r1, racc[g]);
-                            racc[g] = __fmaf_rn(qv.z, r2, racc[g]);
-                            racc[g] = __fmaf_rn(qv.w, r3, racc[g]);
-                        }
-                    }
+                for (int k = 0; k < 16; ++k) {
+                    const float qv = __uint_as_float((k & 1) ? (qw[k >> 1] & 0xffff0000u) : (qw[k >> 1] << 16));
+                    acc.x = __fmaf_rn(qv, r[k].x, acc.x);
+                    acc.y = __fmaf_rn(qv, r[k].y, acc.y);
+                    acc.z = __fmaf_rn(qv, r[k].z, acc.z);
+                    acc.w = __fmaf_rn(qv, r[k].w, acc.w);
                 }
-                __syncwarp();
-                if (lane == 0) mbar_arrive(rk_free);
+                *reinterpret_cast<float4 *>(part + (warp * G + g) * kHeadDim + 4 * lane) = acc;
             }
-            // every CTA of the cluster gets the rows: stores to the peers need no round trip
-            if (rot) {
+            consumer_sync();
+            for (int e = threadIdx.x; e < G * kHeadDim; e += kCW * 32) {
+                const int g = e / kHeadDim, j = e % kHeadDim;
+                float v = part[g * kHeadDim + j];
 #pragma unroll
-                for (int g = 0; g < G; ++g) {
-                    float *dst = qrot_s + (hk * G + g) * kQS + qs_col(j);
-                    if (C == 1) {
-                        *dst = racc[g];
-                    } else {
-                        for (int q = 0; q < C; ++q) st_dsmem_f32(saddr(dst), (uint32_t)q, racc[g]);
-                    }
+                for (int w2 = 1; w2 < kCW; ++w2) v = __fadd_rn(v, part[(w2 * G + g) * kHeadDim + j]);
+                float *dst = qrot_s + (hk * G + g) * kQS + qs_col(j);
+                if (C == 1) {
+                    *dst = v;
+                } else {
+                    for (int q = 0; q < C; ++q) st_dsmem_f32(saddr(dst), (uint32_t)q, v);
                 }
             }
+            consumer_sync();                                         // the partial sums are consumed
         }
-        if (C > 1) cluster_sync_all(); else consumer_sync();
+        if (C > 1) cluster_sync_all();                               // phase 0 (the copy warp arrived early)
     }
     // with dynamic history units the per-step demotion of kv head s is done here, by history CTA s
     if (a.dem.dem_pos && a.sched && a.hist_ctas >= Hkv && s < Hkv && threadIdx.x < kHeadDim)
@@ -923,7 +894,27 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
         return a.RK ? qrot_s[hq * kQS + qs_col(d)] : a.q_rot[((size_t)b * Hq + hq) * kHeadDim + d];
     };
 
-    // B operand of QK: q_rot split into f16 hi/lo, divided by the code factor of its k-row.
+    // Power-of-two prescale of the warp's queries: the largest |q_rot| of the kv head's query
+    // heads is brought into [2^14, 2^15), so that q_rot / factor (factors 1 .. 256) uses the f16
+    // range of the split operand whatever the queries' magnitude; 2^e goes into the logit scale.
+    float qsc = 1.f, cscq;
+    {
+        float qmax = 0.f;
+        for (int hh = 0; hh < G; ++hh)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) qmax = fmaxf(qmax, fabsf(qrot(h * G + hh, 4 * lane + c)));
+#pragma unroll
+        for (int o = 16; o; o >>= 1) qmax = fmaxf(qmax, __shfl_xor_sync(0xffffffffu, qmax, o));
+        // qmax in [2^(eb-127), 2^(eb-126)): scale 2^(141-eb), undone by 2^(eb-141)
+        const int eb = min(max((int)((__float_as_uint(qmax) >> 23) & 0xffu), 15), 254);
+        float qinv = 1.f;
+        if (qmax > 0.f && qmax < INFINITY) {
+            qsc = __uint_as_float((uint32_t)(268 - eb) << 23);
+            qinv = __uint_as_float((uint32_t)(eb - 14) << 23);
+        }
+        cscq = a.scale2 * kTwo24 * qinv;
+    }
+    // B operand of QK: q_rot * qsc split into f16 hi/lo, divided by the code factor of its k-row.
     uint32_t bq[NT][8][2];
     float qz[NT][NGRP];
 #pragma unroll
@@ -939,7 +930,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int rr = 2 * sg + e, W = 2 * t + kap;
-                        const float inv = 1.0f / qk_factor(rr);
+                        const float inv = qsc / qk_factor(rr);
                         const float v0 = valid ? qrot(hq, 16 * W + rr) * inv : 0.f;
                         const float v1 = valid ? qrot(hq, 16 * W + 8 + rr) * inv : 0.f;
                         bq[nt][kap * 4 + sg][e] = pack2(split_part(v0, part), split_part(v1, part));
@@ -954,7 +945,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
                         const int rr = qk_rsel(j, e, t & 1), W = 2 * Gb + (t >> 1);
-                        const float inv = 1.0f / qk_factor(rr);
+                        const float inv = qsc / qk_factor(rr);
                         const float v0 = valid ? qrot(hq, 16 * W + rr) * inv : 0.f;
                         const float v1 = valid ? qrot(hq, 16 * W + 8 + rr) * inv : 0.f;
                         bq[nt][2 * Gb + j][e] = pack2(split_part(v0, part), split_part(v1, part));
@@ -1023,7 +1014,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
     auto tile_base = [&](const uint8_t *arr, int j) -> const uint8_t * {
         return TMA ? arr + j * 4096 + (h >> 2) * 2048 : arr + h * 2048 + j * (kTileTokens * 32);
     };
-    const float csc = a.scale2 * kTwo24;
+    const float csc = cscq;                     // logit scale of the MMA dot products
     const int rs = Hkv * NGRP;                  // scale/zero elements per token row in a stage
     const int arr_el = arr_bytes / 2;
     uint32_t *Ws = reinterpret_cast<uint32_t *>(smem + 128 + warp * a.ws_bytes);   // [NGRP][NCOL][kWsWords]
@@ -1042,6 +1033,215 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
             for (int c = 0; c < 4; ++c) oacc[nt][mt][c] = 0.f;
     }
 
+    float vout = 1.f;                            // output factor of the value-scale normalisation
+    if constexpr (TMA && NGRP == 1) {
+        // ---- 8 kv heads, one group per head: a warp takes its kv head's four tiles of a stage in
+        // one pass (64 tokens: one running-maximum update and one rescale vote per stage).
+        //  1. lane l converts the stage's scale/zero of tokens l and l + 32 to fp32 once:
+        //     Sw[tok] = (scale_k * cscq, zero_k, scale_v * vmul, zero_v), zero for tokens outside
+        //     the range.  vmul = 128 / vlim, where vlim is a power of two above every value scale
+        //     seen so far (raised with the stage's maximum; the accumulators rescale by the ratio),
+        //     so that w = p * scale_v * vmul < 2^8 * 2^7 stays inside the f16 range of the split
+        //     PV operand whatever the scales' magnitude; vlim / 128 goes into the output.
+        //  2. QK MMAs of the four tiles, interleaved (four independent accumulator chains).
+        //  3. logits, stage maximum, lazy rescale, P * scale_v -> per-warp P buffer (hi, lo).
+        //  4. PV MMAs of the four tiles.
+        constexpr int kWs4 = kTilesPerStage * 8 + 4;        // words per P-buffer column (bank spread)
+        uint32_t *Wp = reinterpret_cast<uint32_t *>(smem + 128 + warp * a.ws_bytes);   // [NCOL][kWs4]
+        float4 *Sw = reinterpret_cast<float4 *>(Wp + NCOL * kWs4);                    // [64] per token
+        float vlim = 0.f, vmul = 0.f;
+        int st = 0, ph = 0;
+        for (;; st = (st + 1 == a.stages) ? 0 : st + 1, ph ^= (st == 0)) {
+            if (!mbar_wait(saddr(&bars[st]), ph)) {
+                if (lane == 0) flag_status(a.status, OSCAR_DEV_WAIT_TIMEOUT);
+                break;
+            }
+            const int t0 = stage_tile[st];
+            if (t0 < 0) break;                        // the copy warp has no more tiles
+            const uint8_t *sb = stage0 + st * stage_bytes;
+            const int mask = masks[st];
+            const int lim = tok_hi - t0 * kTileTokens;   // stage tokens [0, lim) lie inside the range
+            const bool whole = mask == (1 << kTilesPerStage) - 1 && lim >= kStageTok;
+
+            // 1. per-token fp32 scale/zero of kv head h
+            float vres = 1.f;
+            {
+                const uint16_t *s16 = reinterpret_cast<const uint16_t *>(sb + off_s) + h;
+                float4 e[2];
+                float vm = 0.f;
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const int tok = lane + 32 * r;
+                    const bool ok = ((mask >> (tok >> 4)) & 1) && tok < lim;
+                    const int o = tok * 8;
+                    e[r] = ok ? make_float4(bf16_to_f32(s16[o]), bf16_to_f32(s16[arr_el + o]),
+                                            bf16_to_f32(s16[2 * arr_el + o]), bf16_to_f32(s16[3 * arr_el + o]))
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+                    vm = fmaxf(vm, e[r].z);
+                }
+#pragma unroll
+                for (int o = 16; o; o >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o));
+                if (vm > vlim) {                          // (warp-uniform) raise the value-scale bound
+                    // vm in [2^(eb-127), 2^(eb-126)): vlim = 2^(eb-126), vmul = 2^7 / vlim
+                    const int eb = min(max((int)((__float_as_uint(vm) >> 23) & 0xffu), 7), 252);
+                    const float nl = __uint_as_float((uint32_t)(eb + 1) << 23);
+                    vres = __fdiv_rn(vlim, nl);
+                    vlim = nl;
+                    vmul = __uint_as_float((uint32_t)(260 - eb) << 23);
+                }
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    e[r].x *= cscq;
+                    e[r].z *= vmul;
+                    Sw[lane + 32 * r] = e[r];
+                }
+                __syncwarp();
+            }
+
+            // 2. S = K_codes . q_rot for the four tiles (rows tokens gid, gid + 8; columns 4 heads x hi/lo)
+            float sacc[kTilesPerStage][NT][4];
+#pragma unroll
+            for (int u = 0; u < kTilesPerStage; ++u)
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) sacc[u][nt][c] = 0.f;
+            {
+                uint2 kw0[kTilesPerStage], kw1[kTilesPerStage];
+#pragma unroll
+                for (int u = 0; u < kTilesPerStage; ++u) {
+                    const uint8_t *Kc = sb + u * 4096 + (h >> 2) * 2048;
+                    kw0[u] = *reinterpret_cast<const uint2 *>(Kc + kofs0);
+                    kw1[u] = *reinterpret_cast<const uint2 *>(Kc + kofs1);
+                }
+#pragma unroll
+                for (int kap = 0; kap < 2; ++kap) {
+                    uint32_t w0[kTilesPerStage], w1[kTilesPerStage], w0b[kTilesPerStage], w1b[kTilesPerStage];
+#pragma unroll
+                    for (int u = 0; u < kTilesPerStage; ++u) {
+                        w0[u] = kap ? kw0[u].y : kw0[u].x;
+                        w1[u] = kap ? kw1[u].y : kw1[u].x;
+                        w0b[u] = __byte_perm(w0[u], 0, 0x3321);
+                        w1b[u] = __byte_perm(w1[u], 0, 0x3321);
+                    }
+#pragma unroll
+                    for (int sg = 0; sg < 4; ++sg)
+#pragma unroll
+                        for (int u = 0; u < kTilesPerStage; ++u) {
+                            const uint32_t a0 = qk_reg(w0[u], w0b[u], 2 * sg), a1 = qk_reg(w1[u], w1b[u], 2 * sg);
+                            const uint32_t a2 = qk_reg(w0[u], w0b[u], 2 * sg + 1), a3 = qk_reg(w1[u], w1b[u], 2 * sg + 1);
+#pragma unroll
+                            for (int nt = 0; nt < NT; ++nt)
+                                mma16816_nv(sacc[u][nt], a0, a1, a2, a3, bq[nt][kap * 4 + sg][0], bq[nt][kap * 4 + sg][1]);
+                        }
+                }
+            }
+
+            // 3. logits (base 2) of tokens 16 u + gid (+ 8) for head nt * 4 + t; online softmax
+            float alpha[NT];
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) {
+                float tv[kTilesPerStage][2];
+#pragma unroll
+                for (int u = 0; u < kTilesPerStage; ++u)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const float2 sz = *reinterpret_cast<const float2 *>(Sw + 16 * u + gid + 8 * e);
+                        tv[u][e] = fmaf(sz.x, sacc[u][nt][2 * e] + sacc[u][nt][2 * e + 1], sz.y * qz[nt][0]);
+                    }
+                if (!whole) {                             // (uniform) tokens outside the range
+#pragma unroll
+                    for (int u = 0; u < kTilesPerStage; ++u)
+#pragma unroll
+                        for (int e = 0; e < 2; ++e)
+                            if (!((mask >> u) & 1) || 16 * u + gid + 8 * e >= lim) tv[u][e] = -INFINITY;
+                }
+                float mx = tv[0][0];
+#pragma unroll
+                for (int u = 0; u < kTilesPerStage; ++u)
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) mx = fmaxf(mx, tv[u][e]);
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+                mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+                m_true[nt] = fmaxf(m_true[nt], mx);
+                float mn = m_run[nt], al = 1.f;
+                if (mx > mn + kLazy) {                    // also the first finite maximum (mn = -inf)
+                    al = ex2_approx(mn - mx);
+                    mn = mx;
+                }
+                m_run[nt] = mn;
+                alpha[nt] = al;
+                float ls = 0.f, zadd = 0.f;
+                const int c_hi = nt * 8 + 2 * t;
+#pragma unroll
+                for (int u = 0; u < kTilesPerStage; ++u) {
+                    float w[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const float pv = mn != -INFINITY ? ex2_approx(tv[u][e] - mn) : 0.f;
+                        const float2 vz = *reinterpret_cast<const float2 *>(reinterpret_cast<const float *>(Sw + 16 * u + gid + 8 * e) + 2);
+                        ls += pv;
+                        w[e] = pv * vz.x;
+                        zadd = fmaf(pv, vz.y, zadd);
+                    }
+                    // tokens gid, gid + 8 of tile u are PV k-columns 2 gid, 2 gid + 1: one word
+                    uint32_t hi, lo;
+                    split2(w[0], w[1], hi, lo);
+                    Wp[c_hi * kWs4 + u * 8 + gid] = hi;
+                    Wp[(c_hi + 1) * kWs4 + u * 8 + gid] = lo;
+                }
+                l_run[nt] = fmaf(l_run[nt], al, ls);
+                zs[nt][0] = fmaf(zs[nt][0], al, zadd);
+            }
+            bool any = vres != 1.f;
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) any |= alpha[nt] != 1.f;
+            if (__any_sync(0xffffffffu, any)) {
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const float f = alpha[nt] * vres;
+#pragma unroll
+                    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) oacc[nt][mt][c] *= f;
+                }
+            }
+            __syncwarp();
+
+            // 4. O += V_codes^T . (P * scale_v); m-tile mt row gid / gid + 8 = channel 16 gid + 2 mt / + 1
+#pragma unroll
+            for (int u = 0; u < kTilesPerStage; ++u) {
+                const uint8_t *Vc = sb + off_v + u * 4096 + (h >> 2) * 2048;
+                uint32_t bw[NT][2];
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt) {
+                    const uint32_t *col = Wp + (nt * 8 + gid) * kWs4 + u * 8;
+                    bw[nt][0] = col[t];
+                    bw[nt][1] = col[t + 4];
+                }
+                // k-columns 2t, 2t+1 <- tokens t, t+8; 2t+8, 2t+9 <- tokens t+4, t+12
+                const uint32_t X = *reinterpret_cast<const uint32_t *>(Vc + vofs[0]);
+                const uint32_t Y = *reinterpret_cast<const uint32_t *>(Vc + vofs[1]);
+                const uint32_t X2 = *reinterpret_cast<const uint32_t *>(Vc + vofs[2]);
+                const uint32_t Y2 = *reinterpret_cast<const uint32_t *>(Vc + vofs[3]);
+                const uint32_t P1 = __byte_perm(X, Y, 0x5410), P2 = __byte_perm(X, Y, 0x6521);
+                const uint32_t P3 = __byte_perm(X, Y, 0x7632), P4 = __byte_perm(X, Y, 0x7733);
+                const uint32_t Q1 = __byte_perm(X2, Y2, 0x5410), Q2 = __byte_perm(X2, Y2, 0x6521);
+                const uint32_t Q3 = __byte_perm(X2, Y2, 0x7632), Q4 = __byte_perm(X2, Y2, 0x7733);
+#pragma unroll
+                for (int mt = 0; mt < 8; ++mt) {
+                    const uint32_t a0 = pv_reg(P1, P2, P3, P4, 2 * mt), a1 = pv_reg(P1, P2, P3, P4, 2 * mt + 1);
+                    const uint32_t a2 = pv_reg(Q1, Q2, Q3, Q4, 2 * mt), a3 = pv_reg(Q1, Q2, Q3, Q4, 2 * mt + 1);
+#pragma unroll
+                    for (int nt = 0; nt < NT; ++nt) mma16816_nv(oacc[nt][mt], a0, a1, a2, a3, bw[nt][0], bw[nt][1]);
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(saddr(&bars[4 + st]));
+        }
+        vout = vlim * (1.f / 128.f);
+    } else {
     int st = 0, ph = 0;                          // stage and its phase parity, stepped (no division)
     for (;; st = (st + 1 == a.stages) ? 0 : st + 1, ph ^= (st == 0)) {
         if (!mbar_wait(saddr(&bars[st]), ph)) {
@@ -1297,6 +1497,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
         __syncwarp();
         if (lane == 0) mbar_arrive(saddr(&bars[4 + st]));
     }
+    }
 
     // The next kernel in the stream may launch once every CTA's consumers are past their loop
     // (only they trigger: the copy warp finishes its loop stages ahead of them).
@@ -1328,9 +1529,9 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
             const float z = zs[nt][0];
 #pragma unroll
             for (int mt = 0; mt < 8; ++mt) {
-                outv[nt][2 * mt] = fmaf(oacc[nt][mt][0] + oacc[nt][mt][1], kTwo24 / pv_factor(2 * mt), z) * fix[nt];
+                outv[nt][2 * mt] = fmaf(oacc[nt][mt][0] + oacc[nt][mt][1], kTwo24 / pv_factor(2 * mt) * vout, z) * fix[nt];
                 outv[nt][2 * mt + 1] =
-                    fmaf(oacc[nt][mt][2] + oacc[nt][mt][3], kTwo24 / pv_factor(2 * mt + 1), z) * fix[nt];
+                    fmaf(oacc[nt][mt][2] + oacc[nt][mt][3], kTwo24 / pv_factor(2 * mt + 1) * vout, z) * fix[nt];
             }
         } else {
 #pragma unroll
@@ -1475,8 +1676,14 @@ int mma_smem_plan(const oscar_layout_t &L, MmaArgs &a) {
     a.arr_bytes = kStageTok * Hkv * NGRP * 2;
     a.off_s = 2 * a.off_v;
     a.stage_bytes = (a.off_s + 4 * a.arr_bytes + 127) & ~127;
-    a.ws_bytes = NGRP * 8 * NT * kWsWords * 4;
-    a.stage_off = (128 + kCW * a.ws_bytes + 1023) & ~1023;   // stages start 1024-byte aligned
+    // per consumer warp: the P operand buffer (and, on the 8-kv-head single-group path, the
+    // stage's per-token fp32 scale/zero); the same area first holds the rotation's partial sums
+    if (Hkv == 8 && NGRP == 1)
+        a.ws_bytes = 8 * NT * (kTilesPerStage * 8 + 4) * 4 + kStageTok * 16;
+    else
+        a.ws_bytes = NGRP * 8 * NT * kWsWords * 4;
+    const int pre = kCW * a.ws_bytes > kCW * G * kHeadDim * 4 ? kCW * a.ws_bytes : kCW * G * kHeadDim * 4;
+    a.stage_off = (128 + pre + 1023) & ~1023;   // stages start 1024-byte aligned
     const int budget = (G == 8 ? 200 : 110) * 1024;    // two CTAs per SM below G = 8
     const int rot_bytes = Hq * kQS * 4;                 // rotated queries (fused rotation)
     int stages = kMaxStages;
@@ -1486,7 +1693,7 @@ int mma_smem_plan(const oscar_layout_t &L, MmaArgs &a) {
     a.res_off = combine;
     a.win_off = a.res_off + (res_acc(Hq) + Hq * kHeadDim) * 4;
     const int tail = a.win_off + kCW * G * (2 + kHeadDim) * 4;
-    const int area = stages * a.stage_bytes;             // R_K is staged here a chunk at a time
+    const int area = stages * a.stage_bytes;             // (the window CTAs' demotion stages R here)
     a.rk_chunk = area >= 65536 ? 65536 : area >= 32768 ? 32768 : 16384;
     a.rot_off = a.stage_off + (area > tail ? area : tail);
     // the window CTAs stage their K/V rows in what lies beyond their warp results (they use neither

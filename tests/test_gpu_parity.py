@@ -285,8 +285,9 @@ def test_launch_overlap_gives_identical_bits():
     (1, 1, 16, 32, (700,), 2),
 ])
 def test_fused_rotation_matches_rotate_then_decode(n_kv, gqa, ps, group, seq, S):
-    """oscar_decode_attention_fused writes the partials of oscar_rotate_q + oscar_decode_attention,
-    bit for bit."""
+    """oscar_decode_attention_fused writes the partials of oscar_rotate_q + oscar_decode_attention
+    up to the fp32 rounding of q . R_K: the fused rotation sums the same products in another order
+    (eight row blocks, then their sum), so the partials agree to a few fp32 ulps of the logits."""
     case = sc.make_case(n_kv=n_kv, gqa=gqa, page_size=ps, group=group, seq=seq)
     sc.upload(case)
     L, dev = case.layout, case.dev
@@ -298,8 +299,22 @@ def test_fused_rotation_matches_rotate_then_decode(n_kv, gqa, ps, group, seq, S)
     ob.oscar_decode_attention_fused(L, dev["q"], dev["RK"], dev["bf16"], dev["bf16_table"], dev["int2"],
                                     dev["int2_table"], dev["seq_len"], dev["hist_end"], case.sm_scale, part)
     torch.cuda.synchronize()
-    assert torch.equal(part.m, ref.m) and torch.equal(part.l, ref.l) and torch.equal(part.acc, ref.acc)
+    _assert_partials_close(part, ref)
     assert ob.oscar_get_device_status() == 0
+
+
+def _assert_partials_close(part, ref, rtol=2e-5):
+    """Equal empty slots, and (m, l, acc) within rtol of the reference in each query head's own
+    scale: the partials of one slot share the weights 2^(logit - m), so a logit that moves by a
+    few fp32 ulps moves l and acc by about that much times |logit|."""
+    empty = ~torch.isfinite(ref.m)
+    assert torch.equal(empty, ~torch.isfinite(part.m))
+    mr, mp = ref.m[~empty], part.m[~empty]
+    assert torch.allclose(mp, mr, rtol=0, atol=rtol * max(1.0, float(mr.abs().max())))
+    lr, lp = ref.l[~empty], part.l[~empty]
+    assert torch.allclose(lp, lr, rtol=rtol * max(1.0, float(mr.abs().max())), atol=0)
+    ar, ap = ref.acc[~empty], part.acc[~empty]
+    assert torch.allclose(ap, ar, rtol=0, atol=rtol * max(1.0, float(mr.abs().max())) * float(ar.abs().max()))
 
 
 def _pool_bytes(i2):
