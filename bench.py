@@ -55,6 +55,8 @@ def parse_args():
     ap.add_argument("--layers", type=int, default=0, help="profiling aid: run only this many layers (0 = all)")
     ap.add_argument("--no-overlap", action="store_true",
                     help="launch every kernel after the previous one completes (no programmatic dependent launch)")
+    ap.add_argument("--no-extra", action="store_true",
+                    help="skip the batch-32 target configuration and the 32K per-step demotion measurements")
     ap.add_argument("--bf16-budget", action="store_true",
                     help="run the all-BF16 comparison at this workload's cache footprint: the largest batch of "
                          "its requests whose BF16 cache (shared-prefix pages once) fits in the HBM that the "
@@ -173,7 +175,7 @@ def source_hash(kernel: str) -> str:
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled every 100 ms while the timed region runs."""
+    """nvidia-smi clocks and throttle reasons sampled every 20 ms while the timed region runs."""
     Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -186,7 +188,7 @@ class ClockSampler:
     def __enter__(self):
         try:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.Q}",
-                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -566,6 +568,104 @@ def bulk_demotion(model, w, args, dist) -> dict:
 
 # ------------------------------------------------------------------- main ----
 
+def decode_roofline(model, w, bts, args, torch) -> dict:
+    """Per-launch roofline of oscar_decode_attention_fused: events captured around every decode
+    launch of a KR-step graph (the events split the launch-overlap edges, so a launch is timed
+    alone); algorithmic bytes per launch = the hot-path scope's per-layer bytes (INT2 codes and
+    scale/zero of the history, BF16 sink + recent, q and out)."""
+    KR = min(args.steps, 20)
+    evs = [[(torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
+            for _ in range(w.layers)] for _ in range(KR)]
+    gp = capture(lambda: model.step(events=evs[0]))
+    gk = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gk):
+        for k in range(KR):
+            model.step(events=evs[k])
+    for _ in range(args.warmup):
+        gp.replay()
+    torch.cuda.synchronize()
+    gk.replay()
+    torch.cuda.synchronize()
+    durs = [evs[k][l][0].elapsed_time(evs[k][l][1]) / 1e3 for k in range(KR) for l in range(w.layers)]
+    dur = statistics.mean(durs)
+    peaks = measured_peaks()
+    unit_bytes = bts["per_layer"]
+    achieved = unit_bytes / dur / 1e9
+    return {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": achieved / peaks["hbm_gbs"], "traffic": stored_traffic("decode_attention", w.name),
+            "kernel": "oscar_decode_attention_fused (q.R_K + INT2 history split-K in dynamic 64-token units + "
+                      "BF16 window, one layer, one launch)",
+            "bytes_per_launch": unit_bytes, "launch_us": dur * 1e6,
+            "bytes_definition": "INT2 codes + bf16 scale/zero of [sink, hist_end), BF16 K/V of the sink and recent "
+                                "window, q and out (bf16), per layer",
+            "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs copy bandwidth)"}
+
+
+def unique_bytes_per_step(w: syn.Workload, bts: dict) -> int:
+    """The step's algorithmic bytes with pages shared by several requests (the common prefix held
+    once in the page tables) counted once."""
+    if not w.shared_prefix or w.batch < 2:
+        return bts["per_step"]
+    per_tok_int2 = w.n_kv_heads * (2 * w.head_dim // 4 + 4 * 2 * (w.head_dim // w.group))
+    per_tok_bf16 = w.n_kv_heads * 2 * w.head_dim * 2
+    shared = (w.shared_prefix - w.sink) * per_tok_int2 + w.sink * per_tok_bf16
+    return bts["per_step"] - (w.batch - 1) * shared * w.layers
+
+
+def demotion_overhead(model, args, dist) -> dict:
+    """Step time with the per-step demotion (inside the decode launch) against the same step without."""
+    g0 = capture(lambda: model.step(demote=False))
+    t0 = time_graph(g0, args.steps, args.warmup, dist) / args.steps
+    g1 = capture(lambda: model.step(demote=True))
+    t1 = time_graph(g1, args.steps, args.warmup, dist) / args.steps
+    del g0, g1
+    return {"step_ms_without": t0 * 1e3, "step_ms_with": t1 * 1e3, "step_overhead": t1 / t0,
+            "rows_per_step": model.w.layers * model.w.batch * model.w.n_kv_heads * 2,
+            "bar": "step time with demotion <= 1.02 x without"}
+
+
+def workload_line(w, args, dist, world, bf16_budget: bool) -> dict:
+    """tokens/s, step time and HBM roofline of one workload's decode step (and, with bf16_budget, the
+    all-BF16 cache at the same HBM footprint); the per-step demotion's overhead when it demotes."""
+    import torch
+    model = Model(w, torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0"))), args.splits,
+                  with_bf16_cache=bf16_budget, bf16_budget=bf16_budget)
+    bts = bytes_per_step(w, model.seq, model.hist_end)
+    g = capture(lambda: model.step())
+    t = time_graph(g, args.steps, args.warmup, dist)
+    del g
+    peaks = measured_peaks()
+    sec = t / args.steps
+    uniq = unique_bytes_per_step(w, bts)
+    out = {"workload": workload_text(w), "value": job_throughput(world, w.batch, t, args.steps), "unit": "tokens/s",
+           "ms_per_step": sec * 1e3, "history_splits": model.S,
+           "bytes_per_step": bts["per_step"], "unique_bytes_per_step": uniq,
+           "roofline": {"bound": "hbm", "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                        "achieved_logical": bts["per_step"] / sec / 1e9,
+                        "frac_logical": bts["per_step"] / sec / 1e9 / peaks["hbm_gbs"],
+                        "achieved_unique": uniq / sec / 1e9, "frac_unique": uniq / sec / 1e9 / peaks["hbm_gbs"],
+                        "note": "whole step (decode launch + merge per layer); logical bytes count the shared "
+                                "prefix once per request, unique bytes once"}}
+    if model.demote:
+        out["per_step_demotion"] = demotion_overhead(model, args, dist)
+    if bf16_budget and model.bf16_full is not None:
+        gb = capture(model.step_bf16)
+        tb = time_graph(gb, args.steps, args.warmup, dist)
+        del gb
+        nb = model.bf16_batch
+        vb = job_throughput(world, nb, tb, args.steps)
+        bb = (sum(model.seq[:nb]) * w.n_kv_heads * w.head_dim * 4 + nb * w.n_q_heads * w.head_dim * 4) * w.layers
+        out["bf16_cache_fixed_budget"] = {
+            "batch": nb, "value": vb, "unit": "tokens/s", "ms_per_step": 1e3 * tb / args.steps,
+            "bytes_per_step": bb, "gbs": bb / (tb / args.steps) / 1e9, "fixed_hbm_budget": model.bf16_fit,
+            "int2_job_speedup": out["value"] / vb,
+            "comparison": "job-level tokens/s of both caches in the same HBM footprint"}
+    del model
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
+
+
 def main():
     args = parse_args()
     w = syn.WORKLOADS[args.workload]
@@ -590,8 +690,8 @@ def main():
                   bf16_budget=args.bf16_budget)
     torch.cuda.synchronize()
     # The step's kernels read pools, tables and lengths that no kernel of the step writes
-    # (the per-step demotion runs on its own stream and writes positions the step does not
-    # read from INT2), so consecutive kernels may overlap.
+    # (the per-step demotion writes positions the step does not read from INT2), so
+    # consecutive kernels may overlap.
     ob.oscar_set_launch_overlap(not args.no_overlap)
     bts = bytes_per_step(w, model.seq, model.hist_end)
 
@@ -601,29 +701,7 @@ def main():
         t = time_graph(g, args.steps, args.warmup, dist)
     ms_step = 1e3 * t / args.steps
     value = job_throughput(world, w.batch, t, args.steps)
-
-    # roofline: per-launch durations of the decode-attention call, events captured in a KR-step graph
-    KR = min(args.steps, 20)
-    evs = [[(torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
-            for _ in range(w.layers)] for _ in range(KR)]
-    gp = capture(lambda: model.step(events=evs[0]))
-    gk = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(gk):
-        for k in range(KR):
-            model.step(events=evs[k])
-    for _ in range(args.warmup):
-        gp.replay()
-    torch.cuda.synchronize()
-    gk.replay()
-    torch.cuda.synchronize()
-    durs = [evs[k][l][0].elapsed_time(evs[k][l][1]) / 1e3 for k in range(KR) for l in range(w.layers)]
-    dur = statistics.mean(durs)
-    peaks = measured_peaks()
-    # one decode-attention launch: INT2 history + BF16 window + q (bf16) + R_K (fp32, one per kv head)
-    unit_bytes = (bts["int2_per_layer"] + bts["bf16_per_layer"] + w.batch * w.n_q_heads * w.head_dim * 2
-                  + w.n_kv_heads * w.head_dim * w.head_dim * 4)
-    achieved = unit_bytes / dur / 1e9
-    traffic = stored_traffic("decode_attention", w.name)
+    roof = decode_roofline(model, w, bts, args, torch)
 
     # e2e: q from pinned host memory -> step -> out to pinned host memory, every step
     q_host = [torch.empty_like(model.q_all, device="cpu").pin_memory() for _ in range(2)]
@@ -677,6 +755,18 @@ def main():
             bf16.update({"batch": nb, "fixed_hbm_budget": model.bf16_fit,
                          "comparison": "job-level tokens/s of both caches in the same HBM footprint"})
     assert ob.oscar_get_device_status() == 0
+    del g, gd, gs, model
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+    # the other single-GPU configurations of the hot path's scope: the batch-32 target (ragged
+    # 64K-100K contexts, 16K shared prefix, per-step demotion) with the all-BF16 cache at the same
+    # HBM footprint, and the 32K context whose every step demotes
+    extra = None
+    if not args.no_extra and args.workload == "qwen3_8b_100k" and not args.layers:
+        extra = {"target_batch32": workload_line(syn.WORKLOADS["qwen3_8b_b32_ragged"], args, dist, world, True),
+                 "ctx32k_per_step_demotion": workload_line(syn.WORKLOADS["qwen3_8b_32k"], args, dist, world, False)}
+        assert ob.oscar_get_device_status() == 0
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -687,25 +777,31 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "fp32", "data": "synthetic",
+            "vs_baseline": None, "dtype": "fp32 accumulate, f16 hi+lo split MMA operands", "data": "synthetic",
             "config": {"workload": workload_text(w), "batch": w.batch, "layers": w.layers,
-                       "history_splits": model.S,
+                       "history_splits": model_splits(w, args),
                        "l2": f"inputs larger than L2: {bts['per_step'] / 1e9:.2f} GB read per step, 129 MB L2",
                        "kv_storage": "INT2 history (codes + bf16 scale/zero per group) + BF16 sink/recent",
                        "timing": "CUDA graph of one step, CUDA events, K replays"},
             "hbm_gbs": bts["per_step"] / (t / args.steps) / 1e9 * world,
             "bytes_per_step": bts["per_step"],
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
-                         "kernel": "oscar_decode_attention_fused (q.R_K + INT2 history split-K in dynamic 64-token units + BF16 window, one layer, one launch)",
-                         "bytes_per_launch": unit_bytes, "launch_us": dur * 1e6,
-                         "peak_source": f"{peaks['source']} (MEASURED_PEAKS.json hbm_gbs copy bandwidth)"},
-            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": model.launches_per_step() * args.steps,
-            "clocks": clk.summary(), "bf16_cache": bf16, "demotion": demotion,
+            "roofline": roof,
+            "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": 2 * w.layers * args.steps,
+            "clocks": clk.summary(), "bf16_cache": bf16, "demotion": demotion, "other_configs": extra,
         }
         print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
+
+
+def model_splits(w, args) -> int:
+    from bit_kv_cache_oscar_gb300 import binding as ob
+    import torch
+    L = ob.Layout(w.n_kv_heads, w.gqa, w.page_size, w.group, w.sink, w.recent)
+    seq = syn.context_lengths(w)
+    hist = [min(t, max(w.sink, t - w.recent - (1 if w.demote_per_step else 0))) for t in seq]
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return args.splits or ob.oscar_suggest_splits(L, w.batch, max(hist) - w.sink, sms)
 
 
 if __name__ == "__main__":

@@ -8,17 +8,23 @@
 // tokens stay BF16 and unrotated, so they meet the unrotated query.
 //
 // Structure (same pipeline as the INT2 kernel): a producer warp stages (kv head,
-// 16-token tile) units of K and V rows into shared memory with cp.async (16-byte
-// chunks XOR-swizzled by row so that ldmatrix is conflict-free) and signals an
-// mbarrier per stage; 8 consumer warps take one unit each per stage.  q and K are
+// 16-token tile) units of K and V rows into shared memory and signals an mbarrier
+// per stage; 8 consumer warps take one unit each per stage.  With 8 kv heads and the
+// whole cache (the comparison kernel) a stage is one tile of all 8 heads, moved by
+// 32 tensor-map boxes of 16 rows x 64 channels (128-byte swizzle: 16-byte chunk c of
+// row r at c ^ (r & 7)); otherwise by 16-byte cp.async chunks under the same swizzle
+// of 256-byte rows.  Either way the ldmatrix reads are conflict-free.  q and K are
 // both bf16, so S = K q^T runs on mma.sync bf16 with exact products; P V takes
 // V^T through ldmatrix.trans and P split into bf16 hi + lo parts (4 query heads x
 // {hi, lo} fill the 8 MMA columns).  Online softmax in the base-2 domain.
 
+#include <cuda.h>
 #include <cuda_bf16.h>
+#include <cstring>
 
 #include "oscar_internal.cuh"
 #include "ptx.cuh"
+#include "tma.cuh"
 
 namespace oscar {
 namespace {
@@ -58,11 +64,16 @@ struct Tiles {
     __device__ int tile(int k) const { return n_sink ? (k < n_sink ? k : rec0 + (k - n_sink)) : first + k; }
 };
 
-template <int G>
-__global__ void __launch_bounds__(kThreads, 1) bf16_mma_kernel(BfArgs a) {
+// TMA: mode 1 with 8 kv heads (a stage = one tile of every head, tensor-map boxes); tmk / tmv map
+// the BF16 pool's K / V as [rows][8 heads][128 channels] bf16.
+template <int G, bool TMA>
+__global__ void __launch_bounds__(kThreads, 1)
+    bf16_mma_kernel(BfArgs a, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
     constexpr int NT = (G == 8) ? 2 : 1;
     constexpr int NCOL = 8 * NT;
-    extern __shared__ __align__(128) uint8_t smem[];
+    extern __shared__ __align__(128) uint8_t smem_raw[];
+    // tensor-map boxes land on 1024-byte boundaries: the carve-up starts at an aligned address
+    uint8_t *smem = smem_raw + ((1024u - (saddr(smem_raw) & 1023u)) & 1023u);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);
     uint8_t *stage0 = smem + a.stage_off;
 
@@ -102,7 +113,7 @@ __global__ void __launch_bounds__(kThreads, 1) bf16_mma_kernel(BfArgs a) {
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
-            mbar_init(saddr(&bars[i]), 32);
+            mbar_init(saddr(&bars[i]), TMA ? 1 : 32);   // TMA: the expect-tx arrival; else 32 cp.async
             mbar_init(saddr(&bars[4 + i]), kCW);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -111,6 +122,7 @@ __global__ void __launch_bounds__(kThreads, 1) bf16_mma_kernel(BfArgs a) {
 
     // ------------------------------------------------------------ producer --
     if (warp == kCW) {
+        int armed = 0;
         for (int it = 0; it < n_iters; ++it) {
             const int st = it % kStages;
             if (it >= kStages && !mbar_wait(saddr(&bars[4 + st]), ((it / kStages) - 1) & 1)) {
@@ -118,6 +130,25 @@ __global__ void __launch_bounds__(kThreads, 1) bf16_mma_kernel(BfArgs a) {
                 break;
             }
             const uint32_t sb = saddr(stage0 + st * kStageBytes);
+            if constexpr (TMA) {
+                // one tile of all 8 heads: lane = 16 kind + 2 head + half (kind 0 K, 1 V) copies the box
+                // of 16 rows x 64 channels of that head and half, to (kind, head, half) x 2 KB
+                const int pos0 = tl.tile(it) * kTileTokens;
+                const int page = a.pt[(size_t)b * a.max_pages + pos0 / a.page_size];
+                const bool ok = page >= 0 && page < a.pool.n_pages;
+                if (lane == 0) {
+                    if (!ok) flag_status(a.status, OSCAR_DEV_BAD_BF16_PAGE);
+                    mbar_arrive_expect_tx(saddr(&bars[st]), ok ? (uint32_t)kStageBytes : 0u);
+                }
+                armed = it + 1;
+                __syncwarp();
+                if (ok) {
+                    const int row0 = page * a.page_size + pos0 % a.page_size;
+                    const int kind = lane >> 4, head = (lane >> 1) & 7, half = lane & 1;
+                    tma_load_3d(sb + lane * 2048, kind ? &tmv : &tmk, half * 64, head, row0, saddr(&bars[st]));
+                }
+                continue;
+            }
             for (int u = 0; u < kCW; ++u) {
                 const int k = it * tps + u / Hc;
                 if (k >= tl.n) break;
@@ -144,6 +175,12 @@ __global__ void __launch_bounds__(kThreads, 1) bf16_mma_kernel(BfArgs a) {
             cp_async_arrive(saddr(&bars[st]));
         }
         asm volatile("cp.async.wait_all;" ::: "memory");
+        if constexpr (TMA) {
+            // no copy may still be landing when the CTA leaves (see the INT2 kernel's copy warp)
+            for (int k = armed > kStages ? armed - kStages : 0; k < armed; ++k)
+                if (!mbar_wait(saddr(&bars[k % kStages]), (k / kStages) & 1) && lane == 0)
+                    flag_status(a.status, OSCAR_DEV_WAIT_TIMEOUT);
+        }
         return;
     }
 
@@ -193,8 +230,16 @@ __global__ void __launch_bounds__(kThreads, 1) bf16_mma_kernel(BfArgs a) {
             const int pos0 = tl.tile(k) * kTileTokens;
             const int page = a.pt[(size_t)b * a.max_pages + pos0 / a.page_size];
             if (page >= 0 && page < a.pool.n_pages) {
-                const uint32_t Kb = saddr(stage0 + st * kStageBytes + warp * kUnitBytes);
-                const uint32_t Vb = Kb + 4096;
+                // TMA: head h's boxes at (h * 2 + half) x 2 KB (K) and 32 KB further (V), rows of 128 bytes;
+                // cp.async: this warp's unit, K rows of 256 bytes then V rows 4 KB further
+                const uint32_t Kb = TMA ? saddr(stage0 + st * kStageBytes + h * 4096)
+                                        : saddr(stage0 + st * kStageBytes + warp * kUnitBytes);
+                const uint32_t Vb = Kb + (TMA ? 32768 : 4096);
+                // 16-byte chunk ch (0..15) of row r: its address under either layout
+                auto chunk_addr = [&](uint32_t base, int r, int ch) -> uint32_t {
+                    return TMA ? base + (ch >> 3) * 2048 + r * 128 + (((ch & 7) ^ (r & 7)) << 4)
+                               : base + r * 256 + ((ch ^ (r & 7)) << 4);
+                };
                 float sacc[NT][4];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt)
@@ -204,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1) bf16_mma_kernel(BfArgs a) {
                 for (int ks = 0; ks < 8; ++ks) {
                     uint32_t a0, a1, a2, a3;
                     const int ch = 2 * ks + qk_half;
-                    ldmatrix_x4(Kb + qk_row * 256 + ((ch ^ (qk_row & 7)) << 4), a0, a1, a2, a3);
+                    ldmatrix_x4(chunk_addr(Kb, qk_row, ch), a0, a1, a2, a3);
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) mma16816_bf16(sacc[nt], a0, a1, a2, a3, bq[nt][ks][0], bq[nt][ks][1]);
                 }
@@ -259,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1) bf16_mma_kernel(BfArgs a) {
                 for (int mt = 0; mt < 8; ++mt) {
                     uint32_t a0, a1, a2, a3;
                     const int ch = 2 * mt + pv_half;
-                    ldmatrix_x4_trans(Vb + pv_row * 256 + ((ch ^ (pv_row & 7)) << 4), a0, a1, a2, a3);
+                    ldmatrix_x4_trans(chunk_addr(Vb, pv_row, ch), a0, a1, a2, a3);
 #pragma unroll
                     for (int nt = 0; nt < NT; ++nt) mma16816_bf16(oacc[nt][mt], a0, a1, a2, a3, bw[nt][0], bw[nt][1]);
                 }
@@ -356,15 +401,40 @@ __global__ void __launch_bounds__(kThreads, 1) bf16_mma_kernel(BfArgs a) {
     }
 }
 
+// The BF16 pool's K or V, [rows = n_pages * page_size][8 heads][128 channels] bf16, as a 3-D tensor
+// map whose box is 64 channels x 1 head x 16 rows (128-byte rows, 128-byte swizzle).
+bool pool_tensor_map(CUtensorMap *tm, const uint16_t *base, long long rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn || !base) return false;
+    const cuuint64_t dims[3] = {128, 8, (cuuint64_t)rows};
+    const cuuint64_t strides[2] = {256, 2048};
+    const cuuint32_t box[3] = {64, 1, (cuuint32_t)kTileTokens};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<uint16_t *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int G>
 cudaError_t launch_bf(BfArgs a, dim3 grid, cudaStream_t st) {
     constexpr int NT = (G == 8) ? 2 : 1;
     a.ws_bytes = 8 * NT * 16 * 2;
-    a.stage_off = 128 + ((kCW * a.ws_bytes + 127) & ~127);
+    // stages start 1024-byte aligned (tensor-map boxes with 128-byte swizzle); the kernel rounds the
+    // dynamic shared memory base up to 1024 bytes
+    a.stage_off = (128 + kCW * a.ws_bytes + 1023) & ~1023;
     const int combine = kCW * NT * 4 * (2 + kHeadDim) * 4;
-    const int smem = a.stage_off + (kStages * kStageBytes > combine ? kStages * kStageBytes : combine);
-    if (cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void *>(bf16_mma_kernel<G>), smem)) return e;
-    bf16_mma_kernel<G><<<grid, kThreads, smem, st>>>(a);
+    const int smem = 1024 + a.stage_off + (kStages * kStageBytes > combine ? kStages * kStageBytes : combine);
+    const bool tma = a.mode == 1 && a.n_kv == 8;
+    CUtensorMap tmk, tmv;
+    memset(&tmk, 0, sizeof(tmk));
+    memset(&tmv, 0, sizeof(tmv));
+    if (tma) {
+        const long long rows = (long long)a.pool.n_pages * a.page_size;
+        if (!pool_tensor_map(&tmk, a.pool.k, rows) || !pool_tensor_map(&tmv, a.pool.v, rows)) return cudaErrorInvalidValue;
+    }
+    auto kern = tma ? bf16_mma_kernel<G, true> : bf16_mma_kernel<G, false>;
+    if (cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void *>(kern), smem)) return e;
+    kern<<<grid, kThreads, smem, st>>>(a, tmk, tmv);
     return cudaGetLastError();
 }
 

@@ -122,11 +122,12 @@ struct MmaArgs {
     int csize;        // CTAs per cluster; each cluster writes one partial slot
     int res_off;      // byte offset (from the first stage) of the per-CTA result area
     int hist_ctas;    // CTAs of grid.x that take the history (after the window CTAs)
-    int win_ctas;     // CTAs [0, win_ctas) of grid.x take the BF16 window (0 or one cluster)
-    int win_off;      // byte offset (from the first stage) of the window CTAs' warp results
+    int win_ctas;     // CTAs [0, win_ctas) of grid.x take the BF16 window (whole clusters)
+    int win_heads;    // kv heads per window cluster
     const float *RK;            // non-null: history CTAs rotate q themselves (q_rot unused)
     int rot_off;                // byte offset (from the aligned base) of the rotated-query rows [Hq][128]
-    int wbuf_off, wbuf_tok;     // window CTAs: two row buffers (from the first stage), tokens per buffer
+    int wbuf_tok;               // window CTAs: tokens per row buffer (two buffers from the first stage)
+    int wbuf_bytes;             // window CTAs: bytes available for the two buffers
     int rk_chunk;               // bytes of R staged per step in the stage area by the window CTAs' demotion
     const uint16_t *q;          // raw bf16 queries (window CTAs, and the rotation when RK is set)
     FusedDemotion dem;          // per-step demotion done by the window CTAs (dem.dem_pos NULL: none)
@@ -135,35 +136,55 @@ struct MmaArgs {
     int32_t *arrivals;          // [batch]: +1 per cluster once its partial slot is written
     // dynamic tile scheduling (NULL: fixed splits): [batch] units taken, [batch] CTAs done
     int32_t *sched;
+    int pf_units;               // dynamic units: the taker of unit u brings unit u + pf_units into L2 (0: none)
     Bf16PoolView bpool;         // BF16 sink/recent pool and its page table (window CTAs)
     const int32_t *bpt;
 };
 
 // Per-CTA result area: m [Hq], l [Hq], then acc [Hq][128] from float res_acc(Hq) on, a multiple
-// of 4 floats so that the accumulator rows take 16-byte vector stores for any Hq.
+// of 4 floats so that the accumulator rows take 16-byte vector stores for any Hq.  The cluster
+// combine's receive area follows it: one record per (source CTA, query head), kRec floats each.
 __host__ __device__ constexpr int res_acc(int Hq) { return (2 * Hq + 3) & ~3; }
+__host__ __device__ constexpr int res_floats(int Hq) { return res_acc(Hq) + Hq * kHeadDim; }
+constexpr int kRec = kHeadDim + 4;   // acc [128], m, l, 2 unused
+// bytes of the receive area for n query heads (clusters of at most 8 CTAs)
+__host__ __device__ constexpr int recv_bytes(int n) { return (n + 7) * kRec * 4; }
 
 // Cluster reduction: every CTA of a cluster holds (m, l, acc) for each query head of its
-// sub-split in shared memory; CTA `rank` combines query heads rank, rank + C, ... over the
-// C CTAs in rank order and writes partial slot `slot`.  Every thread calls this once.
-__device__ __forceinline__ void cluster_combine(const MmaArgs &a, const float *res, int Hq, int b, int slot) {
+// sub-split in `res`; CTA `rank` combines query heads hq0 + rank, hq0 + rank + C, ... (of the nhq
+// heads from hq0 on) over the C CTAs in rank order and writes partial slot `slot`.  Each CTA first
+// pushes its results to the owning CTAs (16-byte remote stores into their receive areas, right
+// after `res`), so that the owners combine from their own shared memory.  Every thread calls this.
+__device__ __forceinline__ void cluster_combine(const MmaArgs &a, const float *res, int Hq, int b, int slot,
+                                                int hq0 = 0, int nhq = -1) {
     const int C = a.csize;
-    cluster_sync_all();
+    if (nhq < 0) nhq = Hq;
+    const int J = (nhq + C - 1) / C;                     // query heads per owning CTA
+    float *recv = const_cast<float *>(res) + res_floats(Hq);   // [C sources][J][kRec]
+    cluster_sync_all();                 // every CTA of the cluster has its result and a free receive area
     const int rank = (int)cluster_ctarank();
+    constexpr int kQ = kRec / 4;                         // float4 per record
+    for (int e = threadIdx.x; e < nhq * kQ; e += blockDim.x) {
+        const int i = e / kQ, p = e % kQ, hq = hq0 + i;
+        const float4 v = p < kHeadDim / 4 ? *reinterpret_cast<const float4 *>(res + res_acc(Hq) + hq * kHeadDim + 4 * p)
+                                          : make_float4(res[hq], res[Hq + hq], 0.f, 0.f);
+        float *dst = recv + (size_t)(rank * J + i / C) * kRec + 4 * p;
+        st_dsmem_f32x4(saddr(dst), (uint32_t)(i % C), v);
+    }
+    cluster_sync_all();                 // every record is in place (no CTA reads another's memory after this)
     const size_t S1 = (size_t)a.out.S + 1;
-    const int mine = (Hq - rank + C - 1) / C;
-    const uint32_t rm = saddr(res), rl = rm + Hq * 4, ra = rm + res_acc(Hq) * 4;
+    const int mine = (nhq - rank + C - 1) / C;
     for (int e = threadIdx.x; e < mine * kHeadDim; e += blockDim.x) {
-        const int hq = rank + (e / kHeadDim) * C, d = e % kHeadDim;
+        const int j = e / kHeadDim, d = e % kHeadDim, hq = hq0 + rank + j * C;
         float M = -INFINITY;
-        for (int q = 0; q < C; ++q) M = fmaxf(M, ld_dsmem_f32(rm + hq * 4, q));
+        for (int q = 0; q < C; ++q) M = fmaxf(M, recv[(q * J + j) * kRec + kHeadDim]);
         float L = 0.f, A = 0.f;
         if (M != -INFINITY) {
             for (int q = 0; q < C; ++q) {
-                const float mq = ld_dsmem_f32(rm + hq * 4, q);
-                const float f = exp2f(mq - M);
-                L = fmaf(ld_dsmem_f32(rl + hq * 4, q), f, L);
-                A = fmaf(ld_dsmem_f32(ra + (hq * kHeadDim + d) * 4, q), f, A);
+                const float *r = recv + (q * J + j) * kRec;
+                const float f = exp2f(r[kHeadDim] - M);
+                L = fmaf(r[kHeadDim + 1], f, L);
+                A = fmaf(r[d], f, A);
             }
         }
         const size_t row = ((size_t)b * Hq + hq) * S1 + slot;
@@ -173,7 +194,6 @@ __device__ __forceinline__ void cluster_combine(const MmaArgs &a, const float *r
             a.out.l[row] = L;
         }
     }
-    cluster_sync_all();                 // no CTA leaves while its shared memory is being read
 }
 
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -258,21 +278,26 @@ __device__ __forceinline__ void window_fold(const float (&q)[G][4], const uint2 
     }
 }
 
-// ---- BF16 sink/recent window, on CUDA cores, in the CTAs after the history ones.
+// ---- BF16 sink/recent window, on CUDA cores, in the window clusters (first in the grid).
 // Window positions of request b, in order: [0, n0) then [lo1, T), n0 = min(sink, T),
-// lo1 = max(h_end, n0).  Window CTA wr of wc takes positions [wr*n/wc, (wr+1)*n/wc); warp w
-// takes kv head w % Hkv and every (8/Hkv)-th position of that range; lane l owns channels
-// 4l..4l+3.  Each token is folded into a per-warp online softmax (base 2), the warps of a kv
-// head are combined in a fixed order, and the CTA's result goes to `res` (cluster) or
-// straight to partial slot S.  Every thread of the CTA calls this.
+// lo1 = max(h_end, n0).  Window cluster k takes kv heads [k nh, (k + 1) nh) (nh = win_heads);
+// its CTA of rank r takes positions [r n / C, (r + 1) n / C).  Warp w takes kv head k nh + w % nh
+// and every (8 / nh)-th group of positions of that range; lane l owns channels 4l..4l+3.  Each
+// token is folded into a per-warp online softmax (base 2), the warps of a kv head are combined in
+// a fixed order, and the CTA's result goes to the cluster combine or straight to partial slot S.
+// The K and V rows come through shared memory: the copy warp fills chunks of up to 32 tokens (this
+// cluster's heads of each token: one bulk copy per token for K and one for V) in two buffers, so
+// that up to two chunks are in flight at once.  `area` is the CTA's stage area; after the fold it
+// holds the warp results and the CTA result.  Every thread of the CTA calls this.
 template <int G>
-__device__ void window_cta(const MmaArgs &a, float *wsm, float *res, uint8_t *wbuf, uint64_t *wbar, int T, int he,
-                           int b, int wr, int wc) {
+__device__ void window_cta(const MmaArgs &a, uint8_t *area, uint64_t *wbar, int T, int he, int b, int wr) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int Hkv = a.n_kv, Hq = Hkv * G, nsub = kCW / Hkv, S = a.out.S;
+    const int Hkv = a.n_kv, Hq = Hkv * G, S = a.out.S;
+    const int C = a.csize, nh = a.win_heads;
+    const int h0 = (wr / C) * nh, rk = wr % C;
     const int n0 = min(a.sink, T), lo1 = max(he, n0);
     const int n = n0 + (T - lo1);
-    const int i_lo = (int)((long long)wr * n / wc), i_hi = (int)((long long)(wr + 1) * n / wc);
+    const int i_lo = (int)((long long)rk * n / C), i_hi = (int)((long long)(rk + 1) * n / C);
     float m[G], l[G], acc[G][4];
 #pragma unroll
     for (int hh = 0; hh < G; ++hh) {
@@ -281,7 +306,7 @@ __device__ void window_cta(const MmaArgs &a, float *wsm, float *res, uint8_t *wb
 #pragma unroll
         for (int c = 0; c < 4; ++c) acc[hh][c] = 0.f;
     }
-    const int h = warp % Hkv, sub = warp / Hkv;
+    const int hl = warp % nh, h = h0 + hl, sub = warp / nh, nsub = kCW / nh;
     float q[G][4];
     if (warp < kCW) {
 #pragma unroll
@@ -293,71 +318,56 @@ __device__ void window_cta(const MmaArgs &a, float *wsm, float *res, uint8_t *wb
     }
     constexpr int U = 4;
     if (a.wbuf_tok >= U) {
-        // The CTA's rows go through shared memory: chunks of CH tokens (all kv heads, K then V) in two
-        // buffers, each filled by one thread with bulk copies of the chunk's page pieces, so a chunk
-        // costs one round trip; the warps fold a chunk while the next one lands.
         const int CH = a.wbuf_tok, nt = i_hi - i_lo, nch = (nt + CH - 1) / CH;
-        const int rowb = Hkv * kHeadDim * 2;                  // one token's K (or V) row, all heads
+        const int rowb = nh * kHeadDim * 2;                   // this cluster's heads of one token's K (or V) row
         uint32_t *valid = reinterpret_cast<uint32_t *>(wbar + 2);   // per buffer: bit j = token j's page is valid
-        auto fill = [&](int k) {                              // thread 0
-            const int buf = k & 1, j0 = k * CH, n = min(CH, nt - j0);
-            uint8_t *dk = wbuf + (size_t)buf * 2 * CH * rowb, *dv = dk + (size_t)CH * rowb;
-            fence_proxy_async_smem();                         // the warps' reads of this buffer came first
-            uint32_t bytes = 0, vbits = 0;
-            for (int j = 0; j < n;) {                         // page pieces of contiguous positions
-                const int i = i_lo + j0 + j;
+        auto fill = [&](int k) {                              // the copy warp; lane j copies token j of the chunk
+            const int buf = k & 1, j0 = k * CH, cnt = min(CH, nt - j0);
+            uint8_t *dk = area + (size_t)buf * 2 * CH * rowb, *dv = dk + (size_t)CH * rowb;
+            size_t row = 0;
+            bool ok = false;
+            if (lane < cnt) {
+                const int i = i_lo + j0 + lane;
                 const int p = i < n0 ? i : lo1 + (i - n0);
-                const int run_end = i < n0 ? n0 : T;
-                const int cnt = min(min((p / a.page_size + 1) * a.page_size, run_end) - p, n - j);
                 const int page = p / a.page_size < a.max_pages ? a.bpt[(size_t)b * a.max_pages + p / a.page_size] : -1;
-                if (page >= 0 && page < a.bpool.n_pages) {
-                    vbits |= (cnt == 32 ? 0xffffffffu : (1u << cnt) - 1u) << j;
-                    bytes += 2u * cnt * rowb;
-                } else {
-                    flag_status(a.status, OSCAR_DEV_BAD_BF16_PAGE);
-                }
-                j += cnt;
+                ok = page >= 0 && page < a.bpool.n_pages;
+                if (ok) row = ((size_t)page * a.page_size + p % a.page_size) * Hkv + h0;
+                else flag_status(a.status, OSCAR_DEV_BAD_BF16_PAGE);
             }
-            valid[buf] = vbits;
-            mbar_arrive_expect_tx(saddr(&wbar[buf]), bytes);
-            for (int j = 0; j < n;) {
-                const int i = i_lo + j0 + j;
-                const int p = i < n0 ? i : lo1 + (i - n0);
-                const int run_end = i < n0 ? n0 : T;
-                const int cnt = min(min((p / a.page_size + 1) * a.page_size, run_end) - p, n - j);
-                const int page = p / a.page_size < a.max_pages ? a.bpt[(size_t)b * a.max_pages + p / a.page_size] : -1;
-                if (page >= 0 && page < a.bpool.n_pages) {
-                    const size_t row = ((size_t)page * a.page_size + p % a.page_size) * Hkv;
-                    tma_load_1d(saddr(dk + (size_t)j * rowb), a.bpool.k + row * kHeadDim, (uint32_t)cnt * rowb,
-                                saddr(&wbar[buf]));
-                    tma_load_1d(saddr(dv + (size_t)j * rowb), a.bpool.v + row * kHeadDim, (uint32_t)cnt * rowb,
-                                saddr(&wbar[buf]));
-                }
-                j += cnt;
+            const uint32_t vbits = __ballot_sync(0xffffffffu, ok);
+            fence_proxy_async_smem();                         // the warps' reads of this buffer came first
+            if (lane == 0) {
+                valid[buf] = vbits;
+                mbar_arrive_expect_tx(saddr(&wbar[buf]), 2u * (uint32_t)__popc(vbits) * rowb);
+            }
+            __syncwarp();
+            if (ok) {
+                tma_load_1d(saddr(dk + (size_t)lane * rowb), a.bpool.k + row * kHeadDim, rowb, saddr(&wbar[buf]));
+                tma_load_1d(saddr(dv + (size_t)lane * rowb), a.bpool.v + row * kHeadDim, rowb, saddr(&wbar[buf]));
             }
         };
         if (threadIdx.x == 0) {
             mbar_init(saddr(&wbar[0]), 1);
             mbar_init(saddr(&wbar[1]), 1);
             asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-            for (int k = 0; k < 2 && k < nch; ++k) fill(k);
         }
         __syncthreads();
+        if (warp == kCW)
+            for (int k = 0; k < 2 && k < nch; ++k) fill(k);
         for (int k = 0; k < nch; ++k) {
-            const int buf = k & 1, n = min(CH, nt - k * CH);
-            if (!mbar_wait(saddr(&wbar[buf]), (k >> 1) & 1) && threadIdx.x == 0)
-                flag_status(a.status, OSCAR_DEV_WAIT_TIMEOUT);
+            const int buf = k & 1, cnt = min(CH, nt - k * CH);
             if (warp < kCW) {
+                if (!mbar_wait(saddr(&wbar[buf]), (k >> 1) & 1) && lane == 0) flag_status(a.status, OSCAR_DEV_WAIT_TIMEOUT);
                 const uint32_t vb = valid[buf];
-                const uint8_t *dk = wbuf + (size_t)buf * 2 * CH * rowb, *dv = dk + (size_t)CH * rowb;
-                for (int j0 = sub * U; j0 < n; j0 += U * nsub) {
+                const uint8_t *dk = area + (size_t)buf * 2 * CH * rowb, *dv = dk + (size_t)CH * rowb;
+                for (int j0 = sub * U; j0 < cnt; j0 += U * nsub) {
                     uint2 kk[U], vv[U];
                     bool ok[U];
 #pragma unroll
                     for (int u = 0; u < U; ++u) {
                         const int j = j0 + u;
-                        ok[u] = j < n && ((vb >> j) & 1);
-                        const size_t off = (size_t)(ok[u] ? j : 0) * rowb + h * kHeadDim * 2;
+                        ok[u] = j < cnt && ((vb >> j) & 1);
+                        const size_t off = (size_t)(ok[u] ? j : 0) * rowb + hl * kHeadDim * 2;
                         kk[u] = reinterpret_cast<const uint2 *>(dk + off)[lane];
                         vv[u] = reinterpret_cast<const uint2 *>(dv + off)[lane];
                     }
@@ -365,8 +375,13 @@ __device__ void window_cta(const MmaArgs &a, float *wsm, float *res, uint8_t *wb
                 }
             }
             __syncthreads();                                  // buffer `buf` is consumed
-            if (threadIdx.x == 0 && k + 2 < nch) fill(k + 2);
+            if (warp == kCW && k + 2 < nch) fill(k + 2);
         }
+        // (the consumer warps waited for every fill; after a wait that gave up, the copy warp makes
+        // sure that no copy is still landing before the buffers are reused and the CTA leaves)
+        if (warp == kCW)
+            for (int k = nch > 2 ? nch - 2 : 0; k < nch; ++k)
+                if (!mbar_wait(saddr(&wbar[k & 1]), (k >> 1) & 1) && lane == 0) flag_status(a.status, OSCAR_DEV_WAIT_TIMEOUT);
     } else if (warp < kCW) {
         // (buffers too small for the layout) Tokens in chunks of 64 per warp: the chunk's page ids
         // are read once (two per lane), then U tokens' K/V rows are loaded together and folded.
@@ -407,8 +422,11 @@ __device__ void window_cta(const MmaArgs &a, float *wsm, float *res, uint8_t *wb
           }
         }
     }
+    __syncthreads();                                          // (the row buffers are consumed)
+    // warp results: wsm = [warp][G] m, [warp][G] l, [warp][G][128] acc; the CTA result after them
+    float *wsm = reinterpret_cast<float *>(area);
+    float *res = wsm + kCW * G * (2 + kHeadDim);
     if (warp < kCW) {
-        // warp results: wsm = [warp][G] m, [warp][G] l, [warp][G][128] acc
         float *wm = wsm, *wl = wsm + kCW * G, *wa = wsm + 2 * kCW * G;
 #pragma unroll
         for (int hh = 0; hh < G; ++hh) {
@@ -422,15 +440,15 @@ __device__ void window_cta(const MmaArgs &a, float *wsm, float *res, uint8_t *wb
     }
     pdl_trigger();
     __syncthreads();
-    const bool to_res = a.csize > 1;
+    const bool to_res = C > 1;
     const float *wm = wsm, *wl = wsm + kCW * G, *wa = wsm + 2 * kCW * G;
-    for (int e = threadIdx.x; e < Hq * kHeadDim; e += blockDim.x) {
-        const int hq = e / kHeadDim, d = e % kHeadDim, h = hq / G, hh = hq % G;
+    for (int e = threadIdx.x; e < nh * G * kHeadDim; e += blockDim.x) {
+        const int hq = h0 * G + e / kHeadDim, d = e % kHeadDim, hv = hq / G - h0, hh = hq % G;
         float M = -INFINITY;
-        for (int w = h; w < kCW; w += Hkv) M = fmaxf(M, wm[w * G + hh]);
+        for (int w = hv; w < kCW; w += nh) M = fmaxf(M, wm[w * G + hh]);
         float L = 0.f, A = 0.f;
         if (M != -INFINITY) {
-            for (int w = h; w < kCW; w += Hkv) {
+            for (int w = hv; w < kCW; w += nh) {
                 const float f = exp2f(wm[w * G + hh] - M);
                 L = fmaf(wl[w * G + hh], f, L);
                 A = fmaf(wa[(w * G + hh) * kHeadDim + d], f, A);
@@ -451,7 +469,7 @@ __device__ void window_cta(const MmaArgs &a, float *wsm, float *res, uint8_t *wb
             }
         }
     }
-    if (to_res) cluster_combine(a, res, Hq, b, S);
+    if (to_res) cluster_combine(a, res, Hq, b, S, h0 * G, nh * G);
 }
 
 // ---- Per-step demotion by the window CTAs: request b's position dem_pos[b] (one that left the
@@ -596,10 +614,11 @@ __device__ __forceinline__ void arrive_count(const MmaArgs &a, int b) {
 }
 
 constexpr float kLazy = 8.0f;   // log2 headroom before the running maximum is raised
-// rotated-query rows in shared memory: element d of a row at d + d / 32 (row stride 132), so
-// that the operand reads of a warp (4 heads x 4 column groups) fall in distinct banks
-constexpr int kQS = kHeadDim + kHeadDim / 32;
-__device__ __forceinline__ int qs_col(int d) { return d + (d >> 5); }
+// rotated-query rows in shared memory: element d of a row at d + 4 (d / 32) (row stride 144), so
+// that the operand reads of a warp (4 heads x 4 column groups) spread over the banks and every
+// run of 4 columns stays 16-byte aligned (the cluster's CTAs push the rows 4 columns at a time)
+constexpr int kQS = kHeadDim + kHeadDim / 8;
+__device__ __forceinline__ int qs_col(int d) { return d + 4 * (d >> 5); }
 constexpr int kWsWords = 20;    // words per P-operand column: 2 tiles x 8 + 4 (bank spread)
 
 
@@ -633,16 +652,15 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // With 8 kv heads (the tensor-map path) the stage layout is compile-time: addresses fold.
     const int Hkv = TMA ? 8 : a.n_kv, Hq = Hkv * G, S = a.out.S;
-    const int off_v = TMA ? 8 * 2048 : a.off_v, off_s = TMA ? 2 * 8 * 2048 : a.off_s;
+    constexpr int kCodesTma = kTilesPerStage * 4096;     // one array's codes of a stage (8 kv heads)
+    const int off_v = TMA ? kCodesTma : a.off_v, off_s = TMA ? 2 * kCodesTma : a.off_s;
     const int arr_bytes = TMA ? kStageTok * 8 * NGRP * 2 : a.arr_bytes;
-    const int stage_bytes = TMA ? ((2 * 8 * 2048 + 4 * kStageTok * 8 * NGRP * 2 + 127) & ~127) : a.stage_bytes;
+    const int stage_bytes = TMA ? ((2 * kCodesTma + 4 * kStageTok * 8 * NGRP * 2 + 127) & ~127) : a.stage_bytes;
     int T, he;
     read_lengths(a.seq_len, a.hist_end, b, a.sink, a.max_pages * a.page_size, a.status, T, he);
     if (s < 0) {                               // a BF16 window CTA (uniform over the cluster)
         pdl_wait();                            // q and the partials belong to the previous kernels
-        window_cta<G>(a, reinterpret_cast<float *>(stage0 + a.win_off), reinterpret_cast<float *>(stage0 + a.res_off),
-                      stage0 + a.wbuf_off, reinterpret_cast<uint64_t *>(smem + 112), T, he, b, (int)blockIdx.x,
-                      a.win_ctas);
+        window_cta<G>(a, stage0, reinterpret_cast<uint64_t *>(smem + 112), T, he, b, (int)blockIdx.x);
         // (after the cluster's last barrier: the stage area is free again)
         if (a.dem.dem_pos && !(a.sched && a.hist_ctas >= Hkv))
             window_demote(a, reinterpret_cast<float *>(smem + 128), stage0, T, he, b, (int)blockIdx.x, a.win_ctas);
@@ -666,17 +684,31 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
             mbar_init(saddr(&bars[i]), TMA ? 1 : 33);   // TMA: the expect-tx arrival; else 32 cp.async + mask
             mbar_init(saddr(&bars[4 + i]), kCW);
         }
+        if (a.RK) mbar_init(saddr(smem + 96), kCW);   // every consumer warp holds its rows of R_K
+        if (a.RK && a.csize > 1) mbar_init(saddr(smem + 104), 1);   // the peers' rotated-query rows landed
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     __syncthreads();
-    // phase 0 of the cluster barrier: the rotated queries pushed by every CTA are in place
+    // With the fused rotation each CTA of a cluster rotates the queries of some kv heads and sends
+    // the rows to its peers with bulk copies that complete on their smem + 104 barrier: every CTA
+    // initialises that barrier before any peer may copy into it (the cluster barrier below), and
+    // expects the bytes of the rows it does not compute itself.
     const bool rot_phase = a.RK && a.csize > 1;
+    if (rot_phase) {
+        cluster_sync_all();
+        if (threadIdx.x == 0) {
+            const int C = a.csize, rank = (int)cluster_ctarank();
+            const int own = rank < Hkv ? (Hkv - 1 - rank) / C + 1 : 0;
+            mbar_arrive_expect_tx(saddr(smem + 104), (uint32_t)((Hkv - own) * G * kQS * 4));
+        }
+    }
 
     // ------------------------------------------------------------ producer --
     if (warp == kCW) {
-        // The copy warp takes no part in the rotation: it arrives on phase 0 at once and streams the
-        // KV pages from the start (it waits on the phase only before the cluster's final combine).
-        if (rot_phase) cluster_arrive();
+        // The first KV copies wait until the consumer warps hold their rows of R_K: issued behind the
+        // stages of every CTA, those loads would queue behind megabytes of KV pages and delay the
+        // rotation (and so the whole loop) by microseconds.
+        if (a.RK && !mbar_wait(saddr(smem + 96), 0) && lane == 0) flag_status(a.status, OSCAR_DEV_WAIT_TIMEOUT);
         const int lgH = Hkv == 1 ? 0 : Hkv == 2 ? 1 : Hkv == 4 ? 2 : 3;
         // Page ids of 32 consecutive logical pages, lane i holding page pg_base + i: one load
         // serves 32 pages (128 tiles at 64-token pages), so the copies never wait on the table.
@@ -687,17 +719,36 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
         int pg_reg = (pg_base + lane < a.max_pages) ? prow[pg_base + lane] : -1;
         // dynamic units: the next unit and its tiles' page ids (lane j < kTilesPerStage: tile
         // t0 + j) are taken one stage ahead, so that the count and the table loads overlap the wait
+        // Units are handed out in order, so unit u + pf_units is taken about pf_units / (history CTAs)
+        // stages later: its taker-to-be finds it in L2 if the taker of u asks for it now (lanes
+        // kTilesPerStage .. 2 kTilesPerStage - 1 load its tiles' page ids and issue the L2 prefetches).
+        // This keeps more of the history in flight than the shared-memory stages hold.
         auto take_unit = [&](int &nt0, int &npg) {
             int u = 0;
             if (lane == 0) u = atomicAdd(a.sched + b, 1);
             u = __shfl_sync(0xffffffffu, u, 0);
             nt0 = u < dyn_units ? hist_first + u * kTilesPerStage : -1;
-            const int tile = nt0 + lane;
-            npg = (nt0 >= 0 && lane < kTilesPerStage && tile < tile_hi) ? prow[tile / tpp] : -1;
+            const int pu = u + a.pf_units, j = lane - kTilesPerStage;
+            const bool pf = a.pf_units > 0 && j >= 0 && j < kTilesPerStage && pu < dyn_units;
+            const int tile = pf ? hist_first + pu * kTilesPerStage + j : nt0 + lane;
+            const bool ld = pf || (nt0 >= 0 && lane < kTilesPerStage);
+            npg = (ld && tile < tile_hi) ? prow[tile / tpp] : -1;
+            if (pf && npg >= 0 && npg < a.pool.n_pages) {
+                const size_t row0 = (size_t)npg * a.page_size + (tile * kTileTokens) % a.page_size;
+                const uint32_t cb = kTileTokens * Hkv * 32, sbt = kTileTokens * Hkv * NGRP * 2;
+                prefetch_l2(a.pool.codes_k + row0 * Hkv * 32, cb);
+                prefetch_l2(a.pool.codes_v + row0 * Hkv * 32, cb);
+                const size_t so = row0 * Hkv * NGRP;
+                prefetch_l2(a.pool.scale_k + so, sbt);
+                prefetch_l2(a.pool.zero_k + so, sbt);
+                prefetch_l2(a.pool.scale_v + so, sbt);
+                prefetch_l2(a.pool.zero_v + so, sbt);
+            }
         };
         int nxt_t0 = -1, nxt_pg = -1;
         if (dyn) take_unit(nxt_t0, nxt_pg);
         bool ok = true;
+        int armed = 0;                                         // stage fills started (expect-tx armed)
         for (int it = 0; ok; ++it) {
             const int st = it % a.stages;
             if (it >= a.stages && !mbar_wait(saddr(&bars[4 + st]), ((it / a.stages) - 1) & 1)) {
@@ -705,11 +756,13 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
                 ok = false;
                 break;
             }
+            armed = it + 1;
             int t0, unit_pg = -1;                              // this stage's first tile, -1: no more
+            // (with dynamic units the next unit is taken after this stage's copies are issued: the
+            // count's round trip and the page-table load then overlap the wait for the next stage)
             if (dyn) {
                 t0 = nxt_t0;
                 unit_pg = nxt_pg;
-                if (t0 >= 0) take_unit(nxt_t0, nxt_pg);
             } else {
                 t0 = it < n_iters ? r.tile_lo + it * kTilesPerStage : -1;
             }
@@ -769,6 +822,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
                                     nsb, full);
                     }
                 }
+                if (dyn) take_unit(nxt_t0, nxt_pg);
                 continue;
             }
             for (int j = 0; j < kTilesPerStage; ++j) {
@@ -794,7 +848,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
                 const uint32_t tile_dst = saddr(sb) + j * kTileTokens * 32;
                 for (int c = lane; c < nck; c += 32) {
                     const int slot = c >> (lgH + 1), head = (c >> 1) & (Hkv - 1), half = c & 1;
-                    const uint32_t dst = tile_dst + head * 2048 + slot * 32 + half * 16;
+                    const uint32_t dst = tile_dst + head * (kStageTok * 32) + slot * 32 + half * 16;
                     cp_async16(dst, srck + c * 16);
                     cp_async16(dst + off_v, srcv + c * 16);
                 }
@@ -813,15 +867,22 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
             if (lane == 0) masks[st] = mask;
             cp_async_arrive(saddr(&bars[st]));
             if (lane == 0) mbar_arrive(saddr(&bars[st]));
+            if (dyn) take_unit(nxt_t0, nxt_pg);
         }
         asm volatile("cp.async.wait_all;" ::: "memory");
+        if constexpr (TMA) {
+            // No copy may still be landing when the CTA leaves: after a wait that gave up, the stages'
+            // last fills may be outstanding, so wait (bounded) for each of them (no wait otherwise).
+            for (int k = armed > a.stages ? armed - a.stages : 0; k < armed; ++k)
+                if (!mbar_wait(saddr(&bars[k % a.stages]), (k / a.stages) & 1) && lane == 0)
+                    flag_status(a.status, OSCAR_DEV_WAIT_TIMEOUT);
+        }
         // the last of b's history CTAs to stop taking units resets b's counters for the next launch
         if (dyn && lane == 0 && atomicAdd(a.sched + gridDim.y + b, 1) == a.hist_ctas - 1) {
             a.sched[b] = 0;
             a.sched[gridDim.y + b] = 0;
             __threadfence();
         }
-        if (rot_phase) cluster_wait();
         if (a.csize > 1) cluster_combine(a, reinterpret_cast<const float *>(stage0 + a.res_off), Hq, b, s / a.csize);
         if (a.arrivals) arrive_count(a, b);
         return;
@@ -843,48 +904,81 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
         // query head of the kv head, as fp32 FMA chains in ascending row order; q_rot is the sum of
         // the eight partial sums in warp order, and it is written into every CTA of the cluster.
         float *part = reinterpret_cast<float *>(smem + 128);          // [kCW][G][128] partial sums
+        float *qsl = part + warp * G * kHeadDim;   // this warp's rows of q ([G][16]), in its own partial area
         float4 r[16];
         auto load_r = [&](int hk) {
             const float4 *R4 = reinterpret_cast<const float4 *>(a.RK + ((size_t)hk * kHeadDim + 16 * warp) * kHeadDim) + lane;
 #pragma unroll
             for (int k = 0; k < 16; ++k) r[k] = __ldg(R4 + k * (kHeadDim / 4));
         };
+        auto load_q = [&](int hk) {
+            if (lane < 2 * G) {
+                const int g = lane >> 1, hf = lane & 1;
+                const uint4 v = reinterpret_cast<const uint4 *>(a.q + ((size_t)b * Hq + hk * G + g) * kHeadDim + 16 * warp)[hf];
+                float4 *d = reinterpret_cast<float4 *>(qsl + g * 16 + hf * 8);
+                d[0] = make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xffff0000u),
+                                   __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xffff0000u));
+                d[1] = make_float4(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xffff0000u),
+                                   __uint_as_float(v.w << 16), __uint_as_float(v.w & 0xffff0000u));
+            }
+            __syncwarp();
+        };
+        // R_K and q land before the copy warp starts: behind the stages of every CTA, these loads would
+        // queue behind megabytes of KV pages
         if (rank < Hkv) load_r(rank);
         pdl_wait();                                                  // q may come from the previous kernel
+        if (rank < Hkv) {
+            load_q(rank);
+            // (the loads have landed once their registers are read: an empty asm reads them all)
+#pragma unroll
+            for (int k = 0; k < 16; ++k) asm volatile("" ::"f"(r[k].x));
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(saddr(smem + 96));                // the copy warp may start
         for (int hk = rank; hk < Hkv; hk += C) {
-            if (hk != rank) load_r(hk);
+            if (hk != rank) {
+                load_r(hk);
+                load_q(hk);
+            }
+            float4 acc[G];
 #pragma unroll
             for (int g = 0; g < G; ++g) {
-                const uint4 *qp = reinterpret_cast<const uint4 *>(a.q + ((size_t)b * Hq + hk * G + g) * kHeadDim + 16 * warp);
-                const uint4 qa = qp[0], qb = qp[1];
-                const uint32_t qw[8] = {qa.x, qa.y, qa.z, qa.w, qb.x, qb.y, qb.z, qb.w};
-                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                acc[g] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
                 for (int k = 0; k < 16; ++k) {
-                    const float qv = __uint_as_float((k & 1) ? (qw[k >> 1] & 0xffff0000u) : (qw[k >> 1] << 16));
-                    acc.x = __fmaf_rn(qv, r[k].x, acc.x);
-                    acc.y = __fmaf_rn(qv, r[k].y, acc.y);
-                    acc.z = __fmaf_rn(qv, r[k].z, acc.z);
-                    acc.w = __fmaf_rn(qv, r[k].w, acc.w);
+                    const float qv = qsl[g * 16 + k];
+                    acc[g].x = __fmaf_rn(qv, r[k].x, acc[g].x);
+                    acc[g].y = __fmaf_rn(qv, r[k].y, acc[g].y);
+                    acc[g].z = __fmaf_rn(qv, r[k].z, acc[g].z);
+                    acc[g].w = __fmaf_rn(qv, r[k].w, acc[g].w);
                 }
-                *reinterpret_cast<float4 *>(part + (warp * G + g) * kHeadDim + 4 * lane) = acc;
             }
-            consumer_sync();
-            for (int e = threadIdx.x; e < G * kHeadDim; e += kCW * 32) {
-                const int g = e / kHeadDim, j = e % kHeadDim;
-                float v = part[g * kHeadDim + j];
+            __syncwarp();                                            // (the sums overwrite this warp's q rows)
 #pragma unroll
-                for (int w2 = 1; w2 < kCW; ++w2) v = __fadd_rn(v, part[(w2 * G + g) * kHeadDim + j]);
-                float *dst = qrot_s + (hk * G + g) * kQS + qs_col(j);
-                if (C == 1) {
-                    *dst = v;
-                } else {
-                    for (int q = 0; q < C; ++q) st_dsmem_f32(saddr(dst), (uint32_t)q, v);
+            for (int g = 0; g < G; ++g) *reinterpret_cast<float4 *>(part + (warp * G + g) * kHeadDim + 4 * lane) = acc[g];
+            consumer_sync();
+            // q_rot columns j .. j + 3 of query head g: the partial sums in warp order, pushed to every CTA
+            for (int e = threadIdx.x; e < G * kHeadDim / 4; e += kCW * 32) {
+                const int g = e / (kHeadDim / 4), j = (e % (kHeadDim / 4)) * 4;
+                float4 v = *reinterpret_cast<const float4 *>(part + g * kHeadDim + j);
+#pragma unroll
+                for (int w2 = 1; w2 < kCW; ++w2) {
+                    const float4 u = *reinterpret_cast<const float4 *>(part + (w2 * G + g) * kHeadDim + j);
+                    v.x = __fadd_rn(v.x, u.x);
+                    v.y = __fadd_rn(v.y, u.y);
+                    v.z = __fadd_rn(v.z, u.z);
+                    v.w = __fadd_rn(v.w, u.w);
                 }
+                *reinterpret_cast<float4 *>(qrot_s + (hk * G + g) * kQS + qs_col(j)) = v;
             }
-            consumer_sync();                                         // the partial sums are consumed
+            consumer_sync();                                         // the rows are complete, the sums consumed
+            if (C > 1 && threadIdx.x < C && threadIdx.x != rank) {   // one bulk copy of the rows per peer
+                fence_proxy_async_smem();
+                const uint32_t rows = saddr(qrot_s + hk * G * kQS);
+                dsmem_bulk_copy(rows, rows, (uint32_t)(G * kQS * 4), saddr(smem + 104), (uint32_t)threadIdx.x);
+            }
         }
-        if (C > 1) cluster_sync_all();                               // phase 0 (the copy warp arrived early)
+        if (C > 1 && !mbar_wait(saddr(smem + 104), 0) && lane == 0) flag_status(a.status, OSCAR_DEV_WAIT_TIMEOUT);
     }
     // with dynamic history units the per-step demotion of kv head s is done here, by history CTA s
     if (a.dem.dem_pos && a.sched && a.hist_ctas >= Hkv && s < Hkv && threadIdx.x < kHeadDim)
@@ -1012,7 +1106,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
         }
     }
     auto tile_base = [&](const uint8_t *arr, int j) -> const uint8_t * {
-        return TMA ? arr + j * 4096 + (h >> 2) * 2048 : arr + h * 2048 + j * (kTileTokens * 32);
+        return TMA ? arr + j * 4096 + (h >> 2) * 2048 : arr + h * (kStageTok * 32) + j * (kTileTokens * 32);
     };
     const float csc = cscq;                     // logit scale of the MMA dot products
     const int rs = Hkv * NGRP;                  // scale/zero elements per token row in a stage
@@ -1033,23 +1127,35 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
             for (int c = 0; c < 4; ++c) oacc[nt][mt][c] = 0.f;
     }
 
+    // Value-scale normalisation (both loops): vlim is a power of two above every value scale seen so
+    // far (raised with a stage's maximum; the accumulators rescale by the ratio) and vmul = 128 / vlim,
+    // so that w = p * scale_v * vmul < 2^8 * 2^7 stays inside the f16 range of the split PV operand
+    // whatever the scales' magnitude; vlim / 128 goes into the output.
+    float vlim = 0.f, vmul = 0.f;
+    // raise the bound to cover vm (warp-uniform); returns the factor for the accumulators
+    auto raise_vlim = [&](float vm) -> float {
+        if (!(vm > vlim)) return 1.f;
+        // vm in [2^(eb-127), 2^(eb-126)): vlim = 2^(eb-126), vmul = 2^7 / vlim
+        const int eb = min(max((int)((__float_as_uint(vm) >> 23) & 0xffu), 7), 252);
+        const float nl = __uint_as_float((uint32_t)(eb + 1) << 23);
+        const float r = __fdiv_rn(vlim, nl);
+        vlim = nl;
+        vmul = __uint_as_float((uint32_t)(260 - eb) << 23);
+        return r;
+    };
     float vout = 1.f;                            // output factor of the value-scale normalisation
     if constexpr (TMA && NGRP == 1) {
         // ---- 8 kv heads, one group per head: a warp takes its kv head's four tiles of a stage in
         // one pass (64 tokens: one running-maximum update and one rescale vote per stage).
         //  1. lane l converts the stage's scale/zero of tokens l and l + 32 to fp32 once:
         //     Sw[tok] = (scale_k * cscq, zero_k, scale_v * vmul, zero_v), zero for tokens outside
-        //     the range.  vmul = 128 / vlim, where vlim is a power of two above every value scale
-        //     seen so far (raised with the stage's maximum; the accumulators rescale by the ratio),
-        //     so that w = p * scale_v * vmul < 2^8 * 2^7 stays inside the f16 range of the split
-        //     PV operand whatever the scales' magnitude; vlim / 128 goes into the output.
+        //     the range (vmul from the value-scale bound, raised with the stage's maximum).
         //  2. QK MMAs of the four tiles, interleaved (four independent accumulator chains).
         //  3. logits, stage maximum, lazy rescale, P * scale_v -> per-warp P buffer (hi, lo).
         //  4. PV MMAs of the four tiles.
         constexpr int kWs4 = kTilesPerStage * 8 + 4;        // words per P-buffer column (bank spread)
         uint32_t *Wp = reinterpret_cast<uint32_t *>(smem + 128 + warp * a.ws_bytes);   // [NCOL][kWs4]
         float4 *Sw = reinterpret_cast<float4 *>(Wp + NCOL * kWs4);                    // [64] per token
-        float vlim = 0.f, vmul = 0.f;
         int st = 0, ph = 0;
         for (;; st = (st + 1 == a.stages) ? 0 : st + 1, ph ^= (st == 0)) {
             if (!mbar_wait(saddr(&bars[st]), ph)) {
@@ -1064,13 +1170,14 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
             const bool whole = mask == (1 << kTilesPerStage) - 1 && lim >= kStageTok;
 
             // 1. per-token fp32 scale/zero of kv head h
-            float vres = 1.f;
+            float vres;
             {
                 const uint16_t *s16 = reinterpret_cast<const uint16_t *>(sb + off_s) + h;
-                float4 e[2];
+                constexpr int kRows = (kStageTok + 31) / 32;   // tokens per lane
+                float4 e[kRows];
                 float vm = 0.f;
 #pragma unroll
-                for (int r = 0; r < 2; ++r) {
+                for (int r = 0; r < kRows; ++r) {
                     const int tok = lane + 32 * r;
                     const bool ok = ((mask >> (tok >> 4)) & 1) && tok < lim;
                     const int o = tok * 8;
@@ -1079,18 +1186,12 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
                               : make_float4(0.f, 0.f, 0.f, 0.f);
                     vm = fmaxf(vm, e[r].z);
                 }
+                // (value scales are >= 0, +0 for tokens outside the range: their bit patterns order as
+                // the values do, so one integer reduction gives the warp's maximum)
+                vm = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(vm)));
+                vres = raise_vlim(vm);
 #pragma unroll
-                for (int o = 16; o; o >>= 1) vm = fmaxf(vm, __shfl_xor_sync(0xffffffffu, vm, o));
-                if (vm > vlim) {                          // (warp-uniform) raise the value-scale bound
-                    // vm in [2^(eb-127), 2^(eb-126)): vlim = 2^(eb-126), vmul = 2^7 / vlim
-                    const int eb = min(max((int)((__float_as_uint(vm) >> 23) & 0xffu), 7), 252);
-                    const float nl = __uint_as_float((uint32_t)(eb + 1) << 23);
-                    vres = __fdiv_rn(vlim, nl);
-                    vlim = nl;
-                    vmul = __uint_as_float((uint32_t)(260 - eb) << 23);
-                }
-#pragma unroll
-                for (int r = 0; r < 2; ++r) {
+                for (int r = 0; r < kRows; ++r) {
                     e[r].x *= cscq;
                     e[r].z *= vmul;
                     Sw[lane + 32 * r] = e[r];
@@ -1240,7 +1341,6 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
             __syncwarp();
             if (lane == 0) mbar_arrive(saddr(&bars[4 + st]));
         }
-        vout = vlim * (1.f / 128.f);
     } else {
     int st = 0, ph = 0;                          // stage and its phase parity, stepped (no division)
     for (;; st = (st + 1 == a.stages) ? 0 : st + 1, ph ^= (st == 0)) {
@@ -1252,6 +1352,29 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
         if (t0 < 0) break;                        // the copy warp has no more tiles
         const uint8_t *sb = stage0 + st * stage_bytes;
         const int mask = masks[st];
+        {
+            // value-scale bound over this warp's tiles of the stage (valid tokens only; lane l reads
+            // token l % 16 of a tile, groups l / 16, l / 16 + 2, ...)
+            float vm = 0.f;
+            for (int j = sub; j < kTilesPerStage; j += nsub) {
+                const int tok = lane & 15;
+                if (((mask >> j) & 1) && tok < tok_hi - (t0 + j) * kTileTokens) {
+                    const uint16_t *svp = reinterpret_cast<const uint16_t *>(sb + off_s) + 2 * arr_el +
+                                          (j * kTileTokens + tok) * rs + h * NGRP;
+                    for (int jg = lane >> 4; jg < NGRP; jg += 2) vm = fmaxf(vm, bf16_to_f32(svp[jg]));
+                }
+            }
+            vm = __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(vm)));
+            const float vres = raise_vlim(vm);
+            if (vres != 1.f) {
+#pragma unroll
+                for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+                    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+                        for (int c = 0; c < 4; ++c) oacc[nt][mt][c] *= vres;
+            }
+        }
         // this warp's tiles of the stage: sub, sub + nsub, ...; taken two at a time (32 tokens)
         for (int ja = sub; ja < kTilesPerStage; ja += 2 * nsub) {
             const int jb_raw = ja + nsub;
@@ -1412,7 +1535,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
                             const float zvv = bf16_to_f32(sk[3 * arr_el + tok * rs + jg]);
                             // rows past the valid range hold arbitrary bits (NaN included): select, never multiply
                             const bool ok = tok < lim[u];
-                            w[e] = ok ? pv[u][e] * svv : 0.f;
+                            w[e] = ok ? pv[u][e] * (svv * vmul) : 0.f;
                             zadd = ok ? fmaf(pv[u][e], zvv, zadd) : zadd;
                         }
                         // tokens gid, gid + 8 are PV k-columns 2 gid, 2 gid + 1 of tile u: one word
@@ -1499,6 +1622,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
     }
     }
 
+    vout = vlim * (1.f / 128.f);
     // The next kernel in the stream may launch once every CTA's consumers are past their loop
     // (only they trigger: the copy warp finishes its loop stages ahead of them).
     pdl_trigger();
@@ -1537,8 +1661,8 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
 #pragma unroll
             for (int mt = 0; mt < 8; ++mt) {
                 const float z = zs[nt][(mt >> 1) * NGRP / 4];
-                const float f0 = kTwo24 / (float)(1 << (2 * ((2 * mt) & 3)));
-                const float f1 = kTwo24 / (float)(1 << (2 * ((2 * mt + 1) & 3)));
+                const float f0 = kTwo24 / (float)(1 << (2 * ((2 * mt) & 3))) * vout;
+                const float f1 = kTwo24 / (float)(1 << (2 * ((2 * mt + 1) & 3))) * vout;
                 outv[nt][2 * mt] = fmaf(oacc[nt][mt][0] + oacc[nt][mt][1], f0, z) * fix[nt];
                 outv[nt][2 * mt + 1] = fmaf(oacc[nt][mt][2] + oacc[nt][mt][3], f1, z) * fix[nt];
             }
@@ -1672,7 +1796,7 @@ template <int G, int NGRP>
 int mma_smem_plan(const oscar_layout_t &L, MmaArgs &a) {
     constexpr int NT = (G == 8) ? 2 : 1;
     const int Hkv = L.n_kv_heads, Hq = Hkv * G;
-    a.off_v = Hkv * 2048;
+    a.off_v = Hkv * kStageTok * 32;
     a.arr_bytes = kStageTok * Hkv * NGRP * 2;
     a.off_s = 2 * a.off_v;
     a.stage_bytes = (a.off_s + 4 * a.arr_bytes + 127) & ~127;
@@ -1691,17 +1815,17 @@ int mma_smem_plan(const oscar_layout_t &L, MmaArgs &a) {
     a.stages = stages;
     const int combine = (kCW / Hkv > 1) ? kCW * NT * 4 * (2 + kHeadDim) * 4 : 0;
     a.res_off = combine;
-    a.win_off = a.res_off + (res_acc(Hq) + Hq * kHeadDim) * 4;
-    const int tail = a.win_off + kCW * G * (2 + kHeadDim) * 4;
+    const int res_bytes = res_floats(Hq) * 4;
+    // window CTAs: their warp results, their CTA result and its receive area, from the first stage on
+    const int win_tail = kCW * G * (2 + kHeadDim) * 4 + res_bytes + recv_bytes(Hq);
+    int tail = a.res_off + res_bytes + recv_bytes(Hq);
+    if (win_tail > tail) tail = win_tail;
     const int area = stages * a.stage_bytes;             // (the window CTAs' demotion stages R here)
     a.rk_chunk = area >= 65536 ? 65536 : area >= 32768 ? 32768 : 16384;
     a.rot_off = a.stage_off + (area > tail ? area : tail);
-    // the window CTAs stage their K/V rows in what lies beyond their warp results (they use neither
-    // the stages nor the rotated-query rows): two buffers of wbuf_tok tokens (K rows, then V rows)
-    a.wbuf_off = (tail + 15) & ~15;
-    const int wfree = a.rot_off + rot_bytes - a.stage_off - a.wbuf_off;
-    a.wbuf_tok = wfree / (2 * 2 * Hkv * kHeadDim * 2);
-    if (a.wbuf_tok > 32) a.wbuf_tok = 32;
+    // the window CTAs use everything from the first stage to the end (neither the stages nor the
+    // rotated-query rows) for two row buffers; set_window() sizes them for the launch's batch
+    a.wbuf_bytes = a.rot_off + rot_bytes - a.stage_off;
     // + 1024: the kernel rounds the dynamic shared memory base up to a 1024-byte boundary
     return 1024 + a.rot_off + rot_bytes;
 }
@@ -1729,20 +1853,30 @@ bool codes_tensor_map(CUtensorMap *tm, const uint8_t *base, long long rows) {
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Window clusters per request and the window CTAs' row buffers (tokens of this cluster's kv heads
+// per buffer, at most 32).
+void set_window(const oscar_layout_t &L, int batch, MmaArgs &a) {
+    a.win_heads = L.n_kv_heads / int2_mma_window_clusters(L, batch);
+    a.wbuf_tok = a.wbuf_bytes / (2 * 2 * a.win_heads * kHeadDim * 2);
+    if (a.wbuf_tok > 32) a.wbuf_tok = 32;
+}
+
 template <int G, int NGRP>
 cudaError_t launch_mma(const oscar_layout_t &L, MmaArgs a, int batch, bool history, bool window, cudaStream_t st,
                        int *clusters) {
     const int smem = mma_smem_plan<G, NGRP>(L, a);
+    set_window(L, batch, a);
     // the carve-up's invariants: vector and bulk-copy targets 16-byte aligned, tensor-map boxes
     // 1024-byte aligned, R_K chunks inside the stage area
-    if (((a.stage_off | a.stage_bytes | a.off_v | a.off_s | a.arr_bytes | a.res_off | a.win_off | a.rot_off) & 15) ||
+    if (((a.stage_off | a.stage_bytes | a.off_v | a.off_s | a.arr_bytes | a.res_off | a.rot_off) & 15) ||
         (a.stage_off & 1023) || (a.stage_bytes & 1023 && L.n_kv_heads == 8) ||
         (a.RK && a.stages * a.stage_bytes < a.rk_chunk))
         return cudaErrorInvalidValue;
     const bool tma = L.n_kv_heads == 8;
     // the tensor-map kernel folds these for 8 kv heads
-    if (tma && (a.off_v != 8 * 2048 || a.off_s != 2 * 8 * 2048 || a.arr_bytes != kStageTok * 8 * NGRP * 2 ||
-                a.stage_bytes != ((2 * 8 * 2048 + 4 * kStageTok * 8 * NGRP * 2 + 127) & ~127)))
+    if (tma && (a.off_v != kTilesPerStage * 4096 || a.off_s != 2 * kTilesPerStage * 4096 ||
+                a.arr_bytes != kStageTok * 8 * NGRP * 2 ||
+                a.stage_bytes != ((2 * kTilesPerStage * 4096 + 4 * kStageTok * 8 * NGRP * 2 + 127) & ~127)))
         return cudaErrorInvalidValue;
     auto kern = tma ? int2_mma_kernel<G, NGRP, true> : int2_mma_kernel<G, NGRP, false>;
     CUtensorMap tmk, tmv;
@@ -1756,7 +1890,8 @@ cudaError_t launch_mma(const oscar_layout_t &L, MmaArgs a, int batch, bool histo
     a.csize = int2_cluster_size(reinterpret_cast<const void *>(kern), smem, kThreads);
     if (cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void *>(kern), smem)) return e;
     a.hist_ctas = history ? a.out.S * a.csize : 0;
-    a.win_ctas = window ? a.csize : 0;
+    a.pf_units = 0;      // (measured slower at one, a half and two rounds of units ahead: kept off)
+    a.win_ctas = window ? (L.n_kv_heads / a.win_heads) * a.csize : 0;
     if (clusters) *clusters = (a.hist_ctas + a.win_ctas) / a.csize;   // arrivals per request
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.win_ctas + a.hist_ctas, batch);
@@ -1792,6 +1927,8 @@ int int2_mma_cluster_size(const oscar_layout_t &L, int *active) {
 #undef OSCAR_CL_CASE
     return 1;
 }
+
+int int2_mma_window_clusters(const oscar_layout_t &L, int batch) { return L.n_kv_heads == 8 && batch == 1 ? 2 : 1; }
 
 bool int2_mma_supported(const oscar_layout_t &L) {
     const int H = L.n_kv_heads;

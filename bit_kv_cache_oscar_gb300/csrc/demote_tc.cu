@@ -219,6 +219,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
         int i = cta;
         bool have = wk.find(a, i, b, t, lo, hi);
         int z = have ? piece_row(b, t, lo, hi) : -1;
+        int issued = 0;                            // stage fills armed
         for (int n = 0; have; ++n) {
             int b2 = 0, t2 = 0, lo2 = 0, hi2 = 0;
             const bool have2 = wk.find(a, i + cpp, b2, t2, lo2, hi2);
@@ -228,6 +229,7 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
                 flag_status(a.status, OSCAR_DEV_WAIT_TIMEOUT);
             const unsigned valid = __ballot_sync(0xffffffffu, z >= 0);
             if (lane == 0) mbar_arrive_expect_tx(bar_full + 8 * s, (uint32_t)__popc(valid) * 2 * rpl * 128);
+            issued = n + 1;
             __syncwarp();
             if (z >= 0) {
                 const uint32_t dst = sbase + kOffA + s * kStageBytes + lane * rpl * 128;
@@ -242,6 +244,11 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
             hi = hi2;
             z = z2;
         }
+        // No copy may still be landing when the CTA leaves: the MMA warp waited for every fill, but
+        // after a wait that gave up the last fills may be outstanding; wait (bounded) for each of them.
+        for (int k = issued > kStagesTC ? issued - kStagesTC : 0; k < issued; ++k)
+            if (!mbar_wait(bar_full + 8 * (k % kStagesTC), (k / kStagesTC) & 1) && lane == 0)
+                flag_status(a.status, OSCAR_DEV_WAIT_TIMEOUT);
     } else if (warp == 1) {
         // ---------------------------------------------------------------- MMA issuer
         if (lane == 0) {

@@ -9,14 +9,15 @@
 // lives in this library instead, so the caller passes only inputs and outputs.
 //
 // The array is a file-scope __device__ variable: every GPU that loads the
-// library holds OSCAR_NOALLOC_SCRATCH_BYTES of it until the process exits.
-// Host code cannot use the variable's name as a device address, so the first
-// call on each device (with that device current) looks the address up with
-// cudaGetSymbolAddress and caches it.  All calls share the array, so calls
-// whose work overlaps on the GPU (different streams, or different host threads
-// on one stream order) race on it and must be serialised by the caller.
-
-#include <mutex>
+// library holds OSCAR_NOALLOC_SCRATCH_BYTES of it until the process exits
+// (CUDA may load the library's device code, and reserve the array, when a
+// device first uses it).  Host code cannot use the variable's name as a device
+// address, so every call looks the address up on the current device with
+// cudaGetSymbolAddress (a host-side query, no allocation once the code is
+// loaded; looking it up each time also survives a device reset).  All calls
+// share the array, so calls whose work overlaps on the GPU (different streams,
+// or different host threads on one stream order) race on it and must be
+// serialised by the caller.
 
 #include "oscar_internal.cuh"
 
@@ -26,25 +27,13 @@ constexpr size_t kScratchFloats = OSCAR_NOALLOC_SCRATCH_BYTES / sizeof(float);
 
 __device__ __align__(256) float g_noalloc_partials[kScratchFloats];
 
-constexpr int kMaxDevices = 64;
-float *g_scratch[kMaxDevices] = {nullptr};
-std::mutex g_scratch_mu;
-
-// Device address of g_noalloc_partials on the current device (looked up once per device).
+// Device address of g_noalloc_partials on the current device.
 oscar_status_t scratch_address(float **out) {
-    int dev = -1;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return oscar::set_last_error(OSCAR_ERR_CUDA, "cudaGetDevice failed");
-    if (dev < 0 || dev >= kMaxDevices) return oscar::set_last_error(OSCAR_ERR_UNSUPPORTED, "device index >= 64");
-    std::lock_guard<std::mutex> lk(g_scratch_mu);
-    if (!g_scratch[dev]) {
-        void *p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_partials);
-        if (e != cudaSuccess || !p)
-            return oscar::set_last_error(OSCAR_ERR_CUDA, "cudaGetSymbolAddress of the no-alloc scratch failed");
-        g_scratch[dev] = static_cast<float *>(p);
-    }
-    *out = g_scratch[dev];
+    void *p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_partials);
+    if (e != cudaSuccess || !p)
+        return oscar::set_last_error(OSCAR_ERR_CUDA, "cudaGetSymbolAddress of the no-alloc scratch failed");
+    *out = static_cast<float *>(p);
     return OSCAR_OK;
 }
 

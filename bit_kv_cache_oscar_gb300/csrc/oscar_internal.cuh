@@ -143,6 +143,10 @@ cudaError_t launch_int2_attention(const oscar_layout_t &L, const float *q_rot, I
 
 // Tensor-core INT2 kernel (n_kv_heads in {1, 2, 4, 8}); launch_int2_attention dispatches to it.
 bool int2_mma_supported(const oscar_layout_t &L);
+// Window clusters (the BF16 sink/recent part) per request of the tensor-core INT2 kernel: two for
+// a single request with 8 kv heads (four heads each: a window CTA's rows then fit its buffers in
+// one round trip), else one (with more requests the history clusters need the CTA slots).
+int int2_mma_window_clusters(const oscar_layout_t &L, int batch);
 // CTAs per cluster the tensor-core INT2 kernel will use for this layout (8 if no device is
 // visible); *active (optional) gets how many such clusters are resident at once (0 if unknown).
 int int2_mma_cluster_size(const oscar_layout_t &L, int *active = nullptr);

@@ -220,6 +220,28 @@ __device__ __forceinline__ float ld_dsmem_f32(uint32_t local_saddr, uint32_t ran
     return v;
 }
 
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned) from this CTA's shared
+// memory at local_src to CTA `rank` of the cluster, at the offset local_dst has in this CTA; the
+// copy completes `bytes` of transaction count on that CTA's mbarrier at the offset local_bar.
+__device__ __forceinline__ void dsmem_bulk_copy(uint32_t local_dst, uint32_t local_src, uint32_t bytes,
+                                                uint32_t local_bar, uint32_t rank) {
+    uint32_t rd, rb;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rd) : "r"(local_dst), "r"(rank));
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rb) : "r"(local_bar), "r"(rank));
+    asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(rd), "r"(local_src), "r"(bytes), "r"(rb)
+                 : "memory");
+}
+
+// Store four floats (16-byte aligned) to the shared memory of CTA `rank` of this cluster, at the
+// offset that local_saddr has in this CTA's shared memory (visible to it after a cluster barrier).
+__device__ __forceinline__ void st_dsmem_f32x4(uint32_t local_saddr, uint32_t rank, float4 v) {
+    uint32_t ra;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(ra) : "r"(local_saddr), "r"(rank));
+    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(ra), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+
 // Store a float to the shared memory of CTA `rank` of this cluster, at the offset that
 // local_saddr has in this CTA's shared memory (visible to it after a cluster barrier).
 __device__ __forceinline__ void st_dsmem_f32(uint32_t local_saddr, uint32_t rank, float v) {

@@ -144,9 +144,10 @@ OSCAR_API size_t oscar_partials_acc_floats(const oscar_layout_t *layout, int32_t
  * A split count that fills the GPU for `batch` requests whose longest history
  * spans max_hist_tokens tokens, in one wave: each split is computed by a
  * cluster of up to 8 CTAs that combine their results before writing the
- * split's partial, one more cluster per request computes the BF16 window, and
- * the count is the number of such clusters the current device keeps resident
- * at once divided by `batch`, minus that window cluster (sm_count is used when
+ * split's partial, one or two more clusters per request compute the BF16
+ * window (two for batch 1 with 8 kv heads, four heads each), and the count is the number
+ * of such clusters the current device keeps resident at once divided by
+ * `batch`, minus those window clusters (sm_count is used when
  * no device is visible); at least one 16-token history tile per split, clamped
  * to [1, 1024].
  */
@@ -253,7 +254,8 @@ OSCAR_API oscar_status_t oscar_rotate_q(const oscar_layout_t *layout, const uint
  * first + floor((s+1)·n/S)) clipped to [sink, h); the BF16 partial covers
  * [0, sink) ∪ [h, T).  When the tensor-core kernels support the layout (1, 2,
  * 4 or 8 kv heads) both parts are computed by one launch, whose first cluster
- * per request takes the BF16 window.
+ * per request (first two for batch 1 with 8 kv heads, four kv heads each) takes
+ * the BF16 window.
  */
 OSCAR_API oscar_status_t oscar_decode_attention(const oscar_layout_t *layout,
                                       const uint16_t *q, const float *q_rot,
@@ -385,15 +387,18 @@ OSCAR_API oscar_status_t oscar_bf16_decode_attention(const oscar_layout_t *layou
  * device allocation and offers no workspace, or a loop that must never call
  * an allocator).  Same inputs and outputs as oscar_decode_attention followed
  * by oscar_merge, with n_splits history splits; the partials live in a
- * library-owned device array of OSCAR_NOALLOC_SCRATCH_BYTES per device
- * (allocated statically when the library is loaded, held until exit; this
- * call allocates nothing).  Limit: 2*ceil64(batch*Hq*(n_splits+1)) +
- * batch*Hq*(n_splits+1)*head_dim floats must fit, else
- * OSCAR_ERR_INVALID_ARG.  The first call on a device looks up the array's
- * device address (make that first call before any stream capture).  All
- * calls share the array: calls whose GPU work overlaps race and must be
- * serialised by the caller.  Every slot is written before it is read, so no
- * state carries over between calls.
+ * library-owned device array of OSCAR_NOALLOC_SCRATCH_BYTES per device, part
+ * of the library's device code and held until the process exits.  This call
+ * makes no cudaMalloc/cudaFree.  CUDA may load the library's device code, and
+ * with it reserve the array, only when a device first uses it (lazy module
+ * loading): make one call on each device at initialisation, outside any loop
+ * and before any stream capture; later calls reserve nothing.  Each call looks
+ * the array's device address up again (a host-side query), so a device reset
+ * between calls leaves no stale address.  Limit:
+ * 2*ceil64(batch*Hq*(n_splits+1)) + batch*Hq*(n_splits+1)*head_dim floats
+ * must fit, else OSCAR_ERR_INVALID_ARG.  All calls share the array: calls
+ * whose GPU work overlaps race and must be serialised by the caller.  Every
+ * slot is written before it is read, so no state carries over between calls.
  */
 #define OSCAR_NOALLOC_SCRATCH_BYTES (4u << 20)
 OSCAR_API oscar_status_t oscar_decode_attention_noalloc(

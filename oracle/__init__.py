@@ -371,7 +371,8 @@ def key_logit_error_trace(Q, K, K_hat) -> float:
 
 PINS = {
     "rotate_f32": "fp64 bound + ascending-order rounding case (tests/test_oracle_codec.py)",
-    "quantize_rows": "worked rows tests/golden/quantizer_worked.json, brute-force nearest level, error bound",
+    "quantize_rows": "hand-derived worked rows (tests/test_oracle_codec.py::test_quantizer_worked_rows), "
+                     "brute-force nearest level, error bound",
     "pack_row/unpack_row": "all 256 bytes round trip, worked byte",
     "attend_head": "textbook softmax attention on exactly quantizable caches, rotation invariance",
     "partial/merge_f64": "split + merge equals direct attention; one split is the identity",

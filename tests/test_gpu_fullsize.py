@@ -43,8 +43,8 @@ def _run_like_bench(case, dynamic=True):
     return out, out32
 
 
-def _check(case, out, out32, pairs):
-    ref = sc.oracle_outputs(case, pairs)
+def _check(case, out, out32, pairs, ref=None):
+    ref = ref or sc.oracle_outputs(case, pairs)
     o32 = out32.cpu().numpy()
     ob16 = out.float().cpu().numpy()
     for (b, hq), (o_ref, _) in ref.items():
@@ -101,3 +101,23 @@ def test_fullsize_ragged_shared_prefix():
     sc.upload(case, keep_rotated=False)
     out, out32 = _run_like_bench(case)
     _check(case, out, out32, _pairs(seq, case.layout.gqa, (1, 6)))
+
+
+def test_fullsize_ragged_batch32():
+    """The batch-32 target shape at its full size: 32 requests with contexts drawn from
+    65,536..100,000, a 16,384-token prefix shared through the page tables, run as the benchmark
+    runs it (one window cluster per request, the library's split suggestion for 32 requests),
+    with fixed history splits and then with dynamic 64-token units; sampled heads of the shortest
+    and the longest request and of two more requests against the oracle."""
+    w = syn.WORKLOADS["qwen3_8b_b32_ragged"]
+    seq = tuple(int(t) for t in syn.context_lengths(w))
+    assert len(seq) == 32
+    case = sc.make_case(n_kv=w.n_kv_heads, gqa=w.n_q_heads // w.n_kv_heads, page_size=w.page_size,
+                        group=w.group, seq=seq, gen_device="cuda", shared_prefix=w.shared_prefix)
+    sc.upload(case, keep_rotated=False)
+    reqs = sorted({int(np.argmin(seq)), int(np.argmax(seq)), 5, 21})
+    pairs = [(b, hq) for b in reqs for hq in (4, 7, 25, 26)]          # kv heads 1 and 6
+    ref = sc.oracle_outputs(case, pairs)
+    for dynamic in (False, True):
+        out, out32 = _run_like_bench(case, dynamic)
+        _check(case, out, out32, pairs, ref)

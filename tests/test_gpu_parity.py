@@ -453,16 +453,22 @@ def test_fused_rotation_rejects_other_head_counts():
                                         dev["int2_table"], dev["seq_len"], dev["hist_end"], case.sm_scale, part)
 
 
-def test_bf16_full_cache_parity():
+@pytest.mark.parametrize("n_kv,gqa,ps,seq,S", [
+    (2, 4, 16, (1024, 555), 9),         # cp.async path
+    (8, 4, 64, (3000, 1700), 12),       # 8 kv heads: tensor-map boxes, one tile of every head per stage
+    (8, 8, 16, (1500,), 5),
+])
+def test_bf16_full_cache_parity(n_kv, gqa, ps, seq, S):
     """The all-BF16 comparison kernel: oracle with no history region (sink = h_end = 0)."""
-    case = sc.make_case(n_kv=2, gqa=4, page_size=16, seq=(1024, 555))
+    case = sc.make_case(n_kv=n_kv, gqa=gqa, page_size=ps, seq=seq)
     L = case.layout
     dev = sc.upload(case, demote_history=False)
-    part = ob.Partials.empty(L, 2, 9)
+    part = ob.Partials.empty(L, len(seq), S)
     ob.oscar_bf16_decode_attention(L, dev["q"], dev["stage"], dev["stage_table"], dev["seq_len"], case.sm_scale, part)
-    out32 = torch.empty((2, L.n_q_heads, D), dtype=torch.float32, device="cuda")
+    out32 = torch.empty((len(seq), L.n_q_heads, D), dtype=torch.float32, device="cuda")
     ob.oscar_merge(L, part, None, None, out32)
     torch.cuda.synchronize()
+    assert ob.oscar_get_device_status() == 0
     qb = bf16_bits(case.q)
     got, exp = [], []
     for b, T in enumerate(case.seq):
@@ -573,3 +579,33 @@ def test_dynamic_tile_scheduling(n_kv, gqa, ps, group, seq, S):
         for (b, hq), (oref, lref) in ref.items():
             ok, r, m = sc.tolerance_ok(o32[b, hq], oref)
             assert ok, ((b, hq), r, m)
+
+
+@pytest.mark.parametrize("n_kv,gqa,ps,group,vf,qf", [
+    (8, 4, 64, 128, 50.0, 1.0),       # value scales ~1e3 (P * scale_v would leave the f16 range unscaled)
+    (8, 4, 64, 128, 1e-6, 1.0),       # value scales ~1e-5 (f16 subnormals unscaled)
+    (8, 4, 64, 128, 1.0, 300.0),      # queries ~1e3: q_rot / code factor beyond the f16 range unscaled
+    (8, 8, 16, 32, 50.0, 1.0),        # groups of 32 (group-pure loop, tensor-map copies)
+    (2, 4, 16, 128, 1e-6, 300.0),     # 2 kv heads (cp.async copies)
+    (4, 2, 32, 64, 50.0, 1.0),
+])
+def test_value_and_query_scale_range(n_kv, gqa, ps, group, vf, qf):
+    """Values and queries far from the synthetic data's magnitudes: the decode kernel normalises
+    the value scales by a running power-of-two bound and the rotated queries by a power of two
+    per kv head, so its f16 split operands stay in range; outputs against the oracle (both the
+    rotate + decode + merge calls and the fused launch)."""
+    case = sc.make_case(n_kv=n_kv, gqa=gqa, page_size=ps, group=group, seq=(2000, 900))
+    case.V = [(v.float() * vf).to(torch.bfloat16) for v in case.V]
+    case.q = (case.q.float() * qf).to(torch.bfloat16)
+    sc.upload(case)
+    out, out32, lse, _ = sc.run_decode(case, 5)
+    assert ob.oscar_get_device_status() == 0
+    _check_outputs(case, out, out32, lse)
+    L, dev = case.layout, case.dev
+    part = ob.Partials.empty(L, 2, 5)
+    ob.oscar_decode_attention_fused(L, dev["q"], dev["RK"], dev["bf16"], dev["bf16_table"], dev["int2"],
+                                    dev["int2_table"], dev["seq_len"], dev["hist_end"], case.sm_scale, part)
+    ob.oscar_merge(L, part, dev["RV"], out, out32, lse)
+    torch.cuda.synchronize()
+    assert ob.oscar_get_device_status() == 0
+    _check_outputs(case, out, out32, lse)
