@@ -631,12 +631,14 @@ __device__ __forceinline__ void split2(float v0, float v1, uint32_t &hi, uint32_
     lo = *reinterpret_cast<const uint32_t *>(&l);
 }
 
-// TMA: 8 kv heads.  The copy warp moves each tile's codes with two 2-D tensor-map boxes per
-// array (16 rows x 128 bytes = 4 heads, 128-byte swizzle) and its scale/zero rows with 1-D bulk
-// copies; otherwise (1, 2 or 4 kv heads) it scatters 16-byte cp.async chunks head-major.
+// TMA: 8 kv heads.  The copy warp moves a stage's codes with 3-D tensor-map boxes of whole
+// 256-byte rows (128-byte swizzle; one box per array for a unit inside one page, else one per tile)
+// and its scale/zero rows with 1-D bulk copies; otherwise (1, 2 or 4 kv heads) it scatters
+// 16-byte cp.async chunks head-major.
 template <int G, int NGRP, bool TMA>
 __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
-    int2_mma_kernel(MmaArgs a, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv) {
+    int2_mma_kernel(MmaArgs a, const __grid_constant__ CUtensorMap tmk, const __grid_constant__ CUtensorMap tmv,
+                    const __grid_constant__ CUtensorMap tmk1, const __grid_constant__ CUtensorMap tmv1) {
     constexpr int NT = (G == 8) ? 2 : 1;      // n-tiles of 8 columns: 4 heads x {hi, lo} each
     constexpr int NCOL = 8 * NT;
     extern __shared__ __align__(128) uint8_t smem_raw[];
@@ -668,7 +670,6 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
         return;
     }
     const SplitRange r = history_split(a.sink, he, a.hist_ctas, s);   // C sub-splits per slot
-    const int n_iters = (r.tile_hi - r.tile_lo + kTilesPerStage - 1) / kTilesPerStage;
     // Dynamic scheduling: the copy warps of all of b's history CTAs take units of kTilesPerStage
     // tiles of the whole history [sink, he) from a shared counter, so that CTAs that run faster
     // (an SM to themselves) take more; each stage carries its first tile (or -1: no more).
@@ -747,6 +748,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
         };
         int nxt_t0 = -1, nxt_pg = -1;
         if (dyn) take_unit(nxt_t0, nxt_pg);
+        int fix_t0 = r.tile_lo;                                // fixed splits: the next stage's first tile
         bool ok = true;
         int armed = 0;                                         // stage fills started (expect-tx armed)
         for (int it = 0; ok; ++it) {
@@ -764,7 +766,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
                 t0 = nxt_t0;
                 unit_pg = nxt_pg;
             } else {
-                t0 = it < n_iters ? r.tile_lo + it * kTilesPerStage : -1;
+                t0 = fix_t0 < r.tile_hi ? fix_t0 : -1;
             }
             if (lane == 0) stage_tile[st] = t0;
             if (t0 < 0) {                                      // an empty stage marks the end
@@ -780,15 +782,24 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
                 }
                 break;
             }
+            // the stage takes tiles [t0, t_stop): up to the next unit boundary counted from the first
+            // history tile (a fixed split's first stage may be partial; every later one is whole)
+            const int t_stop = min(tile_hi, t0 + kTilesPerStage - ((t0 - hist_first) & (kTilesPerStage - 1)));
+            fix_t0 = t_stop;
             uint8_t *sb = stage0 + st * stage_bytes;
             int mask = 0;
             if constexpr (TMA) {
-                // lane = 8 j + op: op 0..3 the code boxes (K lo/hi heads, V lo/hi), 4..7 scale/zero rows
-                const int jl = lane >> 3, op = lane & 7;
+                // A unit whose tiles lie in one page moves with six copies, lanes 0..5: one 64-row box
+                // per code array and the unit's rows of each scale/zero array.  Otherwise tile j moves
+                // with lanes 8 j + op: op 0, 1 a 16-row box of the K, V codes, op 2..5 the tile's
+                // scale/zero rows.  (Per copy the engine pays a fixed cost: few large copies move the
+                // stage at a higher rate than a copy per tile, array and half row.)
+                const bool one_page = (t0 % tpp) + kTilesPerStage <= tpp;
+                const int jl = one_page ? 0 : lane >> 3, op = one_page ? lane : lane & 7;
                 int row0 = 0;
                 for (int j = 0; j < kTilesPerStage; ++j) {
                     const int tile = t0 + j;
-                    if (tile >= tile_hi) break;
+                    if (tile >= t_stop) break;
                     const int lp = tile / tpp;
                     if (!dyn && lp - pg_base >= 32) {
                         pg_base = lp;
@@ -803,23 +814,24 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
                     mask |= 1 << j;
                     if (j == jl) row0 = page * a.page_size + (tile * kTileTokens) % a.page_size;
                 }
+                // (one page: the whole unit lands, also the rows past the range, which the mask hides)
                 const uint32_t full = saddr(&bars[st]);
+                const int nsb = kTileTokens * 8 * NGRP * 2;          // bytes of one tile's scale/zero rows
                 if (lane == 0) {
                     masks[st] = mask;
-                    mbar_arrive_expect_tx(full, __popc(mask) * tile_bytes);
+                    mbar_arrive_expect_tx(full, one_page ? (mask ? kTilesPerStage * tile_bytes : 0) : __popc(mask) * tile_bytes);
                 }
                 __syncwarp();
-                if ((mask >> jl) & 1) {
+                if (((mask >> jl) & 1) && op < 6) {
                     const uint32_t d = saddr(sb) + jl * 4096;
-                    if (op < 4) {
-                        tma_load_2d(d + (op >> 1) * off_v + (op & 1) * 2048, (op >> 1) ? &tmv : &tmk, (op & 1) * 128,
-                                    row0, full);
+                    if (op < 2) {
+                        tma_load_3d(d + op * off_v, one_page ? (op ? &tmv : &tmk) : (op ? &tmv1 : &tmk1), 0, 0, row0, full);
                     } else {
-                        const int arr = op - 4, nsb = kTileTokens * 8 * NGRP * 2;   // bytes of one tile's rows
+                        const int arr = op - 2;
                         const uint16_t *src = arr == 0 ? a.pool.scale_k : arr == 1 ? a.pool.zero_k
                                             : arr == 2 ? a.pool.scale_v : a.pool.zero_v;
                         tma_load_1d(saddr(sb + off_s) + arr * arr_bytes + jl * nsb, src + (size_t)row0 * 8 * NGRP,
-                                    nsb, full);
+                                    one_page ? kTilesPerStage * nsb : nsb, full);
                     }
                 }
                 if (dyn) take_unit(nxt_t0, nxt_pg);
@@ -827,7 +839,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
             }
             for (int j = 0; j < kTilesPerStage; ++j) {
                 const int tile = t0 + j;
-                if (tile >= tile_hi) break;
+                if (tile >= t_stop) break;
                 const int pos0 = tile * kTileTokens;
                 const int lp = tile / tpp;
                 if (!dyn && lp - pg_base >= 32) {              // warp-uniform refill of the page window
@@ -1072,11 +1084,12 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
     {
         const int vrow[4] = {t, t + 8, t + 4, t + 12};
         if constexpr (TMA) {
-            const int hh = h & 3, ck = 2 * hh + (t >> 1), cv = 2 * hh + (gid >> 2);
-            kofs0 = gid * 128 + ((ck ^ gid) << 4) + (t & 1) * 8;
-            kofs1 = kofs0 + 8 * 128;
+            const int hh = h & 3, hf = h >> 2, ck = 2 * hh + (t >> 1), cv = 2 * hh + (gid >> 2);
+            kofs0 = gid * 256 + hf * 128 + ((ck ^ ((2 * gid + hf) & 7)) << 4) + (t & 1) * 8;
+            kofs1 = kofs0 + 8 * 256;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) vofs[i] = vrow[i] * 128 + ((cv ^ (vrow[i] & 7)) << 4) + (gid & 3) * 4;
+            for (int i = 0; i < 4; ++i)
+                vofs[i] = vrow[i] * 256 + hf * 128 + ((cv ^ ((2 * vrow[i] + hf) & 7)) << 4) + (gid & 3) * 4;
         } else {
             kofs0 = gid * 32 + 8 * t;
             kofs1 = kofs0 + 8 * 32;
@@ -1093,11 +1106,12 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
         for (int Gb = 0; Gb < 4; ++Gb) {
             const int wk = 2 * Gb + (t >> 1), wv = 2 * Gb + (gid >> 2);
             if constexpr (TMA) {
-                const int hh = h & 3;
-                kofg[Gb] = gid * 128 + (((2 * hh + (wk >> 2)) ^ gid) << 4) + (wk & 3) * 4;
+                const int hh = h & 3, hf = h >> 2;
+                kofg[Gb] = gid * 256 + hf * 128 + (((2 * hh + (wk >> 2)) ^ ((2 * gid + hf) & 7)) << 4) + (wk & 3) * 4;
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
-                    vofg[Gb][i] = vrow[i] * 128 + (((2 * hh + (wv >> 2)) ^ (vrow[i] & 7)) << 4) + (wv & 3) * 4;
+                    vofg[Gb][i] = vrow[i] * 256 + hf * 128 + (((2 * hh + (wv >> 2)) ^ ((2 * vrow[i] + hf) & 7)) << 4) +
+                                  (wv & 3) * 4;
             } else {
                 kofg[Gb] = gid * 32 + 4 * wk;
 #pragma unroll
@@ -1106,7 +1120,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
         }
     }
     auto tile_base = [&](const uint8_t *arr, int j) -> const uint8_t * {
-        return TMA ? arr + j * 4096 + (h >> 2) * 2048 : arr + h * (kStageTok * 32) + j * (kTileTokens * 32);
+        return TMA ? arr + j * 4096 : arr + h * (kStageTok * 32) + j * (kTileTokens * 32);
     };
     const float csc = cscq;                     // logit scale of the MMA dot products
     const int rs = Hkv * NGRP;                  // scale/zero elements per token row in a stage
@@ -1211,7 +1225,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
                 uint2 kw0[kTilesPerStage], kw1[kTilesPerStage];
 #pragma unroll
                 for (int u = 0; u < kTilesPerStage; ++u) {
-                    const uint8_t *Kc = sb + u * 4096 + (h >> 2) * 2048;
+                    const uint8_t *Kc = sb + u * 4096;
                     kw0[u] = *reinterpret_cast<const uint2 *>(Kc + kofs0);
                     kw1[u] = *reinterpret_cast<const uint2 *>(Kc + kofs1);
                 }
@@ -1313,7 +1327,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
             // 4. O += V_codes^T . (P * scale_v); m-tile mt row gid / gid + 8 = channel 16 gid + 2 mt / + 1
 #pragma unroll
             for (int u = 0; u < kTilesPerStage; ++u) {
-                const uint8_t *Vc = sb + off_v + u * 4096 + (h >> 2) * 2048;
+                const uint8_t *Vc = sb + off_v + u * 4096;
                 uint32_t bw[NT][2];
 #pragma unroll
                 for (int nt = 0; nt < NT; ++nt) {
@@ -1402,7 +1416,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
 #pragma unroll
                     for (int Gb = 0; Gb < 4; ++Gb) {
                         const uint32_t w0 = *reinterpret_cast<const uint32_t *>(Kc + kofg[Gb]);
-                        const uint32_t w1 = *reinterpret_cast<const uint32_t *>(Kc + kofg[Gb] + (TMA ? 8 * 128 : 8 * 32));
+                        const uint32_t w1 = *reinterpret_cast<const uint32_t *>(Kc + kofg[Gb] + (TMA ? 8 * 256 : 8 * 32));
                         const uint32_t w0b = __byte_perm(w0, 0, 0x3321), w1b = __byte_perm(w1, 0, 0x3321);
                         const uint32_t w0s = odd ? w0b : w0, w1s = odd ? w1b : w1;
                         if (Gb % kBpg == 0) {
@@ -1839,16 +1853,18 @@ int mma_cluster_size(const oscar_layout_t &L, int *active) {
     return int2_cluster_size(kern, smem, kThreads, active);
 }
 
-// An INT2 codes array of 8 kv heads, [rows = n_pages * page_size][256 bytes], as a 2-D uint8 tensor
-// map whose box is 16 rows x 128 bytes (4 heads) with 128-byte swizzle.
-bool codes_tensor_map(CUtensorMap *tm, const uint8_t *base, long long rows) {
+// An INT2 codes array of 8 kv heads, [rows = n_pages * page_size][256 bytes], as a 3-D uint8 tensor
+// map [rows][2 halves][128 bytes] whose box is box_rows rows (both halves) with 128-byte swizzle:
+// in shared memory row r's half f (4 heads) sits at r * 256 + f * 128, its 16-byte chunk c at
+// chunk c ^ ((2 r + f) & 7).
+bool codes_tensor_map(CUtensorMap *tm, const uint8_t *base, long long rows, int box_rows) {
     EncodeTiledFn fn = encode_fn();
     if (!fn || !base) return false;
-    const cuuint64_t dims[2] = {256, (cuuint64_t)rows};
-    const cuuint64_t strides[1] = {256};
-    const cuuint32_t box[2] = {128, (cuuint32_t)kTileTokens};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t *>(base), dims, strides, box, estr,
+    const cuuint64_t dims[3] = {128, 2, (cuuint64_t)rows};
+    const cuuint64_t strides[2] = {128, 256};
+    const cuuint32_t box[3] = {128, 2, (cuuint32_t)box_rows};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<uint8_t *>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -1879,12 +1895,18 @@ cudaError_t launch_mma(const oscar_layout_t &L, MmaArgs a, int batch, bool histo
                 a.stage_bytes != ((2 * kTilesPerStage * 4096 + 4 * kStageTok * 8 * NGRP * 2 + 127) & ~127)))
         return cudaErrorInvalidValue;
     auto kern = tma ? int2_mma_kernel<G, NGRP, true> : int2_mma_kernel<G, NGRP, false>;
-    CUtensorMap tmk, tmv;
+    // codes: boxes of a whole unit (64 rows) and of one tile (16 rows)
+    CUtensorMap tmk, tmv, tmk1, tmv1;
     memset(&tmk, 0, sizeof(tmk));
     memset(&tmv, 0, sizeof(tmv));
+    memset(&tmk1, 0, sizeof(tmk1));
+    memset(&tmv1, 0, sizeof(tmv1));
     if (tma && history) {
         const long long rows = (long long)a.pool.n_pages * L.page_size;
-        if (!codes_tensor_map(&tmk, a.pool.codes_k, rows) || !codes_tensor_map(&tmv, a.pool.codes_v, rows))
+        if (!codes_tensor_map(&tmk, a.pool.codes_k, rows, kStageTok) ||
+            !codes_tensor_map(&tmv, a.pool.codes_v, rows, kStageTok) ||
+            !codes_tensor_map(&tmk1, a.pool.codes_k, rows, kTileTokens) ||
+            !codes_tensor_map(&tmv1, a.pool.codes_v, rows, kTileTokens))
             return cudaErrorInvalidValue;
     }
     a.csize = int2_cluster_size(reinterpret_cast<const void *>(kern), smem, kThreads);
@@ -1906,7 +1928,7 @@ cudaError_t launch_mma(const oscar_layout_t &L, MmaArgs a, int batch, bool histo
     cfg.attrs = attr;
     cfg.numAttrs = 1;
     add_overlap_attr(cfg, attr);
-    return cudaLaunchKernelEx(&cfg, kern, a, tmk, tmv);
+    return cudaLaunchKernelEx(&cfg, kern, a, tmk, tmv, tmk1, tmv1);
 }
 
 }  // namespace
