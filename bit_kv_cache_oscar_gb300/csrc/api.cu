@@ -166,10 +166,13 @@ int32_t oscar_suggest_splits(const oscar_layout_t *L, int32_t batch, int32_t max
     int active = 0;
     if (oscar::int2_mma_supported(*L)) {
         // one split = a cluster of C CTAs (all kv heads each): as many splits as clusters fit at once
-        // (one or two more clusters per request take the BF16 window)
+        // (one or two more clusters per request take the BF16 window).  When the batch's clusters
+        // cannot run in one wave anyway, about four waves of clusters: the requests' lengths may
+        // differ, and small clusters queued behind the first wave even out the SMs' finishing times.
         const int c = oscar::int2_mma_cluster_size(*L, &active);
         if (active <= 0) active = (2 * sm_count) / c;
-        want = active / batch - oscar::int2_mma_window_clusters(*L, batch);
+        const int win = oscar::int2_mma_window_clusters(*L, batch);
+        want = (long)batch * (1 + win) > active ? (4L * active) / batch - win : active / batch - win;
     } else {
         // one CTA per (split, kv head): about two resident CTAs per SM
         want = (2L * sm_count + (long)batch * L->n_kv_heads - 1) / ((long)batch * L->n_kv_heads);

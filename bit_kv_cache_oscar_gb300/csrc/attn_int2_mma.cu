@@ -614,6 +614,10 @@ __device__ __forceinline__ void arrive_count(const MmaArgs &a, int b) {
 }
 
 constexpr float kLazy = 8.0f;   // log2 headroom before the running maximum is raised
+// The running maximum before any finite logit: far below every logit, so that 2^(logit - it) and
+// 2^(it - first maximum) underflow to 0 and the first finite maximum always raises it (no test for
+// "no maximum yet" per token); masked tokens (-inf) still give 0.
+constexpr float kNoMax = -0x1p100f;
 // rotated-query rows in shared memory: element d of a row at d + 4 (d / 32) (row stride 144), so
 // that the operand reads of a warp (4 heads x 4 column groups) spread over the banks and every
 // run of 4 columns stays 16-byte aligned (the cluster's CTAs push the rows 4 columns at a time)
@@ -1078,25 +1082,22 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
         }
     }
     // Byte offsets of this thread's code words inside a tile (rows gid / gid+8 for K; rows t,
-    // t+8, t+4, t+12 for V), and the tile base of head h.  TMA tiles are [2 halves][16 rows][128 B]
-    // with 16-byte chunk c of row r stored at chunk c ^ (r & 7); cp.async tiles are [head][row][32 B].
-    int kofs0, kofs1, vofs[4];
-    {
-        const int vrow[4] = {t, t + 8, t + 4, t + 12};
-        if constexpr (TMA) {
-            const int hh = h & 3, hf = h >> 2, ck = 2 * hh + (t >> 1), cv = 2 * hh + (gid >> 2);
-            kofs0 = gid * 256 + hf * 128 + ((ck ^ ((2 * gid + hf) & 7)) << 4) + (t & 1) * 8;
-            kofs1 = kofs0 + 8 * 256;
-#pragma unroll
-            for (int i = 0; i < 4; ++i)
-                vofs[i] = vrow[i] * 256 + hf * 128 + ((cv ^ ((2 * vrow[i] + hf) & 7)) << 4) + (gid & 3) * 4;
-        } else {
-            kofs0 = gid * 32 + 8 * t;
-            kofs1 = kofs0 + 8 * 32;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) vofs[i] = vrow[i] * 32 + 4 * gid;
-        }
+    // t+8, t+4, t+12 for V), and the tile base of head h.  TMA tiles are [16 rows][2 halves][128 B]
+    // with 16-byte chunk c of row r, half f stored at chunk c ^ ((2 r + f) & 7); cp.async tiles are
+    // [head][row][32 B].  Rows 8 or 4 apart share the swizzle: kofs1 and the V rows are kofs0 and
+    // vofs0 plus constants (kVrow rows of kRowB bytes).
+    constexpr int kRowB = TMA ? 256 : 32;
+    constexpr int kVrow[4] = {0, 8, 4, 12};
+    int kofs0, kofs1, vofs0;
+    if constexpr (TMA) {
+        const int hh = h & 3, hf = h >> 2, ck = 2 * hh + (t >> 1), cv = 2 * hh + (gid >> 2);
+        kofs0 = gid * 256 + hf * 128 + ((ck ^ ((2 * gid + hf) & 7)) << 4) + (t & 1) * 8;
+        vofs0 = t * 256 + hf * 128 + ((cv ^ ((2 * t + hf) & 7)) << 4) + (gid & 3) * 4;
+    } else {
+        kofs0 = gid * 32 + 8 * t;
+        vofs0 = t * 32 + 4 * gid;
     }
+    kofs1 = kofs0 + 8 * kRowB;
     // group-pure mapping (NGRP > 1): word 2 Gb + (t >> 1) of K rows gid, gid + 8 and word
     // 2 Gb + (gid >> 2) of V rows t, t + 8, t + 4, t + 12, for 32-channel blocks Gb = 0..3
     int kofg[4], vofg[4][4];
@@ -1131,7 +1132,8 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
     float oacc[NT][8][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-        m_run[nt] = m_true[nt] = -INFINITY;
+        m_run[nt] = kNoMax;
+        m_true[nt] = -INFINITY;
         l_run[nt] = 0.f;
 #pragma unroll
         for (int jg = 0; jg < NGRP; ++jg) zs[nt][jg] = 0.f;
@@ -1281,7 +1283,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
                 m_true[nt] = fmaxf(m_true[nt], mx);
                 float mn = m_run[nt], al = 1.f;
-                if (mx > mn + kLazy) {                    // also the first finite maximum (mn = -inf)
+                if (mx > mn + kLazy) {                    // also the first finite maximum (mn = kNoMax)
                     al = ex2_approx(mn - mx);
                     mn = mx;
                 }
@@ -1294,7 +1296,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
                     float w[2];
 #pragma unroll
                     for (int e = 0; e < 2; ++e) {
-                        const float pv = mn != -INFINITY ? ex2_approx(tv[u][e] - mn) : 0.f;
+                        const float pv = ex2_approx(tv[u][e] - mn);
                         const float2 vz = *reinterpret_cast<const float2 *>(reinterpret_cast<const float *>(Sw + 16 * u + gid + 8 * e) + 2);
                         ls += pv;
                         w[e] = pv * vz.x;
@@ -1336,10 +1338,10 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
                     bw[nt][1] = col[t + 4];
                 }
                 // k-columns 2t, 2t+1 <- tokens t, t+8; 2t+8, 2t+9 <- tokens t+4, t+12
-                const uint32_t X = *reinterpret_cast<const uint32_t *>(Vc + vofs[0]);
-                const uint32_t Y = *reinterpret_cast<const uint32_t *>(Vc + vofs[1]);
-                const uint32_t X2 = *reinterpret_cast<const uint32_t *>(Vc + vofs[2]);
-                const uint32_t Y2 = *reinterpret_cast<const uint32_t *>(Vc + vofs[3]);
+                const uint32_t X = *reinterpret_cast<const uint32_t *>(Vc + vofs0 + kVrow[0] * kRowB);
+                const uint32_t Y = *reinterpret_cast<const uint32_t *>(Vc + vofs0 + kVrow[1] * kRowB);
+                const uint32_t X2 = *reinterpret_cast<const uint32_t *>(Vc + vofs0 + kVrow[2] * kRowB);
+                const uint32_t Y2 = *reinterpret_cast<const uint32_t *>(Vc + vofs0 + kVrow[3] * kRowB);
                 const uint32_t P1 = __byte_perm(X, Y, 0x5410), P2 = __byte_perm(X, Y, 0x6521);
                 const uint32_t P3 = __byte_perm(X, Y, 0x7632), P4 = __byte_perm(X, Y, 0x7733);
                 const uint32_t Q1 = __byte_perm(X2, Y2, 0x5410), Q2 = __byte_perm(X2, Y2, 0x6521);
@@ -1518,17 +1520,15 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
                 mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
                 m_true[nt] = fmaxf(m_true[nt], mx);
                 float mn = m_run[nt], al = 1.f;
-                if (mx > mn + kLazy) {                 // also the first finite maximum (mn = -inf)
+                if (mx > mn + kLazy) {                 // also the first finite maximum (mn = kNoMax)
                     al = ex2_approx(mn - mx);
                     mn = mx;
                 }
-                float pv[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
-                if (mn != -INFINITY) {
+                float pv[2][2];
 #pragma unroll
-                    for (int u = 0; u < 2; ++u)
+                for (int u = 0; u < 2; ++u)
 #pragma unroll
-                        for (int e = 0; e < 2; ++e) pv[u][e] = ex2_approx(tv[u][e] - mn);
-                }
+                    for (int e = 0; e < 2; ++e) pv[u][e] = ex2_approx(tv[u][e] - mn);
                 alpha[nt] = al;
                 m_run[nt] = mn;
                 l_run[nt] = fmaf(l_run[nt], al, (pv[0][0] + pv[0][1]) + (pv[1][0] + pv[1][1]));
@@ -1592,10 +1592,10 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
                     }
                 if constexpr (NGRP == 1) {
                     // k-columns 2t, 2t+1 <- tokens t, t+8; 2t+8, 2t+9 <- tokens t+4, t+12
-                    const uint32_t X = *reinterpret_cast<const uint32_t *>(Vc + vofs[0]);
-                    const uint32_t Y = *reinterpret_cast<const uint32_t *>(Vc + vofs[1]);
-                    const uint32_t X2 = *reinterpret_cast<const uint32_t *>(Vc + vofs[2]);
-                    const uint32_t Y2 = *reinterpret_cast<const uint32_t *>(Vc + vofs[3]);
+                    const uint32_t X = *reinterpret_cast<const uint32_t *>(Vc + vofs0 + kVrow[0] * kRowB);
+                    const uint32_t Y = *reinterpret_cast<const uint32_t *>(Vc + vofs0 + kVrow[1] * kRowB);
+                    const uint32_t X2 = *reinterpret_cast<const uint32_t *>(Vc + vofs0 + kVrow[2] * kRowB);
+                    const uint32_t Y2 = *reinterpret_cast<const uint32_t *>(Vc + vofs0 + kVrow[3] * kRowB);
                     const uint32_t P1 = __byte_perm(X, Y, 0x5410), P2 = __byte_perm(X, Y, 0x6521);
                     const uint32_t P3 = __byte_perm(X, Y, 0x7632), P4 = __byte_perm(X, Y, 0x7733);
                     const uint32_t Q1 = __byte_perm(X2, Y2, 0x5410), Q2 = __byte_perm(X2, Y2, 0x6521);

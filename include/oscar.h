@@ -142,14 +142,15 @@ OSCAR_API size_t oscar_partials_acc_floats(const oscar_layout_t *layout, int32_t
 
 /*
  * A split count that fills the GPU for `batch` requests whose longest history
- * spans max_hist_tokens tokens, in one wave: each split is computed by a
- * cluster of up to 8 CTAs that combine their results before writing the
- * split's partial, one or two more clusters per request compute the BF16
- * window (two for batch 1 with 8 kv heads, four heads each), and the count is the number
- * of such clusters the current device keeps resident at once divided by
- * `batch`, minus those window clusters (sm_count is used when
- * no device is visible); at least one 16-token history tile per split, clamped
- * to [1, 1024].
+ * spans max_hist_tokens tokens: each split is computed by a cluster of up to 8
+ * CTAs that combine their results before writing the split's partial, one or
+ * two more clusters per request compute the BF16 window (two for batch 1 with
+ * 8 kv heads, four heads each).  With A the number of such clusters the current
+ * device keeps resident at once (from sm_count when no device is visible) and
+ * W the window clusters per request, the count is A / batch - W (one wave)
+ * when batch·(1 + W) <= A, else 4·A / batch - W (about four waves, so that
+ * requests of different lengths finish evenly); at least one 16-token history
+ * tile per split, clamped to [1, 1024].
  */
 OSCAR_API int32_t oscar_suggest_splits(const oscar_layout_t *layout, int32_t batch, int32_t max_hist_tokens,
                              int32_t sm_count);

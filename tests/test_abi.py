@@ -41,6 +41,12 @@ def test_sizes_and_split_suggestion(lib):
     s = ob.oscar_suggest_splits(L, 1, 99680, 152)
     assert 1 <= s <= 1024
     assert ob.oscar_suggest_splits(L, 1, 100, 152) >= 1
+    # the documented rule: A resident clusters, W = 2 window clusters at batch 1 and 1 above it;
+    # one wave while batch * (1 + W) <= A, else about four waves
+    A = s + 2
+    for b in (2, 4, 8, 16, 20, 32, 64):
+        want = A // b - 1 if 2 * b <= A else 4 * A // b - 1
+        assert ob.oscar_suggest_splits(L, b, 99680, 152) == max(1, want), b
     assert ob.oscar_version() == "0.1.0"
 
 
