@@ -67,10 +67,13 @@ def lib():
         L.ora_pack_row.argtypes = [P, i, P]
         L.ora_unpack_row.argtypes = [P, i, P]
         L.ora_dequant_row.argtypes = [P, P, P, i, i, P]
+        L.ora_dequant_row_cb.argtypes = [P, P, P, i, i, P, P]
+        L.ora_quantize_row_cb.argtypes = [P, i, i, f, P, P, P, P]
         L.ora_demote_rows.argtypes = [P, P, i, i, i, f, P, P, P, P]
-        L.ora_quantize_rows.argtypes = [P, i, i, i, f, P, P, P]
-        L.ora_attend_head_f64.argtypes = [i, i, i, i, i, d] + [P] * 11 + [P, P]
-        L.ora_partial_f64.argtypes = [i, i, i, i, i, d] + [P] * 10 + [i, P, P, P, P, P]
+        L.ora_demote_rows_cb.argtypes = [P, P, i, i, i, f, P, P, P, P, P]
+        L.ora_quantize_rows.argtypes = [P, i, i, i, f, P, P, P, P]
+        L.ora_attend_head_f64.argtypes = [i, i, i, i, i, d] + [P] * 13 + [P, P]
+        L.ora_partial_f64.argtypes = [i, i, i, i, i, d] + [P] * 12 + [i, P, P, P, P, P]
         L.ora_merge_f64.argtypes = [i, i, P, P, P, P, P, P]
         L.ora_exp2f.argtypes = [f]
         L.ora_exp2f.restype = f
@@ -137,15 +140,26 @@ def rotate_f64(x_bf16: np.ndarray, R: np.ndarray) -> np.ndarray:
 
 # ------------------------------------------------------------- quantizer ----
 
-def quantize_rows(x_rot: np.ndarray, group: int, clip: float):
-    """Codec on fp32 rotated rows [..., D] -> (packed uint8 [..., D/4], zero, scale bf16 [..., D/g])."""
+def _levels(levels):
+    """A codebook as fp32 [4] (None: the uniform levels 0, 1, 2, 3)."""
+    if levels is None:
+        return None
+    lv = _c(levels, np.float32).reshape(-1)
+    assert lv.shape == (4,) and np.all(np.isfinite(lv)) and np.all(np.diff(lv) > 0), lv
+    return lv
+
+
+def quantize_rows(x_rot: np.ndarray, group: int, clip: float, levels=None):
+    """Codec on fp32 rotated rows [..., D] -> (packed uint8 [..., D/4], zero, scale bf16 [..., D/g]);
+    levels: a 4-level codebook on the normalised axis (ora_quantize_row_cb), None = uniform."""
     x = _c(x_rot, np.float32)
     D = x.shape[-1]
     n = x.size // D
     packed = np.empty(x.shape[:-1] + (D // 4,), dtype=np.uint8)
     zero = np.empty(x.shape[:-1] + (D // group,), dtype=np.uint16)
     scale = np.empty_like(zero)
-    lib().ora_quantize_rows(_p(x), n, D, group, float(np.float32(clip)), _p(packed), _p(zero), _p(scale))
+    lv = _levels(levels)
+    lib().ora_quantize_rows(_p(x), n, D, group, float(np.float32(clip)), _p(lv), _p(packed), _p(zero), _p(scale))
     return packed, zero, scale
 
 
@@ -174,15 +188,15 @@ def unpack_row(packed: np.ndarray, D: int) -> np.ndarray:
     return out
 
 
-def dequant_row(packed, zero, scale, D: int, group: int) -> np.ndarray:
+def dequant_row(packed, zero, scale, D: int, group: int, levels=None) -> np.ndarray:
     out = np.empty(D, dtype=np.float64)
-    lib().ora_dequant_row(_p(_c(packed, np.uint8)), _p(_c(zero, np.uint16)),
-                          _p(_c(scale, np.uint16)), D, group, _p(out))
+    lib().ora_dequant_row_cb(_p(_c(packed, np.uint8)), _p(_c(zero, np.uint16)),
+                             _p(_c(scale, np.uint16)), D, group, _p(_levels(levels)), _p(out))
     return out
 
 
-def demote_rows(x_bf16: np.ndarray, R: np.ndarray, group: int, clip: float):
-    """Rotate (fp32 chain) + quantize + pack rows [n, D] sharing one R.
+def demote_rows(x_bf16: np.ndarray, R: np.ndarray, group: int, clip: float, levels=None):
+    """Rotate (fp32 chain) + quantize + pack rows [n, D] sharing one R (levels: a codebook, None = uniform).
 
     Returns (rotated fp32 [n, D], packed [n, D/4], zero [n, D/g], scale [n, D/g]).
     """
@@ -193,8 +207,8 @@ def demote_rows(x_bf16: np.ndarray, R: np.ndarray, group: int, clip: float):
     packed = np.empty((n, D // 4), dtype=np.uint8)
     zero = np.empty((n, D // group), dtype=np.uint16)
     scale = np.empty_like(zero)
-    lib().ora_demote_rows(_p(x), _p(R), n, D, group, float(np.float32(clip)),
-                          _p(rot), _p(packed), _p(zero), _p(scale))
+    lib().ora_demote_rows_cb(_p(x), _p(R), n, D, group, float(np.float32(clip)), _p(_levels(levels)),
+                             _p(rot), _p(packed), _p(zero), _p(scale))
     return rot, packed, zero, scale
 
 
@@ -205,10 +219,10 @@ class HeadCache:
 
     k, v: bf16 bits [T, D] (meaningful at BF16 positions); ck, cv: packed
     codes [T, D/4]; zk, sk, zv, sv: bf16 bits [T, D/g] (meaningful at history
-    positions [sink, h_end)).
+    positions [sink, h_end)); levels_k / levels_v: the codebooks the codes index (None = uniform).
     """
 
-    def __init__(self, k, v, ck, cv, zk, sk, zv, sv, sink, h_end, group):
+    def __init__(self, k, v, ck, cv, zk, sk, zv, sv, sink, h_end, group, levels_k=None, levels_v=None):
         self.k = _c(k, np.uint16)
         self.v = _c(v, np.uint16)
         self.ck = _c(ck, np.uint8)
@@ -219,10 +233,11 @@ class HeadCache:
         self.sv = _c(sv, np.uint16)
         self.T, self.D = self.k.shape
         self.sink, self.h_end, self.group = int(sink), int(h_end), int(group)
+        self.lk, self.lv = _levels(levels_k), _levels(levels_v)
 
     def _args(self):
         return [_p(self.k), _p(self.v), _p(self.ck), _p(self.cv),
-                _p(self.zk), _p(self.sk), _p(self.zv), _p(self.sv)]
+                _p(self.zk), _p(self.sk), _p(self.zv), _p(self.sv), _p(self.lk), _p(self.lv)]
 
 
 def attend_head(q_bf16, RK, RV, cache: HeadCache, sm_scale: float):
@@ -369,6 +384,54 @@ def key_logit_error_trace(Q, K, K_hat) -> float:
     return float(np.trace(dK @ (Q.T @ Q) @ dK.T))
 
 
+# ------------------------------------------------ Lloyd-Max codebook (fp64) ----
+
+def lloyd_max(samples, n_levels: int = 4, iters: int = 1000, tol: float = 1e-13):
+    """Lloyd's algorithm (Lloyd 1957; Max 1960) for the n-level scalar quantizer of least mean
+    squared error on an empirical distribution: starting from the sample quantiles at
+    (k + 1/2)/n, alternately put each threshold at the midpoint of its two levels and each level at
+    the mean of the samples of its cell (a value on a threshold belongs to the upper cell, as in
+    the quantizer; a cell that empties keeps its level), until no level moves by more than tol.
+    Returns (levels [n], thresholds [n - 1]) in fp64.  The codebook's use: OSCAR news article,
+    closing paragraph (the latest codebase's Lloyd-Max codebook); the pages give no levels."""
+    x = np.sort(np.asarray(samples, dtype=np.float64).reshape(-1))
+    assert x.size >= n_levels and np.all(np.isfinite(x))
+    lv = np.quantile(x, (np.arange(n_levels) + 0.5) / n_levels)
+    cs = np.concatenate([[0.0], np.cumsum(x)])
+    for _ in range(iters):
+        t = 0.5 * (lv[:-1] + lv[1:])
+        cut = np.concatenate([[0], np.searchsorted(x, t, side="left"), [x.size]])
+        new = lv.copy()
+        for k in range(n_levels):
+            a, b = cut[k], cut[k + 1]
+            if b > a:
+                new[k] = (cs[b] - cs[a]) / (b - a)
+        moved = np.max(np.abs(new - lv))
+        lv = new
+        if moved <= tol:
+            break
+    return lv, 0.5 * (lv[:-1] + lv[1:])
+
+
+def normalised_gaussian_groups(n_groups: int, group: int, clip: float, seed: int) -> np.ndarray:
+    """Design sample of the codebook: u = (y - lo) / ((hi - lo) / 3) for groups of `group`
+    standard normal values y with lo = clip * min, hi = clip * max, i.e. the uniform quantizer's
+    per-group normalisation (in fp64, without its bf16 rounding).  The rotated coordinates are
+    modelled as Gaussian within a group (the rotation mixes every channel into each)."""
+    rng = np.random.default_rng(seed)
+    y = rng.standard_normal((n_groups, group))
+    lo = clip * y.min(axis=1, keepdims=True)
+    hi = clip * y.max(axis=1, keepdims=True)
+    return ((y - lo) / ((hi - lo) / 3.0)).reshape(-1)
+
+
+def lloyd_max_codebook(clip: float, group: int = 128, n_groups: int = 8192, seed: int = 0) -> np.ndarray:
+    """The 4-level codebook (fp32, increasing) on the normalised axis for a clip ratio: Lloyd's
+    algorithm on normalised_gaussian_groups.  Passed to the library as the layout's levels."""
+    lv, _ = lloyd_max(normalised_gaussian_groups(n_groups, group, clip, seed))
+    return lv.astype(np.float32)
+
+
 PINS = {
     "rotate_f32": "fp64 bound + ascending-order rounding case (tests/test_oracle_codec.py)",
     "quantize_rows": "hand-derived worked rows (tests/test_oracle_codec.py::test_quantizer_worked_rows), "
@@ -381,4 +444,10 @@ PINS = {
     "bits_per_element": "page values 2.28 / 2.38 bits and 0.24% BF16 share (tests/golden/pages_numbers.json)",
     "score_weighted_value_covariance": "the value rotation built from it lowers the attention-weighted value "
                                        "error below H·P_br alone on synthetic data (tests/test_oracle_quality.py)",
+    "lloyd_max": "unit Gaussian levels against the continuous Lloyd-Max fixed point (scipy normal "
+                 "integrals) and Max's published 4-level table; centroid and midpoint conditions "
+                 "(tests/test_oracle_codebook.py)",
+    "quantize_rows/demote_rows/dequant_row with levels": "brute-force nearest level, uniform levels "
+                 "reproduce the uniform quantizer off ties, lower error than uniform on fresh Gaussian groups",
+    "attend_head with codebooks": "textbook softmax attention over the dequantised rows",
 }

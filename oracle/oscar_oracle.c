@@ -149,6 +149,54 @@ void ora_unpack_row(const uint8_t *packed, int D, uint8_t *codes) {
         codes[i] = (uint8_t)((packed[i / 4] >> (2 * (i % 4))) & 3u);
 }
 
+/*
+ * Non-uniform 4-level codebook (OSCAR news article, closing paragraph: the latest codebase
+ * brings a Lloyd-Max codebook to the attention-aware rotation).  The pages give no levels and
+ * no formula; the reading taken here keeps the uniform quantizer's per-group normalisation
+ * (zero = bf16(c*min), scale = bf16((c*max - c*min)/3), so u = (x - zero)/scale puts the
+ * clipped range on [0, 3]) and replaces the levels 0, 1, 2, 3 of that axis by a codebook
+ * lv[0] < lv[1] < lv[2] < lv[3] designed offline by Lloyd's algorithm (oracle/__init__.py,
+ * lloyd_max).  A value takes the nearest level: with the fp32 midpoints
+ * t_k = (lv[k] + lv[k+1]) * 0.5, code = [u >= t_0] + [u >= t_1] + [u >= t_2] (a value on a
+ * midpoint takes the upper level; NaN, or scale 0, gives code 0), and it is restored as
+ * zero + lv[code] * scale.  lv == NULL selects the uniform quantizer above.
+ */
+void ora_quantize_row_cb(const float *xr, int D, int g, float clip, const float *lv,
+                         uint8_t *codes, uint16_t *zero_out, uint16_t *scale_out) {
+    if (!lv) {
+        ora_quantize_row(xr, D, g, clip, codes, zero_out, scale_out);
+        return;
+    }
+    float t[3];
+    for (int k = 0; k < 3; ++k) t[k] = (lv[k] + lv[k + 1]) * 0.5f;
+    for (int g0 = 0; g0 < D; g0 += g) {
+        float mn = xr[g0], mx = xr[g0];
+        for (int i = g0 + 1; i < g0 + g; ++i) {
+            if (xr[i] < mn) mn = xr[i];
+            if (xr[i] > mx) mx = xr[i];
+        }
+        mn = mn + 0.0f;
+        mx = mx + 0.0f;
+        float lo = clip * mn;
+        float hi = clip * mx;
+        float step = (hi - lo) / 3.0f;
+        uint16_t zb = ora_f32_to_bf16(lo);
+        uint16_t sb = ora_f32_to_bf16(step);
+        zero_out[g0 / g] = zb;
+        scale_out[g0 / g] = sb;
+        float z = bf16_to_f32(zb);
+        float s = bf16_to_f32(sb);
+        for (int i = g0; i < g0 + g; ++i) {
+            int c = 0;
+            if (s != 0.0f) {
+                float u = (xr[i] - z) / s;
+                c = (u >= t[0]) + (u >= t[1]) + (u >= t[2]);
+            }
+            codes[i] = (uint8_t)c;
+        }
+    }
+}
+
 /* x_hat_i = zero + code_i * scale, in fp64 ("scale/zero point 还原"). */
 void ora_dequant_row(const uint8_t *packed, const uint16_t *zero, const uint16_t *scale,
                      int D, int g, double *out) {
@@ -158,31 +206,53 @@ void ora_dequant_row(const uint8_t *packed, const uint16_t *zero, const uint16_t
     }
 }
 
+/* The same with a codebook: x_hat_i = zero + lv[code_i] * scale in fp64 (lv NULL: uniform). */
+void ora_dequant_row_cb(const uint8_t *packed, const uint16_t *zero, const uint16_t *scale,
+                        int D, int g, const float *lv, double *out) {
+    if (!lv) {
+        ora_dequant_row(packed, zero, scale, D, g, out);
+        return;
+    }
+    for (int i = 0; i < D; ++i) {
+        int c = (packed[i / 4] >> (2 * (i % 4))) & 3;
+        out[i] = ora_bf16_to_f64(zero[i / g]) + (double)lv[c] * ora_bf16_to_f64(scale[i / g]);
+    }
+}
+
 /*
  * Demotion of n rows that share one rotation: rotate (fp32, as above), then
  * clip/quantize/pack.  rot_out may be NULL.
  */
+void ora_demote_rows_cb(const uint16_t *x, const float *R, int n, int D, int g, float clip, const float *lv,
+                        float *rot_out, uint8_t *packed, uint16_t *zero, uint16_t *scale);
+
 void ora_demote_rows(const uint16_t *x, const float *R, int n, int D, int g, float clip,
                      float *rot_out, uint8_t *packed, uint16_t *zero, uint16_t *scale) {
+    ora_demote_rows_cb(x, R, n, D, g, clip, NULL, rot_out, packed, zero, scale);
+}
+
+/* ora_demote_rows with a codebook (lv NULL: uniform). */
+void ora_demote_rows_cb(const uint16_t *x, const float *R, int n, int D, int g, float clip, const float *lv,
+                        float *rot_out, uint8_t *packed, uint16_t *zero, uint16_t *scale) {
     float *y = (float *)malloc(sizeof(float) * (size_t)D);
     uint8_t *c = (uint8_t *)malloc((size_t)D);
     for (int r = 0; r < n; ++r) {
         ora_rotate_f32(x + (size_t)r * D, R, D, y);
         if (rot_out) memcpy(rot_out + (size_t)r * D, y, sizeof(float) * (size_t)D);
-        ora_quantize_row(y, D, g, clip, c, zero + (size_t)r * (D / g), scale + (size_t)r * (D / g));
+        ora_quantize_row_cb(y, D, g, clip, lv, c, zero + (size_t)r * (D / g), scale + (size_t)r * (D / g));
         ora_pack_row(c, D, packed + (size_t)r * (D / 4));
     }
     free(y);
     free(c);
 }
 
-/* Quantize n fp32 rows that are already rotated (the codec alone). */
-void ora_quantize_rows(const float *xr, int n, int D, int g, float clip,
+/* Quantize n fp32 rows that are already rotated (the codec alone; lv NULL: uniform). */
+void ora_quantize_rows(const float *xr, int n, int D, int g, float clip, const float *lv,
                        uint8_t *packed, uint16_t *zero, uint16_t *scale) {
     uint8_t *c = (uint8_t *)malloc((size_t)D);
     for (int r = 0; r < n; ++r) {
-        ora_quantize_row(xr + (size_t)r * D, D, g, clip, c,
-                         zero + (size_t)r * (D / g), scale + (size_t)r * (D / g));
+        ora_quantize_row_cb(xr + (size_t)r * D, D, g, clip, lv, c,
+                            zero + (size_t)r * (D / g), scale + (size_t)r * (D / g));
         ora_pack_row(c, D, packed + (size_t)r * (D / 4));
     }
     free(c);
@@ -203,6 +273,7 @@ typedef struct {
     const uint16_t *k, *v;
     const uint8_t *ck, *cv;
     const uint16_t *zk, *sk, *zv, *sv;
+    const float *lk, *lv;             /* key / value codebooks, NULL: uniform */
 } ora_cache_t;
 
 static int is_history(const ora_cache_t *c, int p) { return p >= c->sink && p < c->h_end; }
@@ -211,8 +282,8 @@ static int is_history(const ora_cache_t *c, int p) { return p >= c->sink && p < 
 static double logit_at(const ora_cache_t *c, int p, const double *q, const double *q_rot, double *tmp) {
     double s = 0.0;
     if (is_history(c, p)) {
-        ora_dequant_row(c->ck + (size_t)p * (c->D / 4), c->zk + (size_t)p * (c->D / c->g),
-                        c->sk + (size_t)p * (c->D / c->g), c->D, c->g, tmp);
+        ora_dequant_row_cb(c->ck + (size_t)p * (c->D / 4), c->zk + (size_t)p * (c->D / c->g),
+                           c->sk + (size_t)p * (c->D / c->g), c->D, c->g, c->lk, tmp);
         for (int d = 0; d < c->D; ++d) s += q_rot[d] * tmp[d];
     } else {
         for (int d = 0; d < c->D; ++d) s += q[d] * ora_bf16_to_f64(c->k[(size_t)p * c->D + d]);
@@ -222,8 +293,8 @@ static double logit_at(const ora_cache_t *c, int p, const double *q, const doubl
 
 static void value_at(const ora_cache_t *c, int p, double *out) {
     if (is_history(c, p)) {
-        ora_dequant_row(c->cv + (size_t)p * (c->D / 4), c->zv + (size_t)p * (c->D / c->g),
-                        c->sv + (size_t)p * (c->D / c->g), c->D, c->g, out);
+        ora_dequant_row_cb(c->cv + (size_t)p * (c->D / 4), c->zv + (size_t)p * (c->D / c->g),
+                           c->sv + (size_t)p * (c->D / c->g), c->D, c->g, c->lv, out);
     } else {
         for (int d = 0; d < c->D; ++d) out[d] = ora_bf16_to_f64(c->v[(size_t)p * c->D + d]);
     }
@@ -243,9 +314,9 @@ void ora_attend_head_f64(int D, int T, int sink, int h_end, int g, double sm_sca
                          const uint16_t *k, const uint16_t *v,
                          const uint8_t *ck, const uint8_t *cv,
                          const uint16_t *zk, const uint16_t *sk,
-                         const uint16_t *zv, const uint16_t *sv,
+                         const uint16_t *zv, const uint16_t *sv, const float *lk, const float *lv,
                          double *out, double *lse) {
-    ora_cache_t c = {D, T, sink, h_end, g, k, v, ck, cv, zk, sk, zv, sv};
+    ora_cache_t c = {D, T, sink, h_end, g, k, v, ck, cv, zk, sk, zv, sv, lk, lv};
     double *qd = (double *)malloc(sizeof(double) * D);
     double *qr = (double *)malloc(sizeof(double) * D);
     double *tmp = (double *)malloc(sizeof(double) * D);
@@ -293,10 +364,10 @@ void ora_partial_f64(int D, int T, int sink, int h_end, int g, double sm_scale,
                      const uint16_t *k, const uint16_t *v,
                      const uint8_t *ck, const uint8_t *cv,
                      const uint16_t *zk, const uint16_t *sk,
-                     const uint16_t *zv, const uint16_t *sv,
+                     const uint16_t *zv, const uint16_t *sv, const float *lk, const float *lv,
                      int n_ranges, const int *lo, const int *hi,
                      double *m2_out, double *l_out, double *acc_out) {
-    ora_cache_t c = {D, T, sink, h_end, g, k, v, ck, cv, zk, sk, zv, sv};
+    ora_cache_t c = {D, T, sink, h_end, g, k, v, ck, cv, zk, sk, zv, sv, lk, lv};
     const double log2e = 1.0 / log(2.0);
     double *qd = (double *)malloc(sizeof(double) * D);
     double *qr = (double *)malloc(sizeof(double) * D);
