@@ -28,7 +28,8 @@ class OscarError(RuntimeError):
 
 class LayoutC(ctypes.Structure):
     _fields_ = [("head_dim", i32), ("n_kv_heads", i32), ("gqa", i32), ("page_size", i32),
-                ("group", i32), ("sink", i32), ("recent", i32)]
+                ("group", i32), ("sink", i32), ("recent", i32),
+                ("levels_k", ctypes.c_float * 4), ("levels_v", ctypes.c_float * 4)]
 
 
 class Int2PoolC(ctypes.Structure):
@@ -143,14 +144,20 @@ class Layout:
     sink: int = 64
     recent: int = 256
     head_dim: int = 128
+    levels_k: Optional[tuple] = None    # key codebook (4 increasing levels), None = uniform
+    levels_v: Optional[tuple] = None    # value codebook
 
     @property
     def n_q_heads(self) -> int:
         return self.n_kv_heads * self.gqa
 
     def c(self) -> LayoutC:
-        return LayoutC(self.head_dim, self.n_kv_heads, self.gqa, self.page_size, self.group, self.sink,
-                       self.recent)
+        lay = LayoutC(self.head_dim, self.n_kv_heads, self.gqa, self.page_size, self.group, self.sink,
+                      self.recent)
+        if self.levels_k is not None or self.levels_v is not None:
+            lay.levels_k = (ctypes.c_float * 4)(*[float(x) for x in self.levels_k])
+            lay.levels_v = (ctypes.c_float * 4)(*[float(x) for x in self.levels_v])
+        return lay
 
 
 @dataclasses.dataclass

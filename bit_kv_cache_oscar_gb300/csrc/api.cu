@@ -2,6 +2,7 @@
 // to the kernels.  Declarations and contracts: include/oscar.h.
 
 #include <atomic>
+#include <cmath>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -66,6 +67,12 @@ oscar_status_t check_layout(const oscar_layout_t *L) {
         return fail(OSCAR_ERR_INVALID_ARG, "sink %d must be >= 0 and a multiple of page_size %d", L->sink,
                     L->page_size);
     if (L->recent < 0) return fail(OSCAR_ERR_INVALID_ARG, "recent %d < 0", L->recent);
+    if (!oscar::uniform_codebook(*L)) {
+        for (const float *lv : {L->levels_k, L->levels_v})
+            for (int k = 0; k < 4; ++k)
+                if (!std::isfinite(lv[k]) || (k > 0 && !(lv[k] > lv[k - 1])))
+                    return fail(OSCAR_ERR_INVALID_ARG, "codebook levels must be finite and strictly increasing");
+    }
     return OSCAR_OK;
 }
 
@@ -226,6 +233,9 @@ oscar_status_t oscar_demote_range(const oscar_layout_t *layout, const oscar_bf16
     if (!oscar::demote_range_supported(*layout))
         return fail(OSCAR_ERR_UNSUPPORTED, "page_size %d neither divides nor is a multiple of 128",
                     layout->page_size);
+    if (!oscar::uniform_codebook(*layout))
+        return fail(OSCAR_ERR_UNSUPPORTED, "the tensor-core bulk demotion quantizes to the uniform levels only; "
+                                           "use oscar_demote");
     return cuda_status(oscar::launch_demote_range(*layout, bf16_view(src), bf16_page_table, *dst, int2_page_table,
                                                   max_pages_per_req, batch, pos_begin, pos_end, R_K, R_V, c_K, c_V,
                                                   rotated_out, status_ptr(), (cudaStream_t)stream),
@@ -308,7 +318,8 @@ oscar_status_t oscar_decode_attention_fused(const oscar_layout_t *layout, const 
     if (!aligned16(q) || !aligned16(R_K)) return fail(OSCAR_ERR_INVALID_ARG, "q/R_K not 16-byte aligned");
     if (max_pages_per_req < 1) return fail(OSCAR_ERR_INVALID_ARG, "max_pages_per_req %d < 1", max_pages_per_req);
     if (!oscar::int2_mma_supported(*layout))
-        return fail(OSCAR_ERR_UNSUPPORTED, "fused rotation needs 1, 2, 4 or 8 kv heads; use oscar_rotate_q + "
+        return fail(OSCAR_ERR_UNSUPPORTED, "fused rotation needs 1, 2, 4 or 8 kv heads and the uniform codebook; "
+                                           "use oscar_rotate_q + "
                                            "oscar_decode_attention");
     oscar::FusedDemotion dem{};
     if (!aligned16(R_V)) return fail(OSCAR_ERR_INVALID_ARG, "R_V not 16-byte aligned");

@@ -1954,7 +1954,8 @@ int int2_mma_window_clusters(const oscar_layout_t &L, int batch) { return L.n_kv
 
 bool int2_mma_supported(const oscar_layout_t &L) {
     const int H = L.n_kv_heads;
-    return (H == 1 || H == 2 || H == 4 || H == 8) && L.head_dim == kHeadDim;
+    // (the code-as-f16-subnormal operands hold the uniform levels only)
+    return (H == 1 || H == 2 || H == 4 || H == 8) && L.head_dim == kHeadDim && uniform_codebook(L);
 }
 
 static cudaError_t decode_mma_impl(const oscar_layout_t &L, const float *RK, Int2PoolView pool, const int32_t *pt,

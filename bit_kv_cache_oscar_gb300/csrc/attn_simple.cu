@@ -102,7 +102,13 @@ struct Int2Args {
     float scale2;
     PartialsView out;
     int32_t *status;
+    float4 lk, lv;           // codebook levels of keys and values (0, 1, 2, 3: uniform)
 };
+
+// level of a 2-bit code
+__device__ __forceinline__ float code_level(const float4 &l, uint32_t c) {
+    return (c & 2u) ? ((c & 1u) ? l.w : l.z) : ((c & 1u) ? l.y : l.x);
+}
 
 template <int G>
 __global__ void __launch_bounds__(128) int2_split_kernel(Int2Args a) {
@@ -141,8 +147,8 @@ __global__ void __launch_bounds__(128) int2_split_kernel(Int2Args a) {
         float kh[4], vh[4];
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
-            kh[c] = fmaf((float)((ck >> (2 * c)) & 3u), sk, zk);
-            vh[c] = fmaf((float)((cv >> (2 * c)) & 3u), sv, zv);
+            kh[c] = fmaf(code_level(a.lk, (ck >> (2 * c)) & 3u), sk, zk);
+            vh[c] = fmaf(code_level(a.lv, (cv >> (2 * c)) & 3u), sv, zv);
         }
         float part[G];
 #pragma unroll
@@ -255,7 +261,7 @@ cudaError_t launch_int2_attention(const oscar_layout_t &L, const float *q_rot, I
         return launch_decode_mma(L, q_rot, nullptr, pool, pt, nullptr, Bf16PoolView{nullptr, nullptr, 0}, nullptr,
                                  max_pages, seq_len, hist_end, batch, sm_scale, out, status, true, false, st);
     Int2Args a{q_rot, pool, pt, max_pages, L.page_size, L.n_kv_heads, L.group, L.sink, seq_len, hist_end,
-               sm_scale * kLog2e, out, status};
+               sm_scale * kLog2e, out, status, codebook_levels(L, false), codebook_levels(L, true)};
     return launch_g<Int2Launcher>(L.gqa, dim3(out.S, L.n_kv_heads, batch), a, st);
 }
 

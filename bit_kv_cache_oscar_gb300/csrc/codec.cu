@@ -28,9 +28,9 @@ constexpr int kTokPerCta = 256;      // rows per CTA before the grid grows
 // Quantize one row held one channel per thread (thread j = channel j of a 128-thread CTA).
 __device__ __forceinline__ void quantize_row_store(float y, float clip, int group, bool store,
                                                    uint8_t *codes_row, uint16_t *scale_row,
-                                                   uint16_t *zero_row, float *red) {
+                                                   uint16_t *zero_row, float *red, bool cb, float4 lv) {
     oscar::quantize_row_store(y, clip, group, store, codes_row, scale_row, zero_row, red, (int)threadIdx.x,
-                              [] { __syncthreads(); });
+                              [] { __syncthreads(); }, cb, lv);
 }
 
 struct DemoteArgs {
@@ -44,6 +44,8 @@ struct DemoteArgs {
     int n;
     const float *RK, *RV;
     float cK, cV;
+    bool cb;                 // non-uniform codebooks lk (keys), lv (values)
+    float4 lk, lv;
     float *rot_out;
     int32_t *status;
 };
@@ -133,20 +135,21 @@ __global__ void __launch_bounds__(kThreads) demote_kernel(DemoteArgs a) {
             if (a.rot_out) a.rot_out[(((size_t)(base + t) * 2 + which) * a.n_kv + h) * kHeadDim + j] = acc[t];
             const size_t r = drow < 0 ? 0 : (size_t)drow;
             quantize_row_store(acc[t], clip, a.group, drow >= 0, codes + r * (kHeadDim / 4),
-                               scale + r * gpr, zero + r * gpr, red);
+                               scale + r * gpr, zero + r * gpr, red, a.cb, which ? a.lv : a.lk);
         }
     }
 }
 
 __global__ void __launch_bounds__(kThreads) quantize_rows_kernel(const float *x, int n, float clip, int group,
-                                                                 uint8_t *codes, uint16_t *scale, uint16_t *zero) {
+                                                                 uint8_t *codes, uint16_t *scale, uint16_t *zero,
+                                                                 bool cb, float4 lv) {
     __shared__ float red[8];
     const int r = blockIdx.x;
     if (r >= n) return;
     const int gpr = kHeadDim / group;
     const float y = x[(size_t)r * kHeadDim + threadIdx.x];
     quantize_row_store(y, clip, group, true, codes + (size_t)r * (kHeadDim / 4), scale + (size_t)r * gpr,
-                       zero + (size_t)r * gpr, red);
+                       zero + (size_t)r * gpr, red, cb, lv);
 }
 
 // grid.x = batch * n_kv * 4 (a quarter of the 128 output channels per CTA), 32*G threads;
@@ -210,6 +213,9 @@ cudaError_t launch_demote(const oscar_layout_t &L, Bf16PoolView src, const int32
     a.RV = RV;
     a.cK = cK;
     a.cV = cV;
+    a.cb = !uniform_codebook(L);
+    a.lk = codebook_levels(L, false);
+    a.lv = codebook_levels(L, true);
     a.rot_out = rot_out;
     a.status = status;
     const size_t smem = sizeof(float) * (kHeadDim * kHeadDim + kTokPerPass * kHeadDim + 8) + sizeof(int) * kTokPerPass;
@@ -222,7 +228,8 @@ cudaError_t launch_demote(const oscar_layout_t &L, Bf16PoolView src, const int32
 cudaError_t launch_quantize_rotated(const oscar_layout_t &L, const float *x, int n, float clip, uint8_t *codes,
                                     uint16_t *scale, uint16_t *zero, cudaStream_t st) {
     if (n <= 0) return cudaSuccess;
-    quantize_rows_kernel<<<n, kThreads, 0, st>>>(x, n, clip, L.group, codes, scale, zero);
+    quantize_rows_kernel<<<n, kThreads, 0, st>>>(x, n, clip, L.group, codes, scale, zero, !uniform_codebook(L),
+                                                 codebook_levels(L, false));
     return cudaGetLastError();
 }
 

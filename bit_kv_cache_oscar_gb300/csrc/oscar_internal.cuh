@@ -143,6 +143,19 @@ cudaError_t launch_int2_attention(const oscar_layout_t &L, const float *q_rot, I
 
 // Tensor-core INT2 kernel (n_kv_heads in {1, 2, 4, 8}); launch_int2_attention dispatches to it.
 bool int2_mma_supported(const oscar_layout_t &L);
+
+// The layout's codebooks: all levels zero = uniform (levels 0, 1, 2, 3).
+inline bool uniform_codebook(const oscar_layout_t &L) {
+    for (int k = 0; k < 4; ++k)
+        if (L.levels_k[k] != 0.0f || L.levels_v[k] != 0.0f) return false;
+    return true;
+}
+// The levels a kernel uses (0, 1, 2, 3 for the uniform codebook).
+inline float4 codebook_levels(const oscar_layout_t &L, bool values) {
+    if (uniform_codebook(L)) return make_float4(0.f, 1.f, 2.f, 3.f);
+    const float *l = values ? L.levels_v : L.levels_k;
+    return make_float4(l[0], l[1], l[2], l[3]);
+}
 // Window clusters (the BF16 sink/recent part) per request of the tensor-core INT2 kernel: two for
 // a single request with 8 kv heads (four heads each: a window CTA's rows then fit its buffers in
 // one round trip), else one (with more requests the history clusters need the CTA slots).

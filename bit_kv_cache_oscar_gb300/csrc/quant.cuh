@@ -6,6 +6,9 @@
 // zero = bf16(lo), scale = bf16((hi - lo)/3), code = clamp(rint((y - zero)/scale), 0, 3)
 // with the stored bf16 zero and scale, code 0 when scale = 0; code i of the row sits at
 // bits 2*(i mod 4) of byte i/4.  Explicit round-to-nearest intrinsics fix every rounding.
+// With a non-uniform codebook lv (cb = true; OSCAR news article, closing paragraph on the
+// Lloyd-Max codebook) the zero and scale are the same and the code is the number of fp32
+// midpoints (lv[k] + lv[k+1]) * 0.5 at or below u = (y - zero)/scale (code 0 for NaN or scale 0).
 #pragma once
 
 #include "oscar_internal.cuh"
@@ -18,7 +21,7 @@ namespace oscar {
 template <typename Sync>
 __device__ __forceinline__ void quantize_row_store(float y, float clip, int group, bool store, uint8_t *codes_row,
                                                    uint16_t *scale_row, uint16_t *zero_row, float *red, int j,
-                                                   Sync sync) {
+                                                   Sync sync, bool cb = false, float4 lv = float4{}) {
     const int lane = j & 31, warp = j >> 5;
     float mn = y, mx = y;
 #pragma unroll
@@ -52,8 +55,15 @@ __device__ __forceinline__ void quantize_row_store(float y, float clip, int grou
     const float z = bf16_to_f32(zb), s = bf16_to_f32(sb);
     int c = 0;
     if (s != 0.0f) {
-        const float r = rintf(__fdiv_rn(__fsub_rn(y, z), s));
-        c = r >= 3.0f ? 3 : (r >= 0.0f ? (int)r : 0);
+        const float u = __fdiv_rn(__fsub_rn(y, z), s);
+        if (cb) {
+            const float t0 = __fmul_rn(__fadd_rn(lv.x, lv.y), 0.5f), t1 = __fmul_rn(__fadd_rn(lv.y, lv.z), 0.5f);
+            const float t2 = __fmul_rn(__fadd_rn(lv.z, lv.w), 0.5f);
+            c = (u >= t0) + (u >= t1) + (u >= t2);
+        } else {
+            const float r = rintf(u);
+            c = r >= 3.0f ? 3 : (r >= 0.0f ? (int)r : 0);
+        }
     }
     uint32_t v = (uint32_t)c << (2 * (lane & 3));
     v |= __shfl_xor_sync(0xffffffffu, v, 1);

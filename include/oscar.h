@@ -95,6 +95,20 @@ typedef struct {
     int32_t group;
     int32_t sink;
     int32_t recent;
+    /*
+     * Codebook of the 2-bit codes on a group's normalised axis u = (x - zero) / scale, where
+     * zero and scale are the uniform quantizer's (zero = bf16(c·min), scale = bf16((c·max -
+     * c·min) / 3)).  All four zero: the uniform levels 0, 1, 2, 3 (code = clamp(rint(u), 0, 3)).
+     * Otherwise four finite, strictly increasing levels lv (a non-uniform codebook such as a
+     * Lloyd-Max one, OSCAR news article, closing paragraph): code = the number of fp32 midpoints
+     * (lv[k] + lv[k+1]) * 0.5 at or below u (code 0 for NaN or scale 0), restored as
+     * zero + lv[code] · scale.  levels_k for keys, levels_v for values.  A non-uniform codebook is
+     * served by oscar_quantize_rotated (with levels_k), oscar_demote, oscar_decode_attention and
+     * oscar_decode_attention_noalloc (their INT2 part on the CUDA cores); the tensor-core-only
+     * paths (oscar_decode_attention_fused, oscar_demote_range) return OSCAR_ERR_UNSUPPORTED.
+     */
+    float levels_k[4];
+    float levels_v[4];
 } oscar_layout_t;
 
 /*

@@ -55,10 +55,12 @@ class Case:
 
 
 def make_case(n_kv=2, gqa=4, page_size=16, group=128, seq=(1024,), seed=0, layer=0, hist_end=None,
-              sink=64, recent=256, device="cuda", gen_device="cpu", shared_prefix=0) -> Case:
+              sink=64, recent=256, device="cuda", gen_device="cpu", shared_prefix=0, levels=None) -> Case:
     """gen_device="cuda" draws K/V on the GPU (long contexts); both sides still get the same
-    tensors (the oracle reads the sampled heads back)."""
-    layout = ob.Layout(n_kv, gqa, page_size, group, sink, recent)
+    tensors (the oracle reads the sampled heads back).  levels: (key, value) codebooks."""
+    lk, lv = (None, None) if levels is None else (tuple(float(x) for x in levels[0]),
+                                                   tuple(float(x) for x in levels[1]))
+    layout = ob.Layout(n_kv, gqa, page_size, group, sink, recent, levels_k=lk, levels_v=lv)
     prof, RK, RV = oracle_rotations(seed, layer, n_kv, gqa)
     w = syn.Workload("case", 1, n_kv * gqa, n_kv, len(seq), max(seq), page_size, group=group,
                      sink=sink, recent=recent, seed=seed, shared_prefix=shared_prefix)
@@ -173,9 +175,11 @@ def oracle_head_cache(case: Case, b: int, h: int) -> oracle.HeadCache:
     cv = np.zeros((T, D // 4), np.uint8)
     zk, sk, zv, sv = (np.zeros((T, D // g), np.uint16) for _ in range(4))
     if he > L.sink:
-        _, ck[L.sink:he], zk[L.sink:he], sk[L.sink:he] = oracle.demote_rows(kb[L.sink:he], case.RK[h], g, oracle.C_K)
-        _, cv[L.sink:he], zv[L.sink:he], sv[L.sink:he] = oracle.demote_rows(vb[L.sink:he], case.RV[h], g, oracle.C_V)
-    return oracle.HeadCache(kb, vb, ck, cv, zk, sk, zv, sv, L.sink, he, g)
+        _, ck[L.sink:he], zk[L.sink:he], sk[L.sink:he] = oracle.demote_rows(kb[L.sink:he], case.RK[h], g, oracle.C_K,
+                                                                            levels=L.levels_k)
+        _, cv[L.sink:he], zv[L.sink:he], sv[L.sink:he] = oracle.demote_rows(vb[L.sink:he], case.RV[h], g, oracle.C_V,
+                                                                            levels=L.levels_v)
+    return oracle.HeadCache(kb, vb, ck, cv, zk, sk, zv, sv, L.sink, he, g, levels_k=L.levels_k, levels_v=L.levels_v)
 
 
 def oracle_outputs(case: Case, heads: Optional[list] = None):

@@ -63,6 +63,18 @@ def test_layout_validation_on_host(lib, field, value, msg):
     assert msg in L.oscar_last_error_string().decode()
 
 
+def test_codebook_validation_on_host(lib):
+    """A non-uniform codebook must be four finite, strictly increasing levels per tensor."""
+    L = ob.lib()
+    for bad in ((0.5, 0.4, 2.0, 3.0), (0.0, 1.0, float("nan"), 3.0), (1.0, 1.0, 2.0, 3.0)):
+        lay = ob.LayoutC(128, 8, 4, 64, 128, 64, 256)
+        lay.levels_k = (ctypes.c_float * 4)(*bad)
+        lay.levels_v = (ctypes.c_float * 4)(0.5, 1.2, 1.8, 2.5)
+        rc = L.oscar_quantize_rotated(ctypes.byref(lay), None, 1, 0.96, None, None, None, None)
+        assert rc in (1, 2)
+        assert "codebook" in L.oscar_last_error_string().decode()
+
+
 def test_null_and_range_checks_on_host(lib):
     L = ob.lib()
     lay = ob.LayoutC(128, 8, 4, 64, 128, 64, 256)
