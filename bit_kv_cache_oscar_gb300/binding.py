@@ -51,7 +51,7 @@ EXPORTS = [
     "oscar_bf16_decode_attention", "oscar_get_device_status", "oscar_last_error_string", "oscar_version",
     "oscar_decode_attention_noalloc", "oscar_decode_attention_history", "oscar_decode_attention_window",
     "oscar_set_launch_overlap", "oscar_get_launch_overlap", "oscar_decode_attention_fused",
-    "oscar_demote_range",
+    "oscar_demote_range", "oscar_decode_attention_shared_prefix",
 ]
 
 
@@ -108,6 +108,10 @@ def lib():
                                                vp, i32, ctypes.c_float, P(PartialsC), vp, vp, ctypes.c_float,
                                                ctypes.c_float, vp, vp, vp, vp, vp, vp]
     L.oscar_decode_attention_fused.restype = st
+    L.oscar_decode_attention_shared_prefix.argtypes = [P(LayoutC), vp, vp, P(Bf16PoolC), vp, P(Int2PoolC), vp,
+                                                        i32, vp, vp, i32, ctypes.c_float, i32, i32, P(PartialsC),
+                                                        vp, vp]
+    L.oscar_decode_attention_shared_prefix.restype = st
     L.oscar_set_launch_overlap.argtypes = [i32]
     L.oscar_set_launch_overlap.restype = st
     L.oscar_get_launch_overlap.argtypes = []
@@ -284,6 +288,20 @@ def oscar_decode_attention(layout: Layout, q: torch.Tensor, q_rot: torch.Tensor,
         ctypes.byref(layout.c()), _ptr(q), _ptr(q_rot), ctypes.byref(bf16_pool.c()), _ptr(bf16_page_table),
         ctypes.byref(int2_pool.c()), _ptr(int2_page_table), int(int2_page_table.shape[-1]), _ptr(seq_len),
         _ptr(hist_end), int(q.shape[0]), float(sm_scale), ctypes.byref(partials.c()), _stream(stream)))
+
+
+def oscar_decode_attention_shared_prefix(layout: Layout, q: torch.Tensor, q_rot: torch.Tensor, bf16_pool: Bf16Pool,
+                                         bf16_page_table: torch.Tensor, int2_pool: Int2Pool,
+                                         int2_page_table: torch.Tensor, seq_len: torch.Tensor, hist_end: torch.Tensor,
+                                         sm_scale: float, prefix_end: int, prefix_splits: int, partials: Partials,
+                                         tile_counters: Optional[torch.Tensor] = None, stream=None):
+    """Shared prefix [sink, prefix_end) once for the whole batch (slots 0 .. prefix_splits - 1), each
+    request's own history after it (slots prefix_splits .. S - 1) and its BF16 window (slot S)."""
+    _check("oscar_decode_attention_shared_prefix", lib().oscar_decode_attention_shared_prefix(
+        ctypes.byref(layout.c()), _ptr(q), _ptr(q_rot), ctypes.byref(bf16_pool.c()), _ptr(bf16_page_table),
+        ctypes.byref(int2_pool.c()), _ptr(int2_page_table), int(int2_page_table.shape[-1]), _ptr(seq_len),
+        _ptr(hist_end), int(q.shape[0]), float(sm_scale), int(prefix_end), int(prefix_splits),
+        ctypes.byref(partials.c()), _ptr(tile_counters), _stream(stream)))
 
 
 def oscar_decode_attention_fused(layout: Layout, q: torch.Tensor, R_K: torch.Tensor, bf16_pool: Bf16Pool,

@@ -298,6 +298,44 @@ oscar_status_t oscar_decode_attention(const oscar_layout_t *layout, const uint16
     return cuda_status(e, "BF16 sink/recent attention launch");
 }
 
+oscar_status_t oscar_decode_attention_shared_prefix(
+    const oscar_layout_t *layout, const uint16_t *q, const float *q_rot, const oscar_bf16_pool_t *bf16_pool,
+    const int32_t *bf16_page_table, const oscar_int2_pool_t *int2_pool, const int32_t *int2_page_table,
+    int32_t max_pages_per_req, const int32_t *seq_len, const int32_t *hist_end, int32_t batch, float sm_scale,
+    int32_t prefix_end, int32_t prefix_splits, const oscar_partials_t *partials, int32_t *tile_counters,
+    void *stream) {
+    TRY(check_layout(layout));
+    TRY(check_bf16_pool(bf16_pool));
+    TRY(check_int2_pool(int2_pool));
+    TRY(check_partials(partials));
+    if (batch < 0 || batch > 65535) return fail(OSCAR_ERR_INVALID_ARG, "batch %d outside 0..65535", batch);
+    if (batch == 0) return OSCAR_OK;
+    if (!q || !q_rot || !bf16_page_table || !int2_page_table || !seq_len || !hist_end)
+        return fail(OSCAR_ERR_INVALID_ARG, "NULL argument");
+    if (!aligned16(q_rot) || !aligned16(q)) return fail(OSCAR_ERR_INVALID_ARG, "q/q_rot not 16-byte aligned");
+    if (max_pages_per_req < 1) return fail(OSCAR_ERR_INVALID_ARG, "max_pages_per_req %d < 1", max_pages_per_req);
+    if (!oscar::int2_mma_supported(*layout) || layout->group != 128)
+        return fail(OSCAR_ERR_UNSUPPORTED, "the shared-prefix path needs 1, 2, 4 or 8 kv heads, the uniform "
+                                           "codebook and group 128");
+    if (prefix_end % 16 != 0 || prefix_end <= layout->sink ||
+        (long long)prefix_end > (long long)max_pages_per_req * layout->page_size)
+        return fail(OSCAR_ERR_INVALID_ARG, "prefix_end %d: a multiple of 16 in (sink, max_pages_per_req*page_size]",
+                    prefix_end);
+    if (prefix_splits < 1 || prefix_splits >= partials->n_splits)
+        return fail(OSCAR_ERR_INVALID_ARG, "prefix_splits %d outside 1..n_splits-1 (%d)", prefix_splits,
+                    partials->n_splits - 1);
+    int32_t *st = status_ptr();
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = oscar::launch_prefix_attention(*layout, q_rot, int2_view(int2_pool), int2_page_table, prefix_end,
+                                                   batch, prefix_splits, sm_scale, part_view(partials), st, s);
+    if (e != cudaSuccess) return cuda_status(e, "shared-prefix attention launch");
+    return cuda_status(oscar::launch_decode_mma_suffix(*layout, q_rot, int2_view(int2_pool), int2_page_table, q,
+                                                       bf16_view(bf16_pool), bf16_page_table, max_pages_per_req,
+                                                       seq_len, hist_end, batch, sm_scale, part_view(partials), st,
+                                                       prefix_end, prefix_splits, tile_counters, s),
+                       "suffix attention launch");
+}
+
 oscar_status_t oscar_decode_attention_fused(const oscar_layout_t *layout, const uint16_t *q, const float *R_K,
                                             const oscar_bf16_pool_t *bf16_pool, const int32_t *bf16_page_table,
                                             const oscar_int2_pool_t *int2_pool, const int32_t *int2_page_table,

@@ -122,6 +122,8 @@ struct MmaArgs {
     int csize;        // CTAs per cluster; each cluster writes one partial slot
     int res_off;      // byte offset (from the first stage) of the per-CTA result area
     int hist_ctas;    // CTAs of grid.x that take the history (after the window CTAs)
+    int hist_lo;      // the history this launch takes starts at max(hist_lo, sink) (a tile boundary)
+    int slot0;        // its splits write partial slots slot0 .. S - 1 (slots below: another launch's)
     int win_ctas;     // CTAs [0, win_ctas) of grid.x take the BF16 window (whole clusters)
     int win_heads;    // kv heads per window cluster
     const float *RK;            // non-null: history CTAs rotate q themselves (q_rot unused)
@@ -196,11 +198,6 @@ __device__ __forceinline__ void cluster_combine(const MmaArgs &a, const float *r
     }
 }
 
-__device__ __forceinline__ float ex2_approx(float x) {
-    float y;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
 
 // Fold U tokens (K/V rows kk, vv: lane l holds channels 4l..4l+3; ok[u] = token present) into
 // the online softmax (base 2) of the warp's G query heads.  The U*G per-lane partial dot
@@ -673,12 +670,14 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
         if (a.arrivals) arrive_count(a, b);
         return;
     }
-    const SplitRange r = history_split(a.sink, he, a.hist_ctas, s);   // C sub-splits per slot
+    // this launch's history: [hl, he) (hist_lo above the sink: a shared prefix another launch takes)
+    const int hl = min(max(a.hist_lo, a.sink), he);
+    const SplitRange r = history_split(hl, he, a.hist_ctas, s);       // C sub-splits per slot
     // Dynamic scheduling: the copy warps of all of b's history CTAs take units of kTilesPerStage
     // tiles of the whole history [sink, he) from a shared counter, so that CTAs that run faster
     // (an SM to themselves) take more; each stage carries its first tile (or -1: no more).
     const bool dyn = a.sched != nullptr;
-    const int hist_first = a.sink / kTileTokens;   // the history starts on a tile boundary
+    const int hist_first = hl / kTileTokens;       // the history starts on a tile boundary
     const int hist_tile_hi = (he + kTileTokens - 1) / kTileTokens;
     const int dyn_units = hist_tile_hi > hist_first ? (hist_tile_hi - hist_first + kTilesPerStage - 1) / kTilesPerStage : 0;
     const int tok_hi = dyn ? he : r.hi, tile_hi = dyn ? hist_tile_hi : r.tile_hi;
@@ -899,7 +898,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
             a.sched[gridDim.y + b] = 0;
             __threadfence();
         }
-        if (a.csize > 1) cluster_combine(a, reinterpret_cast<const float *>(stage0 + a.res_off), Hq, b, s / a.csize);
+        if (a.csize > 1) cluster_combine(a, reinterpret_cast<const float *>(stage0 + a.res_off), Hq, b, a.slot0 + s / a.csize);
         if (a.arrivals) arrive_count(a, b);
         return;
     }
@@ -1694,7 +1693,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
             const int hh = nt * 4 + t;
             if (hh < G) {
                 const int hq = h * G + hh;
-                const size_t row = ((size_t)b * Hq + hq) * S1 + s;
+                const size_t row = ((size_t)b * Hq + hq) * S1 + a.slot0 + s;
                 float *dst = to_res ? res + res_acc(Hq) + hq * kHeadDim : a.out.acc + row * kHeadDim;
 #pragma unroll
                 for (int q4 = 0; q4 < 4; ++q4)
@@ -1706,7 +1705,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
                 }
             }
         }
-        if (to_res) cluster_combine(a, res, Hq, b, s / a.csize);
+        if (to_res) cluster_combine(a, res, Hq, b, a.slot0 + s / a.csize);
         if (a.arrivals) arrive_count(a, b);
         return;
     }
@@ -1747,7 +1746,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
                 }
             }
             const int hq = h * G + hh;
-            const size_t row = ((size_t)b * Hq + hq) * S1 + s;
+            const size_t row = ((size_t)b * Hq + hq) * S1 + a.slot0 + s;
             *reinterpret_cast<float4 *>(to_res ? res + res_acc(Hq) + hq * kHeadDim + c4 : a.out.acc + row * kHeadDim + c4) =
                 make_float4(A0, A1, A2, A3);
             if (c4 == 0) {
@@ -1756,7 +1755,7 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
             }
         }
     }
-    if (to_res) cluster_combine(a, res, Hq, b, s / a.csize);
+    if (to_res) cluster_combine(a, res, Hq, b, a.slot0 + s / a.csize);
     if (a.arrivals) arrive_count(a, b);
 }
 
@@ -1911,7 +1910,7 @@ cudaError_t launch_mma(const oscar_layout_t &L, MmaArgs a, int batch, bool histo
     }
     a.csize = int2_cluster_size(reinterpret_cast<const void *>(kern), smem, kThreads);
     if (cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void *>(kern), smem)) return e;
-    a.hist_ctas = history ? a.out.S * a.csize : 0;
+    a.hist_ctas = history ? (a.out.S - a.slot0) * a.csize : 0;
     a.pf_units = 0;      // (measured slower at one, a half and two rounds of units ahead: kept off)
     a.win_ctas = window ? (L.n_kv_heads / a.win_heads) * a.csize : 0;
     if (clusters) *clusters = (a.hist_ctas + a.win_ctas) / a.csize;   // arrivals per request
@@ -1963,7 +1962,7 @@ static cudaError_t decode_mma_impl(const oscar_layout_t &L, const float *RK, Int
                                    const int32_t *seq_len, const int32_t *hist_end, int batch, float sm_scale,
                                    PartialsView out, int32_t *status, const FusedDemotion &dem, cudaStream_t st,
                                    const float *q_rot, bool history, bool window, int32_t *arrivals,
-                                   int *clusters, int32_t *sched);
+                                   int *clusters, int32_t *sched, int hist_lo = 0, int slot0 = 0);
 
 cudaError_t launch_decode_mma(const oscar_layout_t &L, const float *q_rot, const float *RK, Int2PoolView pool,
                               const int32_t *pt, const uint16_t *q, Bf16PoolView bpool, const int32_t *bpt,
@@ -1973,6 +1972,16 @@ cudaError_t launch_decode_mma(const oscar_layout_t &L, const float *q_rot, const
     FusedDemotion none{};
     return decode_mma_impl(L, RK, pool, pt, q, bpool, bpt, max_pages, seq_len, hist_end, batch, sm_scale, out, status,
                            none, st, q_rot, history, window, nullptr, nullptr, nullptr);
+}
+
+cudaError_t launch_decode_mma_suffix(const oscar_layout_t &L, const float *q_rot, Int2PoolView pool, const int32_t *pt,
+                                     const uint16_t *q, Bf16PoolView bpool, const int32_t *bpt, int max_pages,
+                                     const int32_t *seq_len, const int32_t *hist_end, int batch, float sm_scale,
+                                     PartialsView out, int32_t *status, int hist_lo, int slot0, int32_t *sched,
+                                     cudaStream_t st) {
+    FusedDemotion none{};
+    return decode_mma_impl(L, nullptr, pool, pt, q, bpool, bpt, max_pages, seq_len, hist_end, batch, sm_scale, out,
+                           status, none, st, q_rot, true, true, nullptr, nullptr, sched, hist_lo, slot0);
 }
 
 cudaError_t launch_decode_mma_demote(const oscar_layout_t &L, const float *RK, Int2PoolView pool, const int32_t *pt,
@@ -1989,10 +1998,13 @@ static cudaError_t decode_mma_impl(const oscar_layout_t &L, const float *RK, Int
                                    const int32_t *seq_len, const int32_t *hist_end, int batch, float sm_scale,
                                    PartialsView out, int32_t *status, const FusedDemotion &dem, cudaStream_t st,
                                    const float *q_rot, bool history, bool window, int32_t *arrivals,
-                                   int *clusters, int32_t *sched) {
+                                   int *clusters, int32_t *sched, int hist_lo, int slot0) {
     if (clusters) *clusters = 0;
     if (batch <= 0 || (!history && !window)) return cudaSuccess;
+    if (slot0 < 0 || slot0 >= out.S) return cudaErrorInvalidValue;
     MmaArgs a{};
+    a.hist_lo = hist_lo;
+    a.slot0 = slot0;
     if (history && window) a.arrivals = arrivals;
     if (history) a.sched = sched;
     a.RK = RK;

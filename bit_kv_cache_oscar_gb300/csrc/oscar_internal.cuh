@@ -190,6 +190,21 @@ cudaError_t launch_decode_mma_demote(const oscar_layout_t &L, const float *RK, I
 // slot is written; *clusters gets the count per request that the merge then waits for.
 // sched: NULL (fixed history splits) or int32 [2][batch], zero and left zero: the history CTAs
 // take 64-token units from a shared per-request counter)
+// The history after a shared prefix and the BF16 window, one launch: history [max(hist_lo, sink),
+// hist_end) in partial slots slot0 .. S - 1 (slots below slot0 belong to the prefix launch),
+// window in slot S; q_rot from oscar_rotate_q.
+cudaError_t launch_decode_mma_suffix(const oscar_layout_t &L, const float *q_rot, Int2PoolView pool, const int32_t *pt,
+                                     const uint16_t *q, Bf16PoolView bpool, const int32_t *bpt, int max_pages,
+                                     const int32_t *seq_len, const int32_t *hist_end, int batch, float sm_scale,
+                                     PartialsView out, int32_t *status, int hist_lo, int slot0, int32_t *sched,
+                                     cudaStream_t st);
+// Shared-prefix history partials on the 5th-generation tensor cores: every request of the batch
+// reads the INT2 pages of positions [sink, prefix_end) through the page table row `prefix_pt`; the
+// prefix is cut into `splits` token splits written to partial slots 0 .. splits - 1 of every
+// (request, query head).  Group 128 only.
+cudaError_t launch_prefix_attention(const oscar_layout_t &L, const float *q_rot, Int2PoolView pool,
+                                    const int32_t *prefix_pt, int prefix_end, int batch, int splits, float sm_scale,
+                                    PartialsView out, int32_t *status, cudaStream_t st);
 
 // Tensor-core BF16 kernel (mode 0 any n_kv_heads; mode 1 n_kv_heads in {1, 2, 4, 8}).
 bool bf16_mma_supported(const oscar_layout_t &L, int mode);

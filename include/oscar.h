@@ -340,6 +340,37 @@ OSCAR_API oscar_status_t oscar_decode_attention_fused(const oscar_layout_t *layo
                                                       void *stream);
 
 /*
+ * Decode attention partials of a batch whose requests share the INT2 history pages
+ * of a prefix [sink, prefix_end) (a radix prefix cache: "Together AI 開源 OSCAR",
+ * section 服務系統, paged and prefix-cache compatible; OSCAR news article, the
+ * paragraphs on prefix-cache hits).  The shared prefix is read once per kv head for
+ * every request, on the 5th-generation tensor cores (all requests' query rows of a
+ * kv head meet the same keys: one 128-row operand per 128 / gqa requests), and cut
+ * into prefix_splits token splits written to partial slots 0 .. prefix_splits - 1;
+ * each request's own history [prefix_end, hist_end) goes to slots prefix_splits ..
+ * S - 1 and its BF16 window [0, sink) ∪ [hist_end, seq_len) to slot S
+ * (S = partials->n_splits).  Merge with oscar_merge as usual.
+ *   q, q_rot, pools, page tables, max_pages_per_req, seq_len, hist_end, sm_scale:
+ *       as oscar_decode_attention
+ *   prefix_end     multiple of 16, sink < prefix_end <= max_pages_per_req·page_size
+ *                  (a multiple of 64 keeps the suffix's 64-token units page-aligned);
+ *                  every request's hist_end must be >= prefix_end and its INT2 page
+ *                  table row must hold the same pages for [0, prefix_end) (the prefix
+ *                  is read through request 0's row); neither is checked
+ *   prefix_splits  1 <= prefix_splits < S
+ *   tile_counters  NULL, or int32 [2·batch] zero: the suffix histories taken in dynamic
+ *                  64-token units (as oscar_decode_attention_fused)
+ * Needs the tensor-core layout (1, 2, 4 or 8 kv heads, uniform codebook) and group
+ * 128 (else OSCAR_ERR_UNSUPPORTED).
+ */
+OSCAR_API oscar_status_t oscar_decode_attention_shared_prefix(
+    const oscar_layout_t *layout, const uint16_t *q, const float *q_rot, const oscar_bf16_pool_t *bf16_pool,
+    const int32_t *bf16_page_table, const oscar_int2_pool_t *int2_pool, const int32_t *int2_page_table,
+    int32_t max_pages_per_req, const int32_t *seq_len, const int32_t *hist_end, int32_t batch, float sm_scale,
+    int32_t prefix_end, int32_t prefix_splits, const oscar_partials_t *partials, int32_t *tile_counters,
+    void *stream);
+
+/*
  * The two halves of oscar_decode_attention, for callers that run them on two
  * streams so that they overlap (they write disjoint slots of `partials`):
  * _history writes the history slots 0..S-1 from the INT2 pool and q_rot;
