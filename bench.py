@@ -243,13 +243,24 @@ class ClockSampler:
 class Model:
     """Caches, rotations and buffers of every layer for one batch (device memory)."""
 
-    def __init__(self, w: syn.Workload, device, n_splits: int, with_bf16_cache: bool, bf16_budget: bool = False):
+    def __init__(self, w: syn.Workload, device, n_splits: int, with_bf16_cache: bool, bf16_budget: bool = False,
+                 codebook: bool = False):
         import torch
         from bit_kv_cache_oscar_gb300 import binding as ob
         from bit_kv_cache_oscar_gb300 import calibrate
 
         self.w, self.dev = w, device
         L = self.L = ob.Layout(w.n_kv_heads, w.gqa, w.page_size, w.group, w.sink, w.recent)
+        if codebook:
+            # a non-uniform (Lloyd-Max) codebook designed from layer 0's rotated calibration rows
+            prof = syn.channel_profile(w.seed, 0, w.n_kv_heads)
+            qc, kc, vc = syn.calibration_set(w.seed, 0, w.gqa, prof, device=device)
+            RK0, RV0 = calibrate.rotations(qc, kc, vc, 1.0 / math.sqrt(w.head_dim))
+            lk = calibrate.codebook(torch.bmm(kc.float(), RK0), w.group, 0.96)
+            lv = calibrate.codebook(torch.bmm(vc.float(), RV0), w.group, 0.92)
+            L = self.L = ob.Layout(w.n_kv_heads, w.gqa, w.page_size, w.group, w.sink, w.recent,
+                                   levels_k=lk, levels_v=lv)
+            del qc, kc, vc
         self.seq = syn.context_lengths(w)
         self.demote = w.demote_per_step
         # With per-step demotion, attention still reads the demoted token from BF16 this step.
@@ -319,10 +330,14 @@ class Model:
                 st_table[0, :n_log] = torch.arange(n_log, dtype=torch.int32, device=device)
                 start = w.sink if b == 0 else max(w.sink, w.shared_prefix)
                 stop = int(self.hist_end[b]) + (1 if self.demote else 0)
-                if stop > start:   # the prefill's history, demoted on the tensor cores
+                if stop > start and not codebook:   # the prefill's history, demoted on the tensor cores
                     rng = torch.tensor([[start], [stop]], dtype=torch.int32, device=device)
                     ob.oscar_demote_range(L, stage, st_table, i2, self.int2_table[b:b + 1].contiguous(), rng[0],
                                           rng[1], RK, RV, 0.96, 0.92)
+                elif stop > start:                  # (a non-uniform codebook: the CUDA-core demotion)
+                    pos = torch.arange(start, stop, dtype=torch.int32, device=device)
+                    ob.oscar_demote(L, stage, st_table, i2, self.int2_table[b:b + 1].contiguous(),
+                                    torch.zeros_like(pos), pos, RK, RV, 0.96, 0.92)
                 for lp in range(n_log):
                     pg = int(self.pages.bf16_table[b, lp])
                     if pg >= 0:
@@ -360,6 +375,16 @@ class Model:
             if events is not None:
                 events[l][1].record()
             ob.oscar_merge(L, self.part, st["RV"], self.out_all[l])
+
+    def step_plain(self):
+        """The step through oscar_rotate_q + oscar_decode_attention + oscar_merge (the path a
+        non-uniform codebook takes: its INT2 history on the CUDA cores)."""
+        from bit_kv_cache_oscar_gb300 import binding as ob
+        for l, st in enumerate(self.layers):
+            ob.oscar_rotate_q(self.L, self.q_all[l], st["RK"], self.q_rot)
+            ob.oscar_decode_attention(self.L, self.q_all[l], self.q_rot, st["bf16"], self.bf16_table, st["int2"],
+                                      self.int2_table, self.seq_len, self.hist_dev, self.sm_scale, self.part)
+            ob.oscar_merge(self.L, self.part, st["RV"], self.out_all[l])
 
     def demote_step(self):
         """The per-step demotion alone: one token per request, layer and kv head (K and V)."""
@@ -624,6 +649,79 @@ def demotion_overhead(model, args, dist) -> dict:
             "bar": "step time with demotion <= 1.02 x without"}
 
 
+def range_demotion_step(model, args, dist) -> dict:
+    """The per-step demotion's rows (one position per request and layer, every kv head, K and V)
+    through the tcgen05 range kernel instead: one oscar_demote_range launch per layer over
+    [pos, pos + 1) of every request, timed alone."""
+    import torch
+    from bit_kv_cache_oscar_gb300 import binding as ob
+    end = model.dem_pos + 1
+
+    def step():
+        for st in model.layers:
+            ob.oscar_demote_range(model.L, st["bf16"], model.bf16_table, st["int2"], model.int2_table,
+                                  model.dem_pos, end, st["RK"], st["RV"], 0.96, 0.92)
+    g = capture(step)
+    t = time_graph(g, args.steps, args.warmup, dist) / args.steps
+    del g
+    return {"us_per_step": t * 1e6, "us_per_layer": t * 1e6 / model.w.layers,
+            "kernel": "oscar_demote_range (bulk_demote_kernel: TMA + tcgen05.mma into TMEM), separate launch"}
+
+
+def cascade_step(model, w, args, dist, world, fused_sec: float) -> dict:
+    """The shared prefix read once per kv head for the whole batch: per layer oscar_rotate_q,
+    oscar_decode_attention_shared_prefix (tcgen05 prefix kernel over [sink, shared_prefix) in
+    prefix_splits slots + the requests' own histories and windows), the per-step demotion through
+    oscar_demote when the workload demotes, and oscar_merge."""
+    import torch
+    from bit_kv_cache_oscar_gb300 import binding as ob
+    L = model.L
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    ps = max(1, sms // w.n_kv_heads)
+    part = ob.Partials.empty(L, w.batch, ps + model.S, model.dev)
+
+    def step():
+        for l, st in enumerate(model.layers):
+            ob.oscar_rotate_q(L, model.q_all[l], st["RK"], model.q_rot)
+            ob.oscar_decode_attention_shared_prefix(L, model.q_all[l], model.q_rot, st["bf16"], model.bf16_table,
+                                                    st["int2"], model.int2_table, model.seq_len, model.hist_dev,
+                                                    model.sm_scale, w.shared_prefix, ps, part,
+                                                    tile_counters=model.tiles)
+            if model.demote:
+                ob.oscar_demote(L, st["bf16"], model.bf16_table, st["int2"], model.int2_table, model.dem_req,
+                                model.dem_pos, st["RK"], st["RV"], 0.96, 0.92)
+            ob.oscar_merge(L, part, st["RV"], model.out_all[l])
+    g = capture(step)
+    t = time_graph(g, args.steps, args.warmup, dist)
+    del g, part
+    sec = t / args.steps
+    return {"value": job_throughput(world, w.batch, t, args.steps), "unit": "tokens/s", "ms_per_step": sec * 1e3,
+            "prefix_splits": ps, "suffix_splits": model.S, "shared_prefix_tokens": w.shared_prefix,
+            "step_vs_fused": sec / fused_sec,
+            "path": "oscar_rotate_q + oscar_decode_attention_shared_prefix + oscar_demote + oscar_merge per layer"}
+
+
+def codebook_line(args, dist, world, fused_us_per_layer: float) -> dict:
+    """The 100K workload's decode with a non-uniform (Lloyd-Max) codebook, two layers: the history
+    demoted through oscar_demote with the layout's levels, the step through oscar_rotate_q +
+    oscar_decode_attention (INT2 history on the CUDA cores) + oscar_merge."""
+    import dataclasses
+    import torch
+    w = dataclasses.replace(syn.WORKLOADS["qwen3_8b_100k"], layers=2)
+    model = Model(w, torch.device("cuda", int(os.environ.get("LOCAL_RANK", "0"))), args.splits,
+                  with_bf16_cache=False, codebook=True)
+    g = capture(model.step_plain)
+    t = time_graph(g, args.steps, args.warmup, dist) / args.steps
+    lk, lv = model.L.levels_k, model.L.levels_v
+    del g, model
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    us = t * 1e6 / w.layers
+    return {"workload": workload_text(w), "levels_k": lk, "levels_v": lv, "us_per_layer": us,
+            "uniform_fused_us_per_layer": fused_us_per_layer, "slowdown_vs_uniform": us / fused_us_per_layer,
+            "path": "INT2 history on the CUDA cores (attn_simple int2_split_kernel, codebook lookup)"}
+
+
 def workload_line(w, args, dist, world, bf16_budget: bool) -> dict:
     """tokens/s, step time and HBM roofline of one workload's decode step (and, with bf16_budget, the
     all-BF16 cache at the same HBM footprint); the per-step demotion's overhead when it demotes."""
@@ -648,6 +746,10 @@ def workload_line(w, args, dist, world, bf16_budget: bool) -> dict:
                                 "prefix once per request, unique bytes once"}}
     if model.demote:
         out["per_step_demotion"] = demotion_overhead(model, args, dist)
+        if w.batch > 1:
+            out["per_step_demotion"]["tensor_core_range_kernel"] = range_demotion_step(model, args, dist)
+    if w.shared_prefix > 0:
+        out["shared_prefix_cascade"] = cascade_step(model, w, args, dist, world, sec)
     if bf16_budget and model.bf16_full is not None:
         gb = capture(model.step_bf16)
         tb = time_graph(gb, args.steps, args.warmup, dist)
@@ -765,7 +867,8 @@ def main():
     extra = None
     if not args.no_extra and args.workload == "qwen3_8b_100k" and not args.layers:
         extra = {"target_batch32": workload_line(syn.WORKLOADS["qwen3_8b_b32_ragged"], args, dist, world, True),
-                 "ctx32k_per_step_demotion": workload_line(syn.WORKLOADS["qwen3_8b_32k"], args, dist, world, False)}
+                 "ctx32k_per_step_demotion": workload_line(syn.WORKLOADS["qwen3_8b_32k"], args, dist, world, False),
+                 "codebook_lloyd_max_100k": codebook_line(args, dist, world, 1e6 * t / args.steps / w.layers)}
         assert ob.oscar_get_device_status() == 0
 
     cpu = None

@@ -67,3 +67,35 @@ def rotations(q_cal: torch.Tensor, k_cal: torch.Tensor, v_cal: torch.Tensor, sm_
     RK = _basis(CQ) @ HP
     RV = _basis(CS) @ HP
     return RK.to(torch.float32).contiguous(), RV.to(torch.float32).contiguous()
+
+
+def codebook(x_rot: torch.Tensor, group: int, clip: float, iters: int = 300) -> tuple:
+    """A 4-level non-uniform codebook for the layout's levels_k / levels_v, designed offline from
+    rotated calibration rows x_rot [..., 128] (OSCAR news article, closing paragraph: the latest
+    codebase's Lloyd-Max codebook).  Each group of `group` channels is put on the quantizer's
+    normalised axis u = (x - c*min) / ((c*max - c*min) / 3); then Lloyd's iteration (thresholds at
+    the midpoints of adjacent levels, each level the mean of its cell, a value on a threshold in
+    the upper cell) from the quartile midpoints.  Returns four increasing floats."""
+    x = x_rot.to(torch.float64).reshape(-1, group)
+    lo = clip * x.min(dim=1, keepdim=True).values
+    hi = clip * x.max(dim=1, keepdim=True).values
+    ok = (hi > lo).squeeze(1)
+    u = ((x[ok] - lo[ok]) / ((hi[ok] - lo[ok]) / 3.0)).reshape(-1)
+    u, _ = torch.sort(u)
+    n = u.numel()
+    levels = torch.quantile(u, torch.tensor([0.125, 0.375, 0.625, 0.875], dtype=torch.float64, device=u.device))
+    csum = torch.cat([torch.zeros(1, dtype=torch.float64, device=u.device), torch.cumsum(u, 0)])
+    for _ in range(iters):
+        t = 0.5 * (levels[:-1] + levels[1:])
+        cut = torch.cat([torch.zeros(1, dtype=torch.long, device=u.device),
+                         torch.searchsorted(u, t, right=False),
+                         torch.full((1,), n, dtype=torch.long, device=u.device)])
+        cnt = (cut[1:] - cut[:-1]).to(torch.float64)
+        mean = (csum[cut[1:]] - csum[cut[:-1]]) / cnt.clamp(min=1.0)
+        new = torch.where(cnt > 0, mean, levels)
+        if torch.max(torch.abs(new - levels)).item() <= 1e-12:
+            levels = new
+            break
+        levels = new
+    return tuple(float(v) for v in levels.to(torch.float32).tolist())
+

@@ -181,8 +181,10 @@ int32_t oscar_suggest_splits(const oscar_layout_t *L, int32_t batch, int32_t max
         const int win = oscar::int2_mma_window_clusters(*L, batch);
         want = (long)batch * (1 + win) > active ? (4L * active) / batch - win : active / batch - win;
     } else {
-        // one CTA per (split, kv head): about two resident CTAs per SM
-        want = (2L * sm_count + (long)batch * L->n_kv_heads - 1) / ((long)batch * L->n_kv_heads);
+        // one 4-warp CTA per (split, kv head): about sixteen CTAs per SM (their warps take one
+        // token at a time and need many warps in flight; 100K tokens, 8 kv heads: 1152, 641 and
+        // 484 us per layer at 38, 152 and 304 splits)
+        want = (16L * sm_count + (long)batch * L->n_kv_heads - 1) / ((long)batch * L->n_kv_heads);
     }
     if (want > tiles) want = tiles;
     if (want < 1) want = 1;

@@ -543,11 +543,12 @@ __device__ void window_demote(const MmaArgs &a, float *small, uint8_t *area, int
     }
 }
 
-// ---- The same per-step demotion of kv head hk (K and V), done by the consumer warps 0..3 of a
-// history CTA before its main loop (with dynamic history units, whose sharing absorbs the delay).
-// R is read from global memory (L2: every request's demotion reads it); the stage area holds
-// the KV stream.  xs: 136 floats of free shared memory.  Threads 0..127 call this.
-__device__ void history_demote(const MmaArgs &a, float *xs, int T, int he, int b, int hk) {
+// ---- The same per-step demotion of kv head hk (K for which = 0, V for 1, from w0 to w1 - 1), done
+// by the consumer warps 0..3 of a history CTA before its main loop (with dynamic history units,
+// whose sharing absorbs the delay).  R is read from global memory (L2: every request's demotion
+// reads it); the stage area holds the KV stream.  xs: 136 floats of free shared memory.  Threads
+// 0..127 call this.
+__device__ void history_demote(const MmaArgs &a, float *xs, int T, int he, int b, int hk, int w0, int w1) {
     const int tid = threadIdx.x;
     const int Hkv = a.n_kv, ps = a.page_size;
     const int p = a.dem.dem_pos[b];
@@ -569,7 +570,7 @@ __device__ void history_demote(const MmaArgs &a, float *xs, int T, int he, int b
     const int gpr = kHeadDim / a.group;
     const size_t srow = ((size_t)sp * ps + p % ps) * Hkv + hk, drow = ((size_t)dp * ps + p % ps) * Hkv + hk;
     auto sync128 = [] { asm volatile("bar.sync 2, 128;" ::: "memory"); };
-    for (int which = 0; which < 2; ++which) {
+    for (int which = w0; which < w1; ++which) {
         const float *Rb = which ? a.dem.RV : a.RK;       // NULL R_V: values stored as they are
         sync128();                                       // the previous row's xs is consumed
         xs[tid] = bf16_to_f32((which ? a.bpool.v : a.bpool.k)[srow * kHeadDim + tid]);
@@ -995,9 +996,15 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
         }
         if (C > 1 && !mbar_wait(saddr(smem + 104), 0) && lane == 0) flag_status(a.status, OSCAR_DEV_WAIT_TIMEOUT);
     }
-    // with dynamic history units the per-step demotion of kv head s is done here, by history CTA s
-    if (a.dem.dem_pos && a.sched && a.hist_ctas >= Hkv && s < Hkv && threadIdx.x < kHeadDim)
-        history_demote(a, reinterpret_cast<float *>(smem + 128), T, he, b, s);
+    // with dynamic history units the per-step demotion is done here: K and V of kv head s by history
+    // CTA s, or, with at least 2 Hkv history CTAs, K of head s by CTA s and V by CTA Hkv + s (half
+    // the delay each)
+    if (a.dem.dem_pos && a.sched && a.hist_ctas >= Hkv && threadIdx.x < kHeadDim) {
+        const bool split = a.hist_ctas >= 2 * Hkv;
+        if (s < (split ? 2 * Hkv : Hkv))
+            history_demote(a, reinterpret_cast<float *>(smem + 128), T, he, b, s % Hkv,
+                           split ? s / Hkv : 0, split ? s / Hkv + 1 : 2);
+    }
     // rotated query element (hq, d): the previous kernel's q_rot, or this CTA's copy of the rows
     auto qrot = [&](int hq, int d) -> float {
         return a.RK ? qrot_s[hq * kQS + qs_col(d)] : a.q_rot[((size_t)b * Hq + hq) * kHeadDim + d];

@@ -163,8 +163,10 @@ OSCAR_API size_t oscar_partials_acc_floats(const oscar_layout_t *layout, int32_t
  * device keeps resident at once (from sm_count when no device is visible) and
  * W the window clusters per request, the count is A / batch - W (one wave)
  * when batch·(1 + W) <= A, else 4·A / batch - W (about four waves, so that
- * requests of different lengths finish evenly); at least one 16-token history
- * tile per split, clamped to [1, 1024].
+ * requests of different lengths finish evenly).  Layouts that the tensor-core
+ * kernel does not take (other kv-head counts, a non-uniform codebook) run one
+ * 4-warp CTA per (split, kv head): about 16·sm_count / (batch·n_kv_heads) splits.
+ * At least one 16-token history tile per split, clamped to [1, 1024].
  */
 OSCAR_API int32_t oscar_suggest_splits(const oscar_layout_t *layout, int32_t batch, int32_t max_hist_tokens,
                              int32_t sm_count);
