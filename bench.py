@@ -57,6 +57,9 @@ def parse_args():
                     help="launch every kernel after the previous one completes (no programmatic dependent launch)")
     ap.add_argument("--no-extra", action="store_true",
                     help="skip the batch-32 target configuration and the 32K per-step demotion measurements")
+    ap.add_argument("--path", choices=["fused", "shared_prefix"], default="fused",
+                    help="the step's attention call: oscar_decode_attention_fused (default) or, for workloads with "
+                         "a shared prefix, oscar_rotate_q + oscar_decode_attention_shared_prefix")
     ap.add_argument("--bf16-budget", action="store_true",
                     help="run the all-BF16 comparison at this workload's cache footprint: the largest batch of "
                          "its requests whose BF16 cache (shared-prefix pages once) fits in the HBM that the "
@@ -376,6 +379,24 @@ class Model:
                 events[l][1].record()
             ob.oscar_merge(L, self.part, st["RV"], self.out_all[l])
 
+    def step_shared_prefix(self, part, prefix_splits: int):
+        """The step with the shared prefix read once per kv head for the whole batch: per layer
+        oscar_rotate_q, oscar_decode_attention_shared_prefix (prefix slots 0 .. prefix_splits - 1,
+        the requests' own histories and windows after them), the per-step demotion through
+        oscar_demote when the workload demotes, and oscar_merge."""
+        from bit_kv_cache_oscar_gb300 import binding as ob
+        L, w = self.L, self.w
+        for l, st in enumerate(self.layers):
+            ob.oscar_rotate_q(L, self.q_all[l], st["RK"], self.q_rot)
+            ob.oscar_decode_attention_shared_prefix(L, self.q_all[l], self.q_rot, st["bf16"], self.bf16_table,
+                                                    st["int2"], self.int2_table, self.seq_len, self.hist_dev,
+                                                    self.sm_scale, w.shared_prefix, prefix_splits, part,
+                                                    tile_counters=self.tiles)
+            if self.demote:
+                ob.oscar_demote(L, st["bf16"], self.bf16_table, st["int2"], self.int2_table, self.dem_req,
+                                self.dem_pos, st["RK"], st["RV"], 0.96, 0.92)
+            ob.oscar_merge(L, part, st["RV"], self.out_all[l])
+
     def step_plain(self):
         """The step through oscar_rotate_q + oscar_decode_attention + oscar_merge (the path a
         non-uniform codebook takes: its INT2 history on the CUDA cores)."""
@@ -668,6 +689,13 @@ def range_demotion_step(model, args, dist) -> dict:
             "kernel": "oscar_demote_range (bulk_demote_kernel: TMA + tcgen05.mma into TMEM), separate launch"}
 
 
+def prefix_splits(w) -> int:
+    """Token splits of the shared-prefix kernel: one CTA per (split, kv head), one wave."""
+    import torch
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    return max(1, sms // w.n_kv_heads)
+
+
 def cascade_step(model, w, args, dist, world, fused_sec: float) -> dict:
     """The shared prefix read once per kv head for the whole batch: per layer oscar_rotate_q,
     oscar_decode_attention_shared_prefix (tcgen05 prefix kernel over [sink, shared_prefix) in
@@ -675,23 +703,9 @@ def cascade_step(model, w, args, dist, world, fused_sec: float) -> dict:
     oscar_demote when the workload demotes, and oscar_merge."""
     import torch
     from bit_kv_cache_oscar_gb300 import binding as ob
-    L = model.L
-    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
-    ps = max(1, sms // w.n_kv_heads)
-    part = ob.Partials.empty(L, w.batch, ps + model.S, model.dev)
-
-    def step():
-        for l, st in enumerate(model.layers):
-            ob.oscar_rotate_q(L, model.q_all[l], st["RK"], model.q_rot)
-            ob.oscar_decode_attention_shared_prefix(L, model.q_all[l], model.q_rot, st["bf16"], model.bf16_table,
-                                                    st["int2"], model.int2_table, model.seq_len, model.hist_dev,
-                                                    model.sm_scale, w.shared_prefix, ps, part,
-                                                    tile_counters=model.tiles)
-            if model.demote:
-                ob.oscar_demote(L, st["bf16"], model.bf16_table, st["int2"], model.int2_table, model.dem_req,
-                                model.dem_pos, st["RK"], st["RV"], 0.96, 0.92)
-            ob.oscar_merge(L, part, st["RV"], model.out_all[l])
-    g = capture(step)
+    ps = prefix_splits(w)
+    part = ob.Partials.empty(model.L, w.batch, ps + model.S, model.dev)
+    g = capture(lambda: model.step_shared_prefix(part, ps))
     t = time_graph(g, args.steps, args.warmup, dist)
     del g, part
     sec = t / args.steps
@@ -798,7 +812,14 @@ def main():
     bts = bytes_per_step(w, model.seq, model.hist_end)
 
     # headline: one-step graph replayed K times
-    g = capture(lambda: model.step())
+    if args.path == "shared_prefix":
+        if not w.shared_prefix:
+            raise SystemExit("--path shared_prefix needs a workload with a shared prefix")
+        ps = prefix_splits(w)
+        part_sp = ob.Partials.empty(model.L, w.batch, ps + model.S, model.dev)
+        g = capture(lambda: model.step_shared_prefix(part_sp, ps))
+    else:
+        g = capture(lambda: model.step())
     with ClockSampler(local) as clk:
         t = time_graph(g, args.steps, args.warmup, dist)
     ms_step = 1e3 * t / args.steps
