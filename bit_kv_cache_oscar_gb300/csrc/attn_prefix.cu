@@ -17,8 +17,11 @@
 #include <cuda_fp16.h>
 #include <cstdint>
 
+#include <cstring>
+
 #include "oscar_internal.cuh"
 #include "ptx.cuh"
+#include "tma.cuh"
 
 namespace oscar {
 namespace {
@@ -30,12 +33,13 @@ constexpr int kHalf = kOpBytes / 2;                      // one 64-column half o
 constexpr int kOffQh = 0, kOffQl = kOpBytes, kOffK = 2 * kOpBytes, kOffV = 3 * kOpBytes;
 constexpr int kOffPh = 4 * kOpBytes, kOffPl = 5 * kOpBytes;
 constexpr int kStageB = 2 * kPT * 32;                    // one tile's codes: K [128][32 B], V [128][32 B]
-constexpr int kOffStage = 6 * kOpBytes;                  // two stage buffers (tile t and t + 1)
-constexpr int kOffSzf = kOffStage + 2 * kStageB;         // two fp32 [128][4]: sk * csc, zk, sv, zv
-constexpr int kOffRed = kOffSzf + 2 * kPT * 16;          // [2 halves][128 rows] exchange of row values
+constexpr int kOffStage = 6 * kOpBytes;                  // the stage of the next tile's codes
+constexpr int kOffSzb = kOffStage + kStageB;             // tensor-map path: bf16 [4 arrays][128][8 heads]
+constexpr int kOffSzf = kOffSzb + 4 * kPT * 16;          // fp32 [128][4]: sk * csc, zk, sv, zv
+constexpr int kOffRed = kOffSzf + kPT * 16;              // [2 halves][128 rows] exchange of row values
 constexpr int kOffPages = kOffRed + 2 * kRows * 4;       // the prefix's page ids (up to kMaxPages)
 constexpr int kMaxPages = 1536;
-constexpr int kOffBar = kOffPages + kMaxPages * 4;       // mbarrier, TMEM address
+constexpr int kOffBar = kOffPages + kMaxPages * 4;       // MMA mbarrier, TMEM address, copy mbarrier, piece mask
 constexpr int kSmemP = kOffBar + 64 + 1024;
 constexpr float kNoMaxP = -0x1p100f;                     // running maximum before any logit
 constexpr int kThreadsP = 256;
@@ -62,6 +66,7 @@ __device__ __forceinline__ uint32_t pack_h2(__half lo, __half hi) {
 
 struct PrefixArgs {
     const float *q_rot;          // [B][Hq][128]
+    int tma;                     // 8 kv heads, page size 32 / 64: tiles land by tensor-map copies
     int batch, G, n_kv;
     Int2PoolView pool;
     const int32_t *pages;        // logical page -> physical page of the shared positions
@@ -73,7 +78,13 @@ struct PrefixArgs {
     int32_t *status;
 };
 
-__global__ void __launch_bounds__(kThreadsP, 1) prefix_attn_kernel(PrefixArgs a) {
+// tmaps: codes K, codes V ([rows][8 heads][32 B], box 32 B x 1 head x page rows), scale K, zero K,
+// scale V, zero V ([rows][8 heads] bf16, box 8 heads x page rows); unused when a.tma == 0.
+struct PrefixMaps {
+    CUtensorMap m[6];
+};
+
+__global__ void __launch_bounds__(kThreadsP, 1) prefix_attn_kernel(PrefixArgs a, const __grid_constant__ PrefixMaps tm) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const uint32_t sb = saddr(sm);
@@ -94,8 +105,11 @@ __global__ void __launch_bounds__(kThreadsP, 1) prefix_attn_kernel(PrefixArgs a)
         tmem_alloc(bar + 8, kTmemColsP);
         tmem_relinquish();
     }
+    const uint32_t tbar = bar + 16;              // the tile's tensor-map copies (expect-tx)
+    int *piece_ok = reinterpret_cast<int *>(sm + kOffBar + 24);    // pieces of the tile that were copied
     if (tid == 0) {
         mbar_init(bar, 1);
+        mbar_init(tbar, 1);
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     // the prefix's page ids, read once (the copies of every tile index them)
@@ -140,12 +154,12 @@ __global__ void __launch_bounds__(kThreadsP, 1) prefix_attn_kernel(PrefixArgs a)
     const uint32_t lane_base = (uint32_t)(32 * (warp & 3)) << 16;     // this warp's TMEM lane quarter
     float *red = reinterpret_cast<float *>(sm + kOffRed);              // [2][128]
 
-    // Tile t's codes into stage buffer bf (cp.async, one commit group) and this thread's two
-    // scale/zero values (array c / 128, token c % 128 for c = tid, tid + 256) into sv.
-    auto load_tile = [&](int t, int bf, uint16_t (&sv)[2]) {
+    // Tile t's codes into the stage buffer and this thread's two scale/zero values (array c / 128,
+    // token c % 128 for c = tid, tid + 256) into sv: per-thread cp.async copies and loads.
+    auto load_tile = [&](int t, uint16_t (&sv)[2]) {
         const int p0 = t * kPT;
         const int v_lo = max(a.lo, p0) - p0, v_hi = min(a.hi, p0 + kPT) - p0;
-        const uint32_t stg = sb + kOffStage + bf * kStageB;
+        const uint32_t stg = sb + kOffStage;
         for (int c = tid; c < kPT * 2; c += kThreadsP) {
             const int tk = c >> 1, p = p0 + tk, lp = p / a.page_size;
             const bool in = tk >= v_lo && tk < v_hi && lp < a.n_logical;
@@ -174,8 +188,8 @@ __global__ void __launch_bounds__(kThreadsP, 1) prefix_attn_kernel(PrefixArgs a)
             }
         }
     };
-    auto store_sz = [&](int bf, const uint16_t (&sv)[2]) {
-        float *dst = reinterpret_cast<float *>(sm + kOffSzf) + bf * kPT * 4;
+    auto store_sz = [&](const uint16_t (&sv)[2]) {
+        float *dst = reinterpret_cast<float *>(sm + kOffSzf);
 #pragma unroll
         for (int k = 0; k < 2; ++k) {
             const int c = tid + kThreadsP * k, arr = c >> 7, tk = c & (kPT - 1);
@@ -183,22 +197,73 @@ __global__ void __launch_bounds__(kThreadsP, 1) prefix_attn_kernel(PrefixArgs a)
             dst[tk * 4 + arr] = arr == 0 ? f * csc : f;
         }
     };
+    // The tensor-map path (warp 0): the tile's page pieces (pr rows each) that meet [lo, hi), six
+    // copies per piece (lane 6 k + o: piece k, o = codes K, codes V, scale K, zero K, scale V,
+    // zero V) completing on tbar; the mask of copied pieces goes to piece_ok.
+    const int pr = a.page_size < kPT ? a.page_size : kPT, npc = kPT / pr;
+    auto issue_tma = [&](int t) {
+        const int p0 = t * kPT;
+        int pg = -1;
+        if (lane < npc) {
+            const int p = p0 + lane * pr, lp = p / a.page_size;
+            if (p + pr > a.lo && p < a.hi && lp < a.n_logical) {
+                pg = pages_in_smem ? pages_s[lp] : a.pages[lp];
+                if (pg < 0 || pg >= a.pool.n_pages) {
+                    flag_status(a.status, OSCAR_DEV_BAD_INT2_PAGE);
+                    pg = -1;
+                }
+            }
+        }
+        const unsigned ok = __ballot_sync(0xffffffffu, pg >= 0);
+        const int k = lane / 6, o = lane % 6;
+        const int pgk = __shfl_sync(0xffffffffu, pg, k < npc ? k : 0);
+        if (lane == 0) {
+            *piece_ok = (int)ok;
+            mbar_arrive_expect_tx(tbar, (uint32_t)(__popc(ok) * pr * 128));
+        }
+        __syncwarp();
+        if (k < npc && ((ok >> k) & 1)) {
+            const int row0 = pgk * a.page_size;
+            if (o < 2)
+                tma_load_3d(sb + kOffStage + o * kPT * 32 + k * pr * 32, &tm.m[o], 0, h, row0, tbar);
+            else
+                tma_load_2d(sb + kOffSzb + (o - 2) * kPT * 16 + k * pr * 16, &tm.m[o], 0, row0, tbar);
+        }
+    };
 
     float m_run = kNoMaxP, l_run = 0.f, z_run = 0.f;    // l and zero sums: this half's columns
     if (ta < tb) {
-        uint16_t sv[2];
-        load_tile(ta, 0, sv);
-        store_sz(0, sv);
+        if (a.tma) {
+            if (warp == 0) issue_tma(ta);
+        } else {
+            uint16_t sv[2];
+            load_tile(ta, sv);
+            store_sz(sv);
+        }
     }
     uint32_t r0[32], r1[32];
     for (int t = ta; t < tb; ++t) {
-        const int bf = (t - ta) & 1;
         const bool first = t == ta, more = t + 1 < tb;
         const int p0 = t * kPT;
         const int v_lo = max(a.lo, p0) - p0, v_hi = min(a.hi, p0 + kPT) - p0;   // valid tokens of the tile
-        asm volatile("cp.async.wait_group 0;" ::: "memory");
-        __syncthreads();                         // tile t's codes and scale/zero are in buffer bf
-        const uint8_t *stg = sm + kOffStage + bf * kStageB;
+        if (a.tma) {
+            if (!mbar_wait(tbar, (t - ta) & 1) && lane == 0) flag_status(a.status, OSCAR_DEV_WAIT_TIMEOUT);
+            // this head's scale/zero of the tile to fp32 (zero where nothing was copied or out of range)
+            const int okm = *piece_ok;
+            const uint16_t *szb = reinterpret_cast<const uint16_t *>(sm + kOffSzb);
+            float *dst = reinterpret_cast<float *>(sm + kOffSzf);
+#pragma unroll
+            for (int k = 0; k < 2; ++k) {
+                const int c = tid + kThreadsP * k, arr = c >> 7, tk = c & (kPT - 1);
+                const bool in = tk >= v_lo && tk < v_hi && ((okm >> (tk / pr)) & 1);
+                const float f = in ? bf16_to_f32(szb[(arr * kPT + tk) * 8 + h]) : 0.f;
+                dst[tk * 4 + arr] = arr == 0 ? f * csc : f;
+            }
+        } else {
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+        }
+        __syncthreads();                         // tile t's codes and scale/zero are in place
+        const uint8_t *stg = sm + kOffStage;
         // 1. K codes -> Kc [t][k'] (8 f16 pairs per code word); warp task = (32 tokens, word W)
         for (int task = warp; task < 4 * 8; task += kThreadsP / 32) {
             const int tk = (task >> 3) * 32 + lane, W = task & 7;
@@ -222,12 +287,15 @@ __global__ void __launch_bounds__(kThreadsP, 1) prefix_attn_kernel(PrefixArgs a)
             for (int i = 0; i < 16; ++i)
                 *reinterpret_cast<uint32_t *>(sm + kOffV + sw_off(16 * W + i, t0 & ~7) + (t0 & 7) * 2) = v[i];
         }
-        // 2. tile t + 1's copies start now (its buffer held tile t - 1, consumed) and land under this tile
-        uint16_t nv[2];
-        if (more) load_tile(t + 1, bf ^ 1, nv);
+        // 2. tile t + 1's copies start once every thread is done with the stage, and land under this tile
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
+        uint16_t nv[2];
+        if (more) {
+            if (!a.tma) load_tile(t + 1, nv);
+            else if (warp == 0) issue_tma(t + 1);
+        }
         // 3. S = Q' . Kc^T (Q_hi then Q_lo, 8 K16 steps each)
         if (warp == 4 && lane == 0) {
             tc_fence_after();
@@ -245,7 +313,7 @@ __global__ void __launch_bounds__(kThreadsP, 1) prefix_attn_kernel(PrefixArgs a)
         //    through the exchange, O rescaled when it rises, p = 2^(logit - m), P' = p * sv (f16 hi/lo)
         if (!mbar_wait(bar, 0) && lane == 0) flag_status(a.status, OSCAR_DEV_WAIT_TIMEOUT);
         tc_fence_after();
-        const float *szf = reinterpret_cast<const float *>(sm + kOffSzf) + bf * kPT * 4;
+        const float *szf = reinterpret_cast<const float *>(sm + kOffSzf);
         tmem_ld32(tS + lane_base + 64 * hc, r0);
         tmem_ld32(tS + lane_base + 64 * hc + 32, r1);
         tmem_ld_wait();
@@ -330,12 +398,12 @@ __global__ void __launch_bounds__(kThreadsP, 1) prefix_attn_kernel(PrefixArgs a)
             tc_commit(bar);
         }
         // 6. the operands are rewritten by the next tile only once PV has read them; tile t + 1's
-        //    scale/zero go to the other buffer (this tile's softmax is done with its own)
-        if (more) store_sz(bf ^ 1, nv);
+        //    scale/zero (cp.async path) replace this tile's, whose softmax is done
+        if (more && !a.tma) store_sz(nv);
         if (!mbar_wait(bar, 1) && lane == 0) flag_status(a.status, OSCAR_DEV_WAIT_TIMEOUT);
         tc_fence_after();
     }
-    asm volatile("cp.async.wait_all;" ::: "memory");
+    asm volatile("cp.async.wait_all;" ::: "memory");   // (no copy is outstanding: every tile was waited on)
     // epilogue: the row's l and zero sums over both halves; acc = O * 2^24 / factor(n) + z
     red[hc * kRows + m] = l_run;
     __syncthreads();
@@ -399,9 +467,34 @@ cudaError_t launch_prefix_attention(const oscar_layout_t &L, const float *q_rot,
     a.scale2 = sm_scale * kLog2e;
     a.out = out;
     a.status = status;
+    PrefixMaps tm;
+    memset(&tm, 0, sizeof(tm));
+    a.tma = L.n_kv_heads == 8 && L.page_size >= 32;
+    if (a.tma) {
+        EncodeTiledFn fn = encode_fn();
+        const cuuint64_t rows = (cuuint64_t)pool.n_pages * L.page_size;
+        const cuuint32_t pr = (cuuint32_t)(L.page_size < kPT ? L.page_size : kPT);
+        const cuuint32_t e3[3] = {1, 1, 1}, e2[2] = {1, 1};
+        const cuuint64_t cdims[3] = {32, 8, rows}, cstr[2] = {32, 256};
+        const cuuint32_t cbox[3] = {32, 1, pr};
+        const cuuint64_t sdims[2] = {8, rows}, sstr[1] = {16};
+        const cuuint32_t sbox[2] = {8, pr};
+        const void *cbase[2] = {pool.codes_k, pool.codes_v};
+        const void *sbase[4] = {pool.scale_k, pool.zero_k, pool.scale_v, pool.zero_v};
+        bool ok = fn != nullptr;
+        for (int i = 0; ok && i < 2; ++i)
+            ok = fn(&tm.m[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(cbase[i]), cdims, cstr, cbox, e3,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+        for (int i = 0; ok && i < 4; ++i)
+            ok = fn(&tm.m[2 + i], CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void *>(sbase[i]), sdims, sstr, sbox,
+                    e2, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+        if (!ok) return cudaErrorInvalidValue;
+    }
     if (cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void *>(prefix_attn_kernel), kSmemP)) return e;
     const int groups = (batch + kRows / L.gqa - 1) / (kRows / L.gqa);
-    prefix_attn_kernel<<<dim3(splits, L.n_kv_heads, groups), kThreadsP, kSmemP, st>>>(a);
+    prefix_attn_kernel<<<dim3(splits, L.n_kv_heads, groups), kThreadsP, kSmemP, st>>>(a, tm);
     return cudaGetLastError();
 }
 
