@@ -317,7 +317,7 @@ __global__ void __launch_bounds__(kThreadsP, 1) prefix_attn_kernel(PrefixArgs a,
         tmem_ld32(tS + lane_base + 64 * hc, r0);
         tmem_ld32(tS + lane_base + 64 * hc + 32, r1);
         tmem_ld_wait();
-        float mx = -INFINITY;
+        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};   // (four chains)
 #pragma unroll
         for (int j = 0; j < 64; ++j) {
             const int tk = 64 * hc + j;
@@ -325,9 +325,9 @@ __global__ void __launch_bounds__(kThreadsP, 1) prefix_attn_kernel(PrefixArgs a,
             const float lg = fmaf(f.x, __uint_as_float(j < 32 ? r0[j] : r1[j - 32]), f.y * qz);
             const float lv = tk >= v_lo && tk < v_hi ? lg : -INFINITY;
             if (j < 32) r0[j] = __float_as_uint(lv); else r1[j - 32] = __float_as_uint(lv);
-            mx = fmaxf(mx, lv);
+            mx4[j & 3] = fmaxf(mx4[j & 3], lv);
         }
-        red[hc * kRows + m] = mx;
+        red[hc * kRows + m] = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
         __syncthreads();
         const float m_new = fmaxf(m_run, fmaxf(red[m], red[kRows + m]));
         const float alpha = ex2_approx(m_run - m_new);   // 0 on the first tile
@@ -358,6 +358,7 @@ __global__ void __launch_bounds__(kThreadsP, 1) prefix_attn_kernel(PrefixArgs a,
         l_run *= alpha;
         z_run *= alpha;
         m_run = m_new;
+        float l4[4] = {0.f, 0.f, 0.f, 0.f}, z4[4] = {0.f, 0.f, 0.f, 0.f};   // (four chains each)
 #pragma unroll
         for (int j0 = 0; j0 < 64; j0 += 8) {
             uint32_t hv[4], lw[4];
@@ -369,8 +370,8 @@ __global__ void __launch_bounds__(kThreadsP, 1) prefix_attn_kernel(PrefixArgs a,
                     const int j = j0 + 2 * u + e, tk = 64 * hc + j;
                     const float4 f = *reinterpret_cast<const float4 *>(szf + tk * 4);
                     const float p = ex2_approx(__uint_as_float(j < 32 ? r0[j] : r1[j - 32]) - m_run);
-                    l_run += p;
-                    z_run = fmaf(p, f.w, z_run);
+                    l4[j & 3] += p;
+                    z4[j & 3] = fmaf(p, f.w, z4[j & 3]);
                     pp[e] = p * f.z;
                 }
                 const __half h0 = __float2half_rn(pp[0]), h1 = __float2half_rn(pp[1]);
@@ -381,6 +382,8 @@ __global__ void __launch_bounds__(kThreadsP, 1) prefix_attn_kernel(PrefixArgs a,
             *reinterpret_cast<uint4 *>(sm + kOffPh + sw_off(m, k)) = make_uint4(hv[0], hv[1], hv[2], hv[3]);
             *reinterpret_cast<uint4 *>(sm + kOffPl + sw_off(m, k)) = make_uint4(lw[0], lw[1], lw[2], lw[3]);
         }
+        l_run += (l4[0] + l4[1]) + (l4[2] + l4[3]);
+        z_run += (z4[0] + z4[1]) + (z4[2] + z4[3]);
         fence_proxy_async_smem();
         tc_fence_before();
         __syncthreads();
