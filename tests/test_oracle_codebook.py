@@ -134,3 +134,25 @@ def test_attend_head_with_codebooks_is_textbook_attention():
     # and it differs from the same codes read with the uniform levels
     uni = oracle.HeadCache(kb, vb, ck, cv, zk, sk, zv, sv, sink, h_end, g)
     assert not np.allclose(oracle.attend_head(qb, I, I, uni, 1 / math.sqrt(D))[0], o)
+
+
+def test_product_codebook_designer_matches_the_oracle_design():
+    """The library's offline designer (calibrate.codebook, torch) on normalised Gaussian rows: its
+    levels satisfy the centroid conditions on its own sample and agree with the oracle's design
+    on an independent sample to within sampling error."""
+    import torch
+    from bit_kv_cache_oscar_gb300 import calibrate
+    g = torch.Generator().manual_seed(21)
+    x = torch.randn((8192, 128), generator=g, dtype=torch.float64)
+    lv = np.array(calibrate.codebook(x, 128, oracle.C_K), dtype=np.float64)
+    assert np.all(np.diff(lv) > 0)
+    ref = oracle.lloyd_max_codebook(oracle.C_K).astype(np.float64)
+    assert np.allclose(lv, ref, atol=2e-2), (lv, ref)
+    xs = x.numpy()
+    lo = oracle.C_K * xs.min(1, keepdims=True)
+    hi = oracle.C_K * xs.max(1, keepdims=True)
+    u = np.sort(((xs - lo) / ((hi - lo) / 3.0)).reshape(-1))
+    t = 0.5 * (lv[:-1] + lv[1:])
+    cell = np.searchsorted(t, u, side="right")
+    for k in range(4):
+        assert abs(u[cell == k].mean() - lv[k]) <= 1e-5 * max(1.0, abs(lv[k]))
