@@ -149,8 +149,9 @@ struct MmaArgs {
 __host__ __device__ constexpr int res_acc(int Hq) { return (2 * Hq + 3) & ~3; }
 __host__ __device__ constexpr int res_floats(int Hq) { return res_acc(Hq) + Hq * kHeadDim; }
 constexpr int kRec = kHeadDim + 4;   // acc [128], m, l, 2 unused
-// bytes of the receive area for n query heads (clusters of at most 8 CTAs)
-__host__ __device__ constexpr int recv_bytes(int n) { return (n + 7) * kRec * 4; }
+// bytes of the receive area for n query heads (clusters of at most 8 CTAs: at most n + 7 records)
+// and, after it, one record's room for the combine's weights (J (C + 1) <= 96 floats)
+__host__ __device__ constexpr int recv_bytes(int n) { return (n + 8) * kRec * 4; }
 
 // Cluster reduction: every CTA of a cluster holds (m, l, acc) for each query head of its
 // sub-split in `res`; CTA `rank` combines query heads hq0 + rank, hq0 + rank + C, ... (of the nhq
@@ -176,16 +177,27 @@ __device__ __forceinline__ void cluster_combine(const MmaArgs &a, const float *r
     cluster_sync_all();                 // every record is in place (no CTA reads another's memory after this)
     const size_t S1 = (size_t)a.out.S + 1;
     const int mine = (nhq - rank + C - 1) / C;
+    // per owned head j: the maximum M_j of the C sources and their weights 2^(m - M_j), once
+    // (wt[j][0] = M_j, wt[j][1 + q] = weight of source q), after the receive area
+    float *wt = recv + (size_t)(Hq + 7) * kRec;
+    for (int e = threadIdx.x; e < mine * C; e += blockDim.x) {
+        const int j = e / C, q = e % C;
+        float M = -INFINITY;
+        for (int q2 = 0; q2 < C; ++q2) M = fmaxf(M, recv[(q2 * J + j) * kRec + kHeadDim]);
+        if (q == 0) wt[j * (C + 1)] = M;
+        wt[j * (C + 1) + 1 + q] = M != -INFINITY ? exp2f(recv[(q * J + j) * kRec + kHeadDim] - M) : 0.f;
+    }
+    __syncthreads();
     for (int e = threadIdx.x; e < mine * kHeadDim; e += blockDim.x) {
         const int j = e / kHeadDim, d = e % kHeadDim, hq = hq0 + rank + j * C;
-        float M = -INFINITY;
-        for (int q = 0; q < C; ++q) M = fmaxf(M, recv[(q * J + j) * kRec + kHeadDim]);
+        const float *w = wt + j * (C + 1);
+        const float M = w[0];
         float L = 0.f, A = 0.f;
         if (M != -INFINITY) {
             for (int q = 0; q < C; ++q) {
                 const float *r = recv + (q * J + j) * kRec;
-                const float f = exp2f(r[kHeadDim] - M);
-                L = fmaf(r[kHeadDim + 1], f, L);
+                const float f = w[1 + q];
+                if (d == 0) L = fmaf(r[kHeadDim + 1], f, L);
                 A = fmaf(r[d], f, A);
             }
         }

@@ -25,12 +25,16 @@ namespace {
 
 constexpr int kPad = kHeadDim + 1;   // R_V rows padded: thread j reads row j conflict-free
 constexpr int kQuarter = kHeadDim / 4;
+constexpr int kChunk = 48;                                // history slots staged in shared memory at a time
+constexpr int kV4 = kChunk * kHeadDim / 4 / 128;          // float4 loads per thread and chunk
 
 // grid = (Hq, batch, 4 with R_V / 1 without); 128 threads.  Every CTA merges the history
 // slots of one query head for all 128 channels (thread j owns channel j); with R_V, CTA z
 // then rotates back output channels [32 z, 32 z + 32) (thread j < 32 owns channel 32 z + j)
 // from the 32 rows of R_V that it staged before waiting for the partials' producer.
-// Dynamic smem: [R_V 32 x 129 if RV] [A 128] [w S+1] [l S+1] [red 8].
+// The accumulator rows of up to kChunk slots at a time are brought into shared memory by all
+// threads with 16-byte loads, all in flight at once (the first chunk's together with m and l).
+// Dynamic smem: [R_V 32 x 129 if RV] [A 128] [X kChunk x 128] [w S+1] [l S+1] [red 8].
 __global__ void __launch_bounds__(128) merge_kernel(PartialsView p, const float *RV, int n_q_heads, int gqa,
                                                     uint16_t *out, float *out_f32, float *lse, int32_t *counters,
                                                     int expected, int batch, int32_t *status) {
@@ -39,7 +43,8 @@ __global__ void __launch_bounds__(128) merge_kernel(PartialsView p, const float 
     const int S = p.S;
     float *Rs = smem;
     float *As = smem + (RV ? kQuarter * kPad : 0);
-    float *ws = As + kHeadDim;
+    float *Xs = As + kHeadDim;
+    float *ws = Xs + kChunk * kHeadDim;
     float *ls = ws + (S + 1);
     float *red = ls + (S + 1);
     const size_t row0 = ((size_t)b * n_q_heads + hq) * (S + 1);
@@ -80,13 +85,22 @@ __global__ void __launch_bounds__(128) merge_kernel(PartialsView p, const float 
         __syncthreads();
     }
 
-    // Issue the loads of this thread's accumulator column (history slots < kPre and the BF16
-    // slot) before anything that depends on them, so that they are all in flight at once.
-    constexpr int kPre = 48;
-    const float *acc = p.acc + row0 * kHeadDim + j;
-    float xs[kPre];
+    // slots [c0, c0 + kChunk) of the accumulator rows (contiguous, 512 bytes each) -> Xs
+    const float4 *acc4 = reinterpret_cast<const float4 *>(p.acc + row0 * kHeadDim);
+    float4 xv[kV4];
+    auto load_chunk = [&](int c0) {
+        const int n4 = min(kChunk, S - c0) * (kHeadDim / 4);
 #pragma unroll
-    for (int i = 0; i < kPre; ++i) xs[i] = i < S ? acc[(size_t)i * kHeadDim] : 0.0f;
+        for (int u = 0; u < kV4; ++u)
+            if (j + 128 * u < n4) xv[u] = acc4[(size_t)c0 * (kHeadDim / 4) + j + 128 * u];
+    };
+    auto store_chunk = [&](int c0) {
+        const int n4 = min(kChunk, S - c0) * (kHeadDim / 4);
+#pragma unroll
+        for (int u = 0; u < kV4; ++u)
+            if (j + 128 * u < n4) reinterpret_cast<float4 *>(Xs)[j + 128 * u] = xv[u];
+    };
+    load_chunk(0);
     const int c = RV ? z * kQuarter + (j & (kQuarter - 1)) : j;   // output channel (threads j < 32 with R_V)
     const float xS = p.acc[(row0 + S) * kHeadDim + c];
 
@@ -100,6 +114,7 @@ __global__ void __launch_bounds__(128) merge_kernel(PartialsView p, const float 
 #pragma unroll
     for (int o = 16; o; o >>= 1) mloc = fmaxf(mloc, __shfl_xor_sync(0xffffffffu, mloc, o));
     if ((j & 31) == 0) red[j >> 5] = mloc;
+    store_chunk(0);
     __syncthreads();
     const float M = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
     for (int i = j; i <= S; i += 128) ws[i] = ls[i] > 0.0f ? exp2_taylor(__fsub_rn(ws[i], M)) : 0.0f;
@@ -107,22 +122,21 @@ __global__ void __launch_bounds__(128) merge_kernel(PartialsView p, const float 
 
     // empty slots are skipped by select: L = fma(l_i, w_i, L), A = fma(acc_i, w_i, A), i ascending
     float L = 0.0f, A = 0.0f;
-#pragma unroll
-    for (int i = 0; i < kPre; ++i) {
-        if (i < S) {
-            const float li = ls[i], w = ws[i];
+    for (int c0 = 0; c0 < S; c0 += kChunk) {
+        if (c0 > 0) {
+            __syncthreads();                     // the previous chunk is consumed
+            load_chunk(c0);
+            store_chunk(c0);
+            __syncthreads();
+        }
+        const int n = min(kChunk, S - c0);
+#pragma unroll 8
+        for (int i = 0; i < n; ++i) {
+            const float li = ls[c0 + i], w = ws[c0 + i];
             const bool on = li > 0.0f;
             L = on ? __fmaf_rn(li, w, L) : L;
-            A = on ? __fmaf_rn(xs[i], w, A) : A;
+            A = on ? __fmaf_rn(Xs[i * kHeadDim + j], w, A) : A;
         }
-    }
-#pragma unroll 8
-    for (int i = kPre; i < S; ++i) {
-        const float li = ls[i], w = ws[i];
-        const float x = acc[(size_t)i * kHeadDim];
-        const bool on = li > 0.0f;
-        L = on ? __fmaf_rn(li, w, L) : L;
-        A = on ? __fmaf_rn(x, w, A) : A;
     }
     float Ar = A;
     if (RV) {
@@ -156,7 +170,7 @@ cudaError_t launch_merge(const oscar_layout_t &L, PartialsView p, const float *R
                          int32_t *status) {
     if (batch <= 0) return cudaSuccess;
     const int hq = L.n_kv_heads * L.gqa;
-    const size_t smem = sizeof(float) * ((RV ? kQuarter * kPad : 0) + kHeadDim + 2 * (p.S + 1) + 8);
+    const size_t smem = sizeof(float) * ((RV ? kQuarter * kPad : 0) + kHeadDim + kChunk * kHeadDim + 2 * (p.S + 1) + 8);
     if (cudaError_t e = ensure_dyn_smem(reinterpret_cast<const void *>(merge_kernel), (int)smem)) return e;
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attrs[1];
