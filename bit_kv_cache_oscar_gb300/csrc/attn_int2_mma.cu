@@ -351,8 +351,10 @@ __device__ void window_cta(const MmaArgs &a, uint8_t *area, uint64_t *wbar, int 
             }
             __syncwarp();
             if (ok) {
-                tma_load_1d(saddr(dk + (size_t)lane * rowb), a.bpool.k + row * kHeadDim, rowb, saddr(&wbar[buf]));
-                tma_load_1d(saddr(dv + (size_t)lane * rowb), a.bpool.v + row * kHeadDim, rowb, saddr(&wbar[buf]));
+                // (the window rows are read once per step: evict-first in L2)
+                const uint64_t pol = l2_evict_first_policy();
+                tma_load_1d(saddr(dk + (size_t)lane * rowb), a.bpool.k + row * kHeadDim, rowb, saddr(&wbar[buf]), pol);
+                tma_load_1d(saddr(dv + (size_t)lane * rowb), a.bpool.v + row * kHeadDim, rowb, saddr(&wbar[buf]), pol);
             }
         };
         if (threadIdx.x == 0) {
@@ -837,15 +839,19 @@ __global__ void __launch_bounds__(kThreads, (G == 8 ? 1 : 2))
                 }
                 __syncwarp();
                 if (((mask >> jl) & 1) && op < 6) {
+                    // the KV stream is read once per step: evict-first in L2, so that the lines read again
+                    // (code, R_K, queries, partials) stay
+                    const uint64_t pol = l2_evict_first_policy();
                     const uint32_t d = saddr(sb) + jl * 4096;
                     if (op < 2) {
-                        tma_load_3d(d + op * off_v, one_page ? (op ? &tmv : &tmk) : (op ? &tmv1 : &tmk1), 0, 0, row0, full);
+                        tma_load_3d(d + op * off_v, one_page ? (op ? &tmv : &tmk) : (op ? &tmv1 : &tmk1), 0, 0, row0, full,
+                                    pol);
                     } else {
                         const int arr = op - 2;
                         const uint16_t *src = arr == 0 ? a.pool.scale_k : arr == 1 ? a.pool.zero_k
                                             : arr == 2 ? a.pool.scale_v : a.pool.zero_v;
                         tma_load_1d(saddr(sb + off_s) + arr * arr_bytes + jl * nsb, src + (size_t)row0 * 8 * NGRP,
-                                    one_page ? kTilesPerStage * nsb : nsb, full);
+                                    one_page ? kTilesPerStage * nsb : nsb, full, pol);
                     }
                 }
                 if (dyn) take_unit(nxt_t0, nxt_pg);
