@@ -82,28 +82,76 @@ struct TileWalk {
     }
 };
 
+// Packed fp32 pairs (sm_100 family: add / sub / mul .f32x2, each half rounded to nearest as
+// the scalar instruction would): two elements per instruction where the quantizer's steps allow.
+__device__ __forceinline__ uint64_t f2_pack(uint32_t lo, uint32_t hi) {
+    uint64_t r;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "r"(lo), "r"(hi));
+    return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t r, float &lo, float &hi) {
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_sub(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// min / max of three (the three-input forms of the sm_100 family)
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+    float d;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // The quantizer's codes of 32 channels y (one chunk of a row, inside one group of zero z, scale
 // s != 0 and inv = 1/s rounded) as two 32-bit words, code i at bits 2i.
 // Per element: q' = clamp((y - z) * inv, 0, 3), rounded to an integer (ties to even) by adding
 // 1.5 * 2^23, whose low bits are then the code.  That is clamp(rint(q), 0, 3) of the correctly
 // rounded quotient q whenever q' lies more than 2^-18 from a half-integer (|q' - q| < 2^-21 there).
 // Returns the largest distance of a q' to its integer: at kFastMargin or above, the caller takes
-// the chunk again through codes_chunk_exact.
+// the chunk again through codes_chunk_exact.  The subtractions, the product and the rounding
+// steps run on element pairs (the same roundings as one element at a time).
 __device__ __forceinline__ float codes_chunk(const uint32_t (&v)[32], float z, float inv, uint32_t &w0,
                                              uint32_t &w1) {
     constexpr float kMagic = 12582912.0f;               // 1.5 * 2^23: y = kMagic + code, bits 0x4B400000 + code
     // sum over the 16 codes of a word of bits(y) * 4^i carries 0x4B400000 * (4^16 - 1) / 3 (mod 2^32)
     // besides the codes' own sum of code * 4^i; one subtraction per word removes it
     constexpr uint32_t kBias = 0x4B400000u * 0x55555555u;
+    const uint64_t z2 = f2_pack(__float_as_uint(z), __float_as_uint(z));
+    const uint64_t inv2 = f2_pack(__float_as_uint(inv), __float_as_uint(inv));
+    const uint64_t mg2 = f2_pack(__float_as_uint(kMagic), __float_as_uint(kMagic));
     uint32_t w[2] = {0u, 0u};
     float e4[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-    for (int i = 0; i < 32; ++i) {
-        const float d = __fsub_rn(__uint_as_float(v[i]), z);
-        const float qc = fminf(fmaxf(__fmul_rn(d, inv), 0.0f), 3.0f);
-        const float y = __fadd_rn(qc, kMagic);
-        e4[i & 3] = fmaxf(e4[i & 3], fabsf(__fsub_rn(qc, __fsub_rn(y, kMagic))));
-        w[i >> 4] += __float_as_uint(y) * (1u << (2 * (i & 15)));
+    for (int i = 0; i < 32; i += 2) {
+        float q0, q1;
+        f2_unpack(f2_mul(f2_sub(f2_pack(v[i], v[i + 1]), z2), inv2), q0, q1);
+        const float c0 = fminf(fmaxf(q0, 0.0f), 3.0f), c1 = fminf(fmaxf(q1, 0.0f), 3.0f);
+        const uint64_t c2 = f2_pack(__float_as_uint(c0), __float_as_uint(c1));
+        const uint64_t y2 = f2_add(c2, mg2);
+        float y0, y1, d0, d1;
+        f2_unpack(y2, y0, y1);
+        f2_unpack(f2_sub(c2, f2_sub(y2, mg2)), d0, d1);
+        e4[i & 3] = fmaxf(e4[i & 3], fabsf(d0));
+        e4[(i + 1) & 3] = fmaxf(e4[(i + 1) & 3], fabsf(d1));
+        w[i >> 4] += __float_as_uint(y0) * (1u << (2 * (i & 15))) + __float_as_uint(y1) * (1u << (2 * ((i + 1) & 15)));
     }
     w0 = w[0] - kBias;
     w1 = w[1] - kBias;
@@ -323,16 +371,17 @@ __global__ void __launch_bounds__(kBulkThreads, 1)
             for (int c = 0; c < 4; ++c) {
                 tmem_ld32(ta + 32 * c, v);
                 tmem_ld_wait();
-                float mn4[4], mx4[4];
+                // two chains of three-input minima / maxima (a signed zero's sign is dropped below)
+                float mn2[2], mx2[2];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) mn4[u] = mx4[u] = __uint_as_float(v[u]);
+                for (int u = 0; u < 2; ++u) mn2[u] = mx2[u] = __uint_as_float(v[u]);
 #pragma unroll
-                for (int k = 4; k < 32; ++k) {
-                    mn4[k & 3] = fminf(mn4[k & 3], __uint_as_float(v[k]));
-                    mx4[k & 3] = fmaxf(mx4[k & 3], __uint_as_float(v[k]));
+                for (int k = 2; k < 32; k += 2) {
+                    mn2[(k >> 1) & 1] = fmin3(mn2[(k >> 1) & 1], __uint_as_float(v[k]), __uint_as_float(v[k + 1]));
+                    mx2[(k >> 1) & 1] = fmax3(mx2[(k >> 1) & 1], __uint_as_float(v[k]), __uint_as_float(v[k + 1]));
                 }
-                const float cmn = fminf(fminf(mn4[0], mn4[1]), fminf(mn4[2], mn4[3]));
-                const float cmx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+                const float cmn = fminf(mn2[0], mn2[1]);
+                const float cmx = fmaxf(mx2[0], mx2[1]);
 #pragma unroll
                 for (int g = 0; g < kGroups; ++g)
                     if (g == (32 * c) / GROUP) {
